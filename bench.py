@@ -1,0 +1,554 @@
+"""Benchmark of the DSA hot path on GB300: one step = indexer + top-k
+(chunked), sparse attention forward, and backward (delta, dQ/dK/dV) over one
+synthetic sequence, at S = 131072 by default.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl gb300|reference]
+
+Prints one JSON line (rank 0).  With N > 1 (torchrun) every rank runs an
+independent replica on its own GPU (weak scaling, no collective on the data
+path); the value is all ranks' tokens over the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import multiprocessing as mp
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import long_context_sparse_gb300 as dsa  # noqa: E402
+from long_context_sparse_gb300 import synth  # noqa: E402
+
+METRIC = "DSA fwd+bwd tokens/s at S=128k on 1 GB300; % of tensor/HBM roofline"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0,
+                  "bf16_tflops_sustained": 1700.0}
+
+
+# ------------------------------------------------------------ work model
+
+
+def n_full(t):
+    return (t + 1) // 4
+
+
+def keys_of_row(wl, t):
+    """|K(t)| for a full selection (random inputs select min(K_p, n_full))."""
+    sel = min(wl.K_p, n_full(t))
+    if wl.n_loc == 0:
+        return 4 * sel
+    # locals not already covered: with a full budget all 4*n_full tokens are
+    # pooled and the locals add t+1 - 4*n_full(t); otherwise up to 3 (taken
+    # as 3, the rare overlap with a selected pool ignored here)
+    if sel == n_full(t):
+        return t + 1
+    return 4 * sel + min(3, t + 1)
+
+
+def work_model(wl):
+    """Algorithmic work of one step (valid causal pairs / selected keys)."""
+    S = wl.S
+    t = np.arange(S, dtype=np.int64)
+    nf = (t + 1) // 4
+    idx_flops = float(nf.sum()) * wl.H_I * 2 * wl.D_I
+    sel = np.minimum(nf, wl.K_p)
+    if wl.n_loc == 0:
+        keys = 4 * sel
+    else:
+        keys = np.where(sel == nf, t + 1, 4 * sel + np.minimum(3, t + 1))
+    nk = float(keys.sum())
+    row_bytes = (wl.d_qk + wl.d_v) * 2
+    return {
+        "indexer_flops": idx_flops,
+        "topk_bytes": float(np.where(nf > wl.K_p, nf, 0).sum()) * 4 + S * wl.K_p * 4,
+        "fwd_flops": nk * wl.H * 2 * (wl.d_qk + wl.d_v),
+        "fwd_gather_bytes": nk * row_bytes,
+        "bwd_flops": nk * wl.H * 2 * (3 * wl.d_qk + 2 * wl.d_v),
+        "bwd_gather_bytes": nk * row_bytes,
+        "bwd_scatter_bytes": nk * (wl.d_qk + wl.d_v) * 4,
+        "keys": nk,
+    }
+
+
+def launches_per_step(wl):
+    """Kernel launches of one step, mirroring the library's host loop."""
+    C = min(wl.chunk_q, wl.S)
+    n = 1 if wl.S >= 4 else 0                   # pool
+    for t0 in range(0, wl.S, C):
+        rows = min(C, wl.S - t0)
+        if n_full(t0 + rows - 1) > wl.K_p:
+            n += 1                              # indexer chunk
+        n += 1                                  # top-k chunk
+    n += 1                                      # attention forward
+    if wl.backward:
+        n += 6                                  # delta, 2 zero, main, 2 finalize
+    return n
+
+
+# ---------------------------------------------------------------- clocks
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                 "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 8:
+                continue
+            try:
+                sm.append(float(f[0]))
+                mx = max(mx, float(f[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, f[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [],
+                    "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ CPU oracle
+
+
+_W = {}
+
+
+def _oracle_init(wl_dict, paths, scale):
+    sys.path.insert(0, ROOT)
+    import oracle
+    wl = synth.Workload(**wl_dict)
+    d = {k: np.load(v, mmap_mode="r") for k, v in paths.items()}
+    _W.update(oracle=oracle, wl=wl, d=d, scale=scale,
+              kp=oracle.pool(np.asarray(d["k_idx"])),
+              idx=np.empty((wl.S, wl.K_p), np.int32))
+
+
+def _oracle_row(i):
+    """The oracle, as it stands, on one query row of the workload:
+    index + top-k, forward and (fwd+bwd workloads) backward.  Runs in a
+    spawned worker process."""
+    o, wl, d, scale = _W["oracle"], _W["wl"], _W["d"], _W["scale"]
+    t = int(d["rows"][i])
+    r = np.array([t], np.int64)
+    sc = o.index_scores(np.asarray(d["q_idx"][i:i + 1]), _W["kp"],
+                        np.asarray(d["w"][i:i + 1]), r, wl.S)
+    _W["idx"][t] = o.topk(sc, r, wl.K_p)[0]
+    q = np.asarray(d["q"][i:i + 1])
+    o.attn_fwd(q, d["k"], d["v"], _W["idx"], wl.K_p, wl.n_loc, scale, r)
+    if wl.backward:
+        keys = o.key_set(t, wl.K_p, wl.n_loc, _W["idx"][t])
+        o.attn_bwd(q, d["k"], d["v"], np.asarray(d["dO"][i:i + 1]), _W["idx"],
+                   wl.K_p, wl.n_loc, scale, r, keys)
+    return 1
+
+
+def _np(t):
+    t = t.detach().cpu().contiguous()
+    if t.dtype == torch.bfloat16:
+        return t.view(torch.int16).numpy().view(np.uint16)
+    return t.numpy()
+
+
+def oracle_rows_data(wl, inputs, n_rows=256, seed=99):
+    """Host copies of what the oracle needs for `n_rows` late rows (last
+    S/8, the steady-state cost) of the workload: the rows' queries, weights
+    and upstream gradients, and the full K/V and indexer keys."""
+    rng = np.random.default_rng(seed)
+    lo = max(0, wl.S - max(1, wl.S // 8))
+    rows = np.sort(rng.integers(lo, wl.S, n_rows)).astype(np.int64)
+    rt = torch.from_numpy(rows).to(inputs["q"].device)
+    out = {"rows": rows, "k_idx": _np(inputs["k_idx"]), "k": _np(inputs["k"]),
+           "v": _np(inputs["v"])}
+    for k in ("q_idx", "w", "q", "dO"):
+        out[k] = _np(inputs[k][rt])
+    return out
+
+
+def run_oracle_sample(wl, data, seconds: float, cores: int):
+    """Run the oracle on rows of `data` with `cores` spawned workers until
+    about `seconds` have passed; returns (tokens_per_s, rows, cores, wall)."""
+    import dataclasses
+    import tempfile
+    tmp = tempfile.mkdtemp(prefix="dsa_oracle_")
+    paths = {}
+    for k, a in data.items():
+        paths[k] = os.path.join(tmp, k + ".npy")
+        np.save(paths[k], a)
+    scale = 1.0 / math.sqrt(wl.d_qk)
+    wl_dict = {f.name: getattr(wl, f.name) for f in dataclasses.fields(wl)}
+    n = len(data["rows"])
+    ctx = mp.get_context("spawn")
+    done, nxt = 0, 0
+    with ctx.Pool(cores, initializer=_oracle_init,
+                  initargs=(wl_dict, paths, scale)) as pool:
+        pool.map(_oracle_row, [0] * cores)       # warm the workers (untimed)
+        t0 = time.perf_counter()
+        while time.perf_counter() - t0 < seconds:
+            batch = [(nxt + j) % n for j in range(cores)]
+            nxt += cores
+            done += sum(pool.map(_oracle_row, batch))
+        wall = time.perf_counter() - t0
+    for p in paths.values():
+        os.remove(p)
+    os.rmdir(tmp)
+    return done / wall, done, cores, wall
+
+
+# ----------------------------------------------------------------- main
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def make_inputs(wl, seed, device):
+    q_idx, k_idx, w = synth.indexer_inputs(wl, seed, device)
+    q, k, v, dO = synth.attention_inputs(wl, seed, device)
+    return {"q_idx": q_idx, "k_idx": k_idx, "w": w, "q": q, "k": k, "v": v,
+            "dO": dO}
+
+
+def reference_rows_data(wl, seed, n_rows=256):
+    """Seeded synthetic data for the oracle-only arm, generated on the host
+    for the sampled rows only (same shapes and distributions)."""
+    import math as _m
+    g = torch.Generator().manual_seed(seed)
+    rng = np.random.default_rng(seed)
+    lo = max(0, wl.S - max(1, wl.S // 8))
+    rows = np.sort(rng.integers(lo, wl.S, n_rows)).astype(np.int64)
+
+    def nb(shape, std):
+        return _np((torch.randn(shape, generator=g) * std).to(torch.bfloat16))
+
+    return {"rows": rows,
+            "k_idx": nb((wl.S, wl.D_I), 1 / _m.sqrt(wl.D_I)),
+            "k": nb((wl.S, wl.d_qk), 1 / _m.sqrt(wl.d_qk)),
+            "v": nb((wl.S, wl.d_v), 1 / _m.sqrt(wl.d_v)),
+            "q_idx": nb((n_rows, wl.H_I, wl.D_I), 1 / _m.sqrt(wl.D_I)),
+            "w": torch.softmax(torch.randn((n_rows, wl.H_I), generator=g),
+                               -1).numpy(),
+            "q": nb((n_rows, wl.H, wl.d_qk), 1 / _m.sqrt(wl.d_qk)),
+            "dO": nb((n_rows, wl.H, wl.d_v), 1.0)}
+
+
+class Step:
+    """Device buffers and workspaces for one replica of the hot path."""
+
+    def __init__(self, wl, dev, inputs):
+        self.wl, self.dev = wl, dev
+        self.cfg = dsa.config_for(wl)
+        self.x = inputs
+        S, H = wl.S, wl.H
+        self.idx = torch.empty((S, wl.K_p), dtype=torch.int32, device=dev)
+        self.o = torch.empty((S, H, wl.d_v), dtype=torch.bfloat16, device=dev)
+        self.lse = torch.empty((S, H), dtype=torch.float32, device=dev)
+        self.dq = torch.empty((S, H, wl.d_qk), dtype=torch.bfloat16, device=dev)
+        self.dk = torch.empty((S, wl.d_qk), dtype=torch.bfloat16, device=dev)
+        self.dv = torch.empty((S, wl.d_v), dtype=torch.bfloat16, device=dev)
+        self.ws_i = dsa.workspace(self.cfg, dsa.WS_INDEX, dev)
+        self.ws_f = dsa.workspace(self.cfg, dsa.WS_FWD, dev)
+        self.ws_b = dsa.workspace(self.cfg, dsa.WS_BWD, dev)
+
+    def run(self, ev=None):
+        x, c = self.x, self.cfg
+        if ev is not None:
+            ev[0].record()
+        dsa.index_scores_topk(c, x["q_idx"], x["k_idx"], x["w"], out=self.idx,
+                              ws=self.ws_i)
+        if ev is not None:
+            ev[1].record()
+        dsa.sparse_attn_fwd(c, x["q"], x["k"], x["v"], self.idx, o=self.o,
+                            lse=self.lse, ws=self.ws_f)
+        if ev is not None:
+            ev[2].record()
+        if self.wl.backward:
+            dsa.sparse_attn_bwd(c, x["q"], x["k"], x["v"], self.o, self.lse,
+                                x["dO"], self.idx, dq=self.dq, dk=self.dk,
+                                dv=self.dv, ws=self.ws_b)
+        if ev is not None:
+            ev[3].record()
+
+    def outputs(self):
+        out = [self.idx, self.o, self.lse]
+        if self.wl.backward:
+            out += [self.dq, self.dk, self.dv]
+        return out
+
+    def status(self):
+        return [dsa.get_device_status(w) for w in (self.ws_i, self.ws_f,
+                                                   self.ws_b)]
+
+
+def barrier(dist_on):
+    if dist_on:
+        torch.distributed.barrier()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--workload", default="glm_chunked_s128k",
+                    choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--seq-len", type=int, default=0,
+                    help="override S (smaller runs for profiling)")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu", action="store_true")
+    args = ap.parse_args()
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    dist_on = world > 1
+    wl = synth.WORKLOADS[args.workload]
+    if args.seq_len:
+        wl = synth.scaled(wl, args.seq_len)
+    wm = work_model(wl)
+    base_cfg = {"workload": wl.name, "S": wl.S, "indexer": f"{wl.H_I}x{wl.D_I}",
+                "topk_pools": wl.K_p, "keys": wl.keys_per_query,
+                "heads": wl.H, "d_qk": wl.d_qk, "d_v": wl.d_v,
+                "chunk_q": wl.chunk_q, "passes": "fwd+bwd" if wl.backward else "fwd",
+                "replica_per_gpu": True,
+                "l2": "inputs larger than L2 (q 8 GiB, k/v 256 MiB at S=131072)"
+                      if wl.S >= 65536 else "working set may fit L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        if args.warmup < 0 or args.steps < 1:
+            raise SystemExit("bad steps")
+        cores = max(1, min(16, os.cpu_count() or 1))
+        data = reference_rows_data(wl, 20262)
+        per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
+        vals = []
+        for i in range(args.warmup + args.steps):
+            v, rows, used, wall = run_oracle_sample(wl, data, per_step, cores)
+            if i >= args.warmup:
+                vals.append((v, rows, wall))
+        value = statistics.median([v for v, _, _ in vals])
+        rows_tot = sum(r for _, r, _ in vals)
+        line = {"impl": "reference", "metric": METRIC, "value": value,
+                "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps,
+                "warmup": args.warmup,
+                "ms_per_step": 1000.0 * sum(w for _, _, w in vals) / len(vals),
+                "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+                "config": base_cfg,
+                "cpu_baseline": {"value": value, "unit": "tokens/s",
+                                 "cores": cores, "kind": "oracle",
+                                 "sample": f"{rows_tot} late query rows of the "
+                                 "workload (index+top-k+fwd+bwd per row, fp64),"
+                                 f" about {per_step:.0f} s per step"},
+                "e2e": {"value": value, "unit": "tokens/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    if dist_on:
+        torch.distributed.init_process_group("nccl")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    seed = 20262 + rank
+    inputs = make_inputs(wl, seed, dev)
+    step = Step(wl, dev, inputs)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
+           for _ in range(args.steps)]
+    for _ in range(args.warmup):
+        step.run()
+    torch.cuda.synchronize()
+    st = step.status()
+    if any(st):
+        raise SystemExit(f"device status after warm-up: {st}")
+
+    barrier(dist_on)
+    torch.cuda.synchronize()
+    start = torch.cuda.Event(enable_timing=True)
+    stop = torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        start.record()
+        for i in range(args.steps):
+            step.run(evs[i])
+        stop.record()
+        torch.cuda.synchronize()
+    barrier(dist_on)
+    ms = start.elapsed_time(stop) / args.steps
+    if any(step.status()):
+        raise SystemExit(f"device status after timed steps: {step.status()}")
+    t_idx = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
+    t_fwd = statistics.mean(e[1].elapsed_time(e[2]) for e in evs)
+    t_bwd = statistics.mean(e[2].elapsed_time(e[3]) for e in evs)
+
+    ms_max = ms
+    if dist_on:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms_max = float(tt.item())
+    value = world * wl.S / (ms_max / 1000.0)
+
+    # ---- e2e through the public API with pinned host buffers
+    e2e = None
+    if not args.no_e2e:
+        host_in = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                   for k, t in inputs.items()}
+        for k in host_in:
+            host_in[k].copy_(inputs[k])
+        host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+                    for t in step.outputs()]
+        h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+        d2h = sum(t.numel() * t.element_size() for t in host_out)
+        e_start = torch.cuda.Event(enable_timing=True)
+        e_stop = torch.cuda.Event(enable_timing=True)
+        n_e2e = max(1, min(args.steps, 3))
+
+        def one():
+            for k in host_in:
+                inputs[k].copy_(host_in[k], non_blocking=True)
+            step.run()
+            for h, d in zip(host_out, step.outputs()):
+                h.copy_(d, non_blocking=True)
+
+        one()
+        torch.cuda.synchronize()
+        barrier(dist_on)
+        e_start.record()
+        for _ in range(n_e2e):
+            one()
+        e_stop.record()
+        torch.cuda.synchronize()
+        e_ms = e_start.elapsed_time(e_stop) / n_e2e
+        if dist_on:
+            tt = torch.tensor([e_ms], device=dev)
+            torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+            e_ms = float(tt.item())
+        e2e = {"value": world * wl.S / (e_ms / 1000.0), "unit": "tokens/s",
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "ms_per_step": e_ms}
+        del host_in, host_out
+
+    if rank != 0:
+        if dist_on:
+            torch.distributed.destroy_process_group()
+        return
+
+    pk, pk_kind = peaks()
+    parts = {"index_topk_ms": t_idx, "attn_fwd_ms": t_fwd, "attn_bwd_ms": t_bwd}
+    # dominant call and its roofline (algorithmic bytes / flops per launch)
+    dom = max(parts, key=parts.get)
+    if dom == "index_topk_ms":
+        achieved = wm["indexer_flops"] / (t_idx / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved,
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "kernel": "dsa_index_scores_topk (pool + indexer + top-k)"}
+    elif dom == "attn_fwd_ms":
+        achieved = wm["fwd_gather_bytes"] / (t_fwd / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s", "kernel": "attn_fwd_kernel (gathered K/V bytes)"}
+    else:
+        achieved = wm["bwd_gather_bytes"] / (t_bwd / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
+                "unit": "GB/s",
+                "kernel": "dsa_sparse_attn_bwd call (gathered K/V bytes; "
+                          "delta + main + finalize launches)",
+                "achieved_with_scatter": (wm["bwd_gather_bytes"] +
+                                          wm["bwd_scatter_bytes"]) /
+                                         (t_bwd / 1e3) / 1e9}
+    roof["frac"] = roof["achieved"] / roof["peak"]
+    roof["traffic"] = None
+    roof["peak_source"] = pk_kind
+    aux = {
+        "indexer_tflops": wm["indexer_flops"] / (t_idx / 1e3) / 1e12,
+        "fwd_gather_gbs": wm["fwd_gather_bytes"] / (t_fwd / 1e3) / 1e9,
+        "fwd_tflops": wm["fwd_flops"] / (t_fwd / 1e3) / 1e12,
+    }
+    if wl.backward:
+        aux["bwd_gather_gbs"] = wm["bwd_gather_bytes"] / (t_bwd / 1e3) / 1e9
+        aux["bwd_tflops"] = wm["bwd_flops"] / (t_bwd / 1e3) / 1e12
+
+    line = {"metric": METRIC, "value": value, "unit": "tokens/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": ms_max, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic", "config": base_cfg,
+            "parallelism": f"replicas{world}",
+            "breakdown_ms": parts, "rates": aux,
+            "roofline": roof,
+            "clocks": clk.summary(),
+            "gpu_launches": launches_per_step(wl) * args.steps,
+            "e2e": e2e}
+
+    if not args.no_cpu:
+        cores = max(1, min(16, os.cpu_count() or 1))
+        v, rows, used, wall = run_oracle_sample(
+            wl, oracle_rows_data(wl, inputs), args.cpu_seconds, cores)
+        line["cpu_baseline"] = {
+            "value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"{rows} late query rows (last S/8) of the same workload, "
+                      "each through index+top-k+fwd+bwd in fp64, "
+                      f"{wall:.1f} s wall"}
+    print(json.dumps(line), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * dsa.h -- C ABI of the GB300 (sm_103a) DeepSeek-Sparse-Attention hot path.
+ *
+ * The method is the DSA layer of "Scaling Training to 1M Token Context on
+ * GLM-5.3-Flash" (sections "DeepSeek Sparse Attention (DSA) Optimizations",
+ * "Making Sparse Attention Actually Sparse", "Splitting the DSA Indexer"):
+ *
+ *   1. pool     k_pool[p] = mean of indexer keys 4p..4p+3 (pools of 4 tokens)
+ *   2. score    I[t,p] = sum_h w[t,h] * max(0, q_idx[t,h,:] . k_pool[p,:])
+ *               for every complete earlier pool p < n_full(t) = (t+1)/4
+ *   3. chunk    queries are scored a few hundred at a time ("Over Time:
+ *               Chunking") so the S x S/4 score matrix never exists at once
+ *   4. select   the K_p best pools per query, ties to the lower pool index,
+ *               emitted as int32 ("Across GPUs: Sharding": int32 indices)
+ *   5. attend   softmax attention of each query head over the tokens of the
+ *               selected pools (4*K_p = 2048 keys), plus, when n_local = 3,
+ *               the query's own 3 most recent tokens (2,051 keys), with one
+ *               NoPE K and one V shared by all heads
+ *   6. backward recompute P, scatter dK/dV ("MTraining: Efficient
+ *               Distributed Training for Ultra-Long Contexts via Dynamic
+ *               Sparse Attention", section 3.2: every backward GEMM depends
+ *               on the attention weights)
+ *
+ * Conventions for every entry point:
+ *  - Ownership: the caller owns every buffer, the workspace included.  The
+ *    library allocates no device or host memory and keeps no state between
+ *    calls (a per-process cache of device attributes aside).
+ *  - Pointers: device pointers unless stated.  Dense, row-major, contiguous.
+ *    Every tensor pointer must be 16-byte aligned, else DSA_ERR_MISALIGNED.
+ *  - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *    default stream).  Calls are asynchronous on that stream; argument
+ *    errors are returned before anything is launched; launch failures return
+ *    DSA_ERR_CUDA.  Errors found by a kernel (a bounded wait that ran out, an
+ *    out-of-range index) are latched in the workspace status word and read
+ *    back with dsa_get_device_status().
+ *  - No fallback: a shape the kernels do not support returns
+ *    DSA_ERR_UNSUPPORTED_SHAPE.  There is no dense or CPU path.
+ *  - bf16 = IEEE bfloat16; fp32 = IEEE binary32.
+ */
+#ifndef DSA_GB300_H
+#define DSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define DSA_ABI_VERSION 1
+
+#if defined(__GNUC__)
+#define DSA_API __attribute__((visibility("default")))
+#else
+#define DSA_API
+#endif
+
+typedef enum dsa_status {
+  DSA_OK = 0,
+  DSA_ERR_INVALID_ARG = 1,       /* null pointer, negative size, bad value */
+  DSA_ERR_UNSUPPORTED_SHAPE = 2, /* valid, but not a shape the kernels run */
+  DSA_ERR_WORKSPACE_TOO_SMALL = 3,
+  DSA_ERR_MISALIGNED = 4,        /* a pointer is not 16-byte aligned */
+  DSA_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed */
+  DSA_ERR_DEVICE_TIMEOUT = 6,    /* a kernel's bounded wait ran out */
+  DSA_ERR_DEVICE_BAD_INDEX = 7,  /* a kernel read an out-of-range pool index */
+  DSA_ERR_SCRATCH_CAP = 8        /* one score chunk would exceed scratch_cap */
+} dsa_status_t;
+
+/* Problem description (one sequence per call; batch = 1).
+ * Layout is fixed for foreign callers: 56 bytes, natural alignment. */
+typedef struct dsa_config {
+  int64_t seq_len;     /* S >= 1 */
+  int32_t pool_size;   /* tokens per pool; must be 4 */
+  int32_t topk_pools;  /* K_p, selected pools per query: 1..2048 */
+  int32_t n_local;     /* 0 (4*K_p keys) or 3 (4*K_p + 3 keys) */
+  int32_t idx_heads;   /* H_I in {1,2,4,8,16,32,64} */
+  int32_t idx_dim;     /* D_I in {64,128} */
+  int32_t attn_heads;  /* H, 1..128 */
+  int32_t d_qk;        /* NoPE q/k dim in {64,128,256,512} */
+  int32_t d_v;         /* must equal d_qk */
+  int32_t chunk_q;     /* C, queries scored per indexer chunk, >= 1 */
+  float sm_scale;      /* softmax scale; 0 -> 1/sqrt(d_qk) */
+  uint64_t scratch_cap;/* max bytes of one [C, ld] fp32 score chunk */
+} dsa_config_t;
+
+/* Workspace kinds for dsa_workspace_size(). */
+#define DSA_WS_INDEX 0 /* dsa_index_scores_topk */
+#define DSA_WS_FWD 1   /* dsa_sparse_attn_fwd */
+#define DSA_WS_BWD 2   /* dsa_sparse_attn_bwd */
+#define DSA_WS_STATUS 3 /* dsa_index_scores, dsa_topk_from_scores */
+
+/* Bytes of device workspace the call `which` needs for `cfg`.  Every
+ * workspace begins with a 256-byte header holding the device status word;
+ * zero it once with dsa_workspace_init() before first use. */
+DSA_API dsa_status_t dsa_workspace_size(const dsa_config_t* cfg, int32_t which,
+                                size_t* bytes);
+
+/* Zero the workspace header (status word) on `stream`. */
+DSA_API dsa_status_t dsa_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Step 1 alone.  k_idx [S, D_I] bf16 -> k_pool [S/4, D_I] bf16.
+ * k_pool[p,d] = bf16_rne(((k[4p,d] + k[4p+1,d]) + (k[4p+2,d] + k[4p+3,d]))
+ *               * 0.25) in fp32.  The S mod 4 trailing tokens form no pool. */
+DSA_API dsa_status_t dsa_pool_keys(const dsa_config_t* cfg, const void* k_idx,
+                           void* k_pool, void* stream);
+
+/* Step 2 for one block of queries t0 .. t0+rows-1 (rows <= 4096):
+ *   scores[r*ld + p] = I[t0 + r, p]  (fp32, tensor-core bf16 products,
+ *   fp32 accumulation) for p < n_full(t0 + r).  Entries with p >= n_full(t)
+ *   and p < ld may be overwritten with unspecified values.
+ * q_idx [S, H_I, D_I] bf16; k_pool [S/4, D_I] bf16; w [S, H_I] fp32;
+ * ld >= n_full(t0+rows-1), ld % 4 == 0.  ws: DSA_WS_STATUS. */
+DSA_API dsa_status_t dsa_index_scores(const dsa_config_t* cfg, const void* q_idx,
+                              const void* k_pool, const float* w, int64_t t0,
+                              int64_t rows, float* scores, int64_t ld,
+                              void* ws, size_t ws_bytes, void* stream);
+
+/* Step 4 alone (the bit-exact selection check).  Row r of scores [rows, ld]
+ * fp32 belongs to query t = row0 + r; its candidates are entries
+ * 0 .. n_full(t)-1.  topk_idx[r*K_p ..] receives the min(K_p, n_full(t))
+ * best pools (larger score first, equal scores -> lower pool index; -0.0 ==
+ * +0.0) in ascending pool order, then -1.  Scores must not be NaN.
+ * ws: DSA_WS_STATUS. */
+DSA_API dsa_status_t dsa_topk_from_scores(const dsa_config_t* cfg,
+                                  const float* scores, int64_t ld,
+                                  int64_t row0, int64_t rows,
+                                  int32_t* topk_idx, void* ws,
+                                  size_t ws_bytes, void* stream);
+
+/* Steps 1-4: pool, then per chunk of C queries score and select.
+ * q_idx [S, H_I, D_I] bf16, k_idx [S, D_I] bf16, w [S, H_I] fp32 ->
+ * topk_idx [S, K_p] int32 (as dsa_topk_from_scores).  The workspace holds
+ * the pooled keys and one [C, ld] fp32 score chunk (ld = S/4 rounded up to
+ * 128); C * ld * 4 > scratch_cap returns DSA_ERR_SCRATCH_CAP.
+ * ws: DSA_WS_INDEX. */
+DSA_API dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg,
+                                   const void* q_idx, const void* k_idx,
+                                   const float* w, int32_t* topk_idx,
+                                   void* ws, size_t ws_bytes, void* stream);
+
+/* Step 5, forward.  For every query t and head h, over the key set K(t):
+ *   O[t,h]   = sum_j softmax_j(scale * q[t,h] . k_j) v_j
+ *   LSE[t,h] = log sum_j exp(scale * q[t,h] . k_j)      (natural log)
+ * K(t) = tokens 4p..4p+3 of every selected pool (topk_idx[t,:] >= 0, each
+ * must be < n_full(t), else DSA_ERR_DEVICE_BAD_INDEX is latched and the row
+ * skips that pool), plus {t-2, t-1, t} clipped to >= 0 when n_local = 3, each
+ * token counted once.  An empty K(t) gives O = 0 and LSE = -inf.
+ * q [S, H, d_qk], k [S, d_qk], v [S, d_v] bf16; topk_idx [S, K_p] int32 ->
+ * o [S, H, d_v] bf16, lse [S, H] fp32.  ws: DSA_WS_FWD. */
+DSA_API dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q,
+                                 const void* k, const void* v,
+                                 const int32_t* topk_idx, void* o, float* lse,
+                                 void* ws, size_t ws_bytes, void* stream);
+
+/* Step 6, backward of step 5 for upstream gradient dO [S, H, d_v] bf16, with
+ * o and lse from dsa_sparse_attn_fwd on the same inputs:
+ *   P = exp(scale q.k_j - LSE), dP = dO . v_j, delta = dO . O,
+ *   dS = P (dP - delta), dq = scale sum_j dS k_j,
+ *   dk_j = scale sum_{t,h} dS q[t,h], dv_j = sum_{t,h} P dO[t,h].
+ * dk/dv are accumulated in fp32 in the workspace and written once as bf16.
+ * dq [S, H, d_qk], dk [S, d_qk], dv [S, d_v] bf16 are overwritten.
+ * ws: DSA_WS_BWD. */
+DSA_API dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q,
+                                 const void* k, const void* v, const void* o,
+                                 const float* lse, const void* dO,
+                                 const int32_t* topk_idx, void* dq, void* dk,
+                                 void* dv, void* ws, size_t ws_bytes,
+                                 void* stream);
+
+/* Synchronise `stream`, read the workspace status word into *device_status
+ * (a dsa_status_t value, DSA_OK if nothing was latched) and clear it. */
+DSA_API dsa_status_t dsa_get_device_status(void* ws, void* stream,
+                                   uint32_t* device_status);
+
+/* Static, human-readable name of a status code. */
+DSA_API const char* dsa_status_string(dsa_status_t status);
+
+/* DSA_ABI_VERSION of the loaded library. */
+DSA_API int32_t dsa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DSA_GB300_H */

@@ -1,0 +1,347 @@
+"""GB300-native DeepSeek-Sparse-Attention hot path.
+
+Thin ctypes binding over the C ABI in ``include/dsa.h`` (library
+``libdsa_gb300.so`` in this directory, built by ``build.py``).  This module
+only marshals arguments: torch supplies device memory and the current CUDA
+stream, every step of the computation runs in the library's CUDA kernels.
+There is no CPU or dense fallback: if the library is missing or the device
+cannot run it, calls raise.
+
+Function names follow the C entry points without the ``dsa_`` prefix.
+"""
+from __future__ import annotations
+
+import ctypes
+import dataclasses
+import math
+import os
+import threading
+
+import torch
+
+from .synth import Workload
+
+__all__ = [
+    "Config", "DsaError", "config_for", "workspace_size", "workspace",
+    "pool_keys", "index_scores", "topk_from_scores", "index_scores_topk",
+    "sparse_attn_fwd", "sparse_attn_bwd", "get_device_status",
+    "status_string", "library_path", "WS_INDEX", "WS_FWD", "WS_BWD",
+    "WS_STATUS",
+]
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
+_lock = threading.Lock()
+_lib = None
+
+WS_INDEX, WS_FWD, WS_BWD, WS_STATUS = 0, 1, 2, 3
+
+STATUS_NAMES = {
+    0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED_SHAPE",
+    3: "DSA_ERR_WORKSPACE_TOO_SMALL", 4: "DSA_ERR_MISALIGNED",
+    5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT",
+    7: "DSA_ERR_DEVICE_BAD_INDEX", 8: "DSA_ERR_SCRATCH_CAP",
+}
+
+# every symbol include/dsa.h declares
+EXPORTS = [
+    "dsa_workspace_size", "dsa_workspace_init", "dsa_pool_keys",
+    "dsa_index_scores", "dsa_topk_from_scores", "dsa_index_scores_topk",
+    "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_get_device_status",
+    "dsa_status_string", "dsa_abi_version",
+]
+
+
+class DsaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = int(code)
+        super().__init__(f"{where}: {STATUS_NAMES.get(self.code, self.code)}")
+
+
+class _CConfig(ctypes.Structure):
+    _fields_ = [
+        ("seq_len", ctypes.c_int64), ("pool_size", ctypes.c_int32),
+        ("topk_pools", ctypes.c_int32), ("n_local", ctypes.c_int32),
+        ("idx_heads", ctypes.c_int32), ("idx_dim", ctypes.c_int32),
+        ("attn_heads", ctypes.c_int32), ("d_qk", ctypes.c_int32),
+        ("d_v", ctypes.c_int32), ("chunk_q", ctypes.c_int32),
+        ("sm_scale", ctypes.c_float), ("scratch_cap", ctypes.c_uint64),
+    ]
+
+
+assert ctypes.sizeof(_CConfig) == 56
+
+
+@dataclasses.dataclass(frozen=True)
+class Config:
+    """Mirror of dsa_config_t."""
+    seq_len: int
+    topk_pools: int = 512
+    n_local: int = 0
+    idx_heads: int = 32
+    idx_dim: int = 128
+    attn_heads: int = 64
+    d_qk: int = 512
+    d_v: int = 512
+    chunk_q: int = 256
+    sm_scale: float = 0.0
+    scratch_cap: int = 2 << 30
+    pool_size: int = 4
+
+    @property
+    def scale(self) -> float:
+        return self.sm_scale if self.sm_scale > 0 else 1.0 / math.sqrt(self.d_qk)
+
+    def c(self) -> _CConfig:
+        return _CConfig(self.seq_len, self.pool_size, self.topk_pools,
+                        self.n_local, self.idx_heads, self.idx_dim,
+                        self.attn_heads, self.d_qk, self.d_v, self.chunk_q,
+                        float(self.sm_scale), self.scratch_cap)
+
+
+def config_for(wl: Workload, **over) -> Config:
+    cfg = Config(seq_len=wl.S, topk_pools=wl.K_p, n_local=wl.n_loc,
+                 idx_heads=wl.H_I, idx_dim=wl.D_I, attn_heads=wl.H,
+                 d_qk=wl.d_qk, d_v=wl.d_v, chunk_q=wl.chunk_q,
+                 scratch_cap=wl.scratch_cap)
+    return dataclasses.replace(cfg, **over) if over else cfg
+
+
+def library_path() -> str:
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(_LIB_PATH):
+            raise ImportError(
+                f"CUDA library {_LIB_PATH} is missing; build it with "
+                "`python -m long_context_sparse_gb300.build` (there is no "
+                "CPU fallback)")
+        lib = ctypes.CDLL(_LIB_PATH)
+        P, I32, I64, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                           ctypes.c_size_t)
+        CP = ctypes.POINTER(_CConfig)
+        sig = {
+            "dsa_workspace_size": [CP, I32, ctypes.POINTER(SZ)],
+            "dsa_workspace_init": [P, SZ, P],
+            "dsa_pool_keys": [CP, P, P, P],
+            "dsa_index_scores": [CP, P, P, P, I64, I64, P, I64, P, SZ, P],
+            "dsa_topk_from_scores": [CP, P, I64, I64, I64, P, P, SZ, P],
+            "dsa_index_scores_topk": [CP, P, P, P, P, P, SZ, P],
+            "dsa_sparse_attn_fwd": [CP, P, P, P, P, P, P, P, SZ, P],
+            "dsa_sparse_attn_bwd": [CP, P, P, P, P, P, P, P, P, P, P, P, SZ,
+                                    P],
+            "dsa_get_device_status": [P, P, ctypes.POINTER(ctypes.c_uint32)],
+        }
+        for name, args in sig.items():
+            f = getattr(lib, name)
+            f.argtypes = args
+            f.restype = ctypes.c_int
+        lib.dsa_status_string.argtypes = [ctypes.c_int]
+        lib.dsa_status_string.restype = ctypes.c_char_p
+        lib.dsa_abi_version.argtypes = []
+        lib.dsa_abi_version.restype = ctypes.c_int32
+        _lib = lib
+        return lib
+
+
+def status_string(code: int) -> str:
+    return _load().dsa_status_string(int(code)).decode()
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise DsaError(rc, where)
+
+
+def _stream(dev: torch.device):
+    return ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+
+
+def _ptr(t) -> ctypes.c_void_p:
+    return ctypes.c_void_p(0 if t is None else t.data_ptr())
+
+
+def _need(t: torch.Tensor, name: str, dtype, shape=None, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected "
+                         f"{tuple(shape)}")
+
+
+def workspace_size(cfg: Config, which: int) -> int:
+    n = ctypes.c_size_t(0)
+    cc = cfg.c()
+    _check(_load().dsa_workspace_size(ctypes.byref(cc), which,
+                                      ctypes.byref(n)), "dsa_workspace_size")
+    return n.value
+
+
+def workspace(cfg: Config, which: int, device="cuda") -> torch.Tensor:
+    """A zero-initialised workspace for the call `which` (uint8 tensor)."""
+    dev = torch.device(device)
+    nbytes = workspace_size(cfg, which)
+    ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    _check(_load().dsa_workspace_init(_ptr(ws), nbytes, _stream(dev)),
+           "dsa_workspace_init")
+    return ws
+
+
+def _ws(cfg, which, ws, dev):
+    if ws is None:
+        return workspace(cfg, which, dev)
+    _need(ws, "ws", torch.uint8, device=dev)
+    return ws
+
+
+def pool_keys(cfg: Config, k_idx: torch.Tensor, k_pool=None) -> torch.Tensor:
+    S, D = cfg.seq_len, cfg.idx_dim
+    _need(k_idx, "k_idx", torch.bfloat16, (S, D))
+    dev = k_idx.device
+    if k_pool is None:
+        k_pool = torch.empty((S // 4, D), dtype=torch.bfloat16, device=dev)
+    _need(k_pool, "k_pool", torch.bfloat16, (S // 4, D), dev)
+    cc = cfg.c()
+    _check(_load().dsa_pool_keys(ctypes.byref(cc), _ptr(k_idx), _ptr(k_pool),
+                                 _stream(dev)), "dsa_pool_keys")
+    return k_pool
+
+
+def index_scores(cfg: Config, q_idx, k_pool, w, t0: int, rows: int,
+                 scores=None, ld: int = None, ws=None) -> torch.Tensor:
+    """Indexer scores of queries t0..t0+rows-1: [rows, ld] fp32; entry (r,p)
+    is valid for p < n_full(t0 + r)."""
+    S = cfg.seq_len
+    _need(q_idx, "q_idx", torch.bfloat16, (S, cfg.idx_heads, cfg.idx_dim))
+    dev = q_idx.device
+    _need(k_pool, "k_pool", torch.bfloat16, (S // 4, cfg.idx_dim), dev)
+    _need(w, "w", torch.float32, (S, cfg.idx_heads), dev)
+    if ld is None:
+        ld = max(4, (S // 4 + 127) // 128 * 128)
+    if scores is None:
+        scores = torch.empty((rows, ld), dtype=torch.float32, device=dev)
+    _need(scores, "scores", torch.float32, (rows, ld), dev)
+    ws = _ws(cfg, WS_STATUS, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_index_scores(ctypes.byref(cc), _ptr(q_idx), _ptr(k_pool),
+                                    _ptr(w), t0, rows, _ptr(scores), ld,
+                                    _ptr(ws), ws.numel(), _stream(dev)),
+           "dsa_index_scores")
+    return scores
+
+
+def topk_from_scores(cfg: Config, scores: torch.Tensor, row0: int,
+                     out=None, ws=None) -> torch.Tensor:
+    """Top-K_p selection of fp32 score rows (row r <-> query row0 + r)."""
+    if scores.dim() != 2:
+        raise ValueError("scores must be [rows, ld]")
+    rows, ld = scores.shape
+    _need(scores, "scores", torch.float32)
+    dev = scores.device
+    if out is None:
+        out = torch.empty((rows, cfg.topk_pools), dtype=torch.int32, device=dev)
+    _need(out, "topk_idx", torch.int32, (rows, cfg.topk_pools), dev)
+    ws = _ws(cfg, WS_STATUS, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_topk_from_scores(ctypes.byref(cc), _ptr(scores), ld,
+                                        row0, rows, _ptr(out), _ptr(ws),
+                                        ws.numel(), _stream(dev)),
+           "dsa_topk_from_scores")
+    return out
+
+
+def index_scores_topk(cfg: Config, q_idx, k_idx, w, out=None,
+                      ws=None) -> torch.Tensor:
+    """Pool, score (chunked) and select: topk_idx [S, K_p] int32."""
+    S = cfg.seq_len
+    _need(q_idx, "q_idx", torch.bfloat16, (S, cfg.idx_heads, cfg.idx_dim))
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, (S, cfg.idx_dim), dev)
+    _need(w, "w", torch.float32, (S, cfg.idx_heads), dev)
+    if out is None:
+        out = torch.empty((S, cfg.topk_pools), dtype=torch.int32, device=dev)
+    _need(out, "topk_idx", torch.int32, (S, cfg.topk_pools), dev)
+    ws = _ws(cfg, WS_INDEX, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_index_scores_topk(ctypes.byref(cc), _ptr(q_idx),
+                                         _ptr(k_idx), _ptr(w), _ptr(out),
+                                         _ptr(ws), ws.numel(), _stream(dev)),
+           "dsa_index_scores_topk")
+    return out
+
+
+def sparse_attn_fwd(cfg: Config, q, k, v, topk_idx, o=None, lse=None,
+                    ws=None):
+    """Sparse attention forward: (o [S,H,d_v] bf16, lse [S,H] fp32)."""
+    S, H = cfg.seq_len, cfg.attn_heads
+    _need(q, "q", torch.bfloat16, (S, H, cfg.d_qk))
+    dev = q.device
+    _need(k, "k", torch.bfloat16, (S, cfg.d_qk), dev)
+    _need(v, "v", torch.bfloat16, (S, cfg.d_v), dev)
+    _need(topk_idx, "topk_idx", torch.int32, (S, cfg.topk_pools), dev)
+    if o is None:
+        o = torch.empty((S, H, cfg.d_v), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((S, H), dtype=torch.float32, device=dev)
+    _need(o, "o", torch.bfloat16, (S, H, cfg.d_v), dev)
+    _need(lse, "lse", torch.float32, (S, H), dev)
+    ws = _ws(cfg, WS_FWD, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_sparse_attn_fwd(ctypes.byref(cc), _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(topk_idx), _ptr(o),
+                                       _ptr(lse), _ptr(ws), ws.numel(),
+                                       _stream(dev)), "dsa_sparse_attn_fwd")
+    return o, lse
+
+
+def sparse_attn_bwd(cfg: Config, q, k, v, o, lse, dO, topk_idx, dq=None,
+                    dk=None, dv=None, ws=None):
+    """Sparse attention backward: (dq [S,H,d_qk], dk [S,d_qk], dv [S,d_v])."""
+    S, H = cfg.seq_len, cfg.attn_heads
+    _need(q, "q", torch.bfloat16, (S, H, cfg.d_qk))
+    dev = q.device
+    _need(k, "k", torch.bfloat16, (S, cfg.d_qk), dev)
+    _need(v, "v", torch.bfloat16, (S, cfg.d_v), dev)
+    _need(o, "o", torch.bfloat16, (S, H, cfg.d_v), dev)
+    _need(lse, "lse", torch.float32, (S, H), dev)
+    _need(dO, "dO", torch.bfloat16, (S, H, cfg.d_v), dev)
+    _need(topk_idx, "topk_idx", torch.int32, (S, cfg.topk_pools), dev)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dk is None:
+        dk = torch.empty_like(k)
+    if dv is None:
+        dv = torch.empty_like(v)
+    _need(dq, "dq", torch.bfloat16, (S, H, cfg.d_qk), dev)
+    _need(dk, "dk", torch.bfloat16, (S, cfg.d_qk), dev)
+    _need(dv, "dv", torch.bfloat16, (S, cfg.d_v), dev)
+    ws = _ws(cfg, WS_BWD, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_sparse_attn_bwd(ctypes.byref(cc), _ptr(q), _ptr(k),
+                                       _ptr(v), _ptr(o), _ptr(lse), _ptr(dO),
+                                       _ptr(topk_idx), _ptr(dq), _ptr(dk),
+                                       _ptr(dv), _ptr(ws), ws.numel(),
+                                       _stream(dev)), "dsa_sparse_attn_bwd")
+    return dq, dk, dv
+
+
+def get_device_status(ws: torch.Tensor) -> int:
+    """Synchronise the current stream, read and clear the status word."""
+    v = ctypes.c_uint32(0)
+    _check(_load().dsa_get_device_status(_ptr(ws), _stream(ws.device),
+                                         ctypes.byref(v)),
+           "dsa_get_device_status")
+    return v.value

@@ -1,0 +1,408 @@
+// dsa_api.cu -- the C ABI declared in include/dsa.h: argument validation,
+// workspace carving, the chunked indexer loop and kernel launches.  Host
+// code only; every step of the path runs in this library's kernels.
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr size_t kHeader = 256;        // status word + padding
+constexpr int64_t kPoolTile = 128;     // score row pitch granularity
+constexpr int kMaxDevices = 64;
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct DeviceInfo {
+  int num_sms = 0;
+  int cc_major = 0, cc_minor = 0;
+};
+
+std::mutex g_mu;
+DeviceInfo g_dev[kMaxDevices];
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+dsa_status_t device_info(DeviceInfo* out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    return DSA_ERR_CUDA;
+  std::lock_guard<std::mutex> lk(g_mu);
+  DeviceInfo& d = g_dev[dev];
+  if (d.num_sms == 0) {
+    if (cudaDeviceGetAttribute(&d.num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) !=
+            cudaSuccess ||
+        cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) !=
+            cudaSuccess) {
+      d.num_sms = 0;
+      return DSA_ERR_CUDA;
+    }
+  }
+  *out = d;
+  return DSA_OK;
+}
+
+dsa_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_encode) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                         cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !p)
+      return DSA_ERR_CUDA;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  *fn = g_encode;
+  return DSA_OK;
+}
+
+// 2D bf16 row-major [rows, cols] tensor, box {64 cols, box_rows}, 128B swizzle.
+dsa_status_t encode_2d(CUtensorMap* map, const void* base, uint64_t rows,
+                       uint64_t cols, uint32_t box_rows) {
+  PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  dsa_status_t st = get_encoder(&fn);
+  if (st != DSA_OK) return st;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base),
+                  dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
+}
+
+uint64_t timeout_ns() {
+  static uint64_t v = [] {
+    const char* e = getenv("DSA_WAIT_TIMEOUT_MS");
+    double ms = e ? atof(e) : 2000.0;
+    if (!(ms > 0)) ms = 2000.0;
+    return (uint64_t)(ms * 1e6);
+  }();
+  return v;
+}
+
+bool is_pow2_upto(int x, int hi) { return x >= 1 && x <= hi && (x & (x - 1)) == 0; }
+
+// Shape checks common to every entry point.  Values outside the problem
+// statement are INVALID_ARG; valid values the kernels do not run are
+// UNSUPPORTED_SHAPE (never a fallback).
+dsa_status_t check_cfg(const dsa_config_t* c, bool need_index, bool need_attn) {
+  if (!c) return DSA_ERR_INVALID_ARG;
+  if (c->seq_len < 1 || c->pool_size < 1 || c->topk_pools < 1 || c->chunk_q < 1 ||
+      c->n_local < 0 || c->idx_heads < 1 || c->idx_dim < 1 || c->attn_heads < 1 ||
+      c->d_qk < 1 || c->d_v < 1 || !(c->sm_scale >= 0.f) || isinf(c->sm_scale))
+    return DSA_ERR_INVALID_ARG;
+  if (c->seq_len > (int64_t)1 << 26) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (c->pool_size != 4) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (c->topk_pools > 2048) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (c->n_local != 0 && c->n_local != 3) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (need_index) {
+    if (!is_pow2_upto(c->idx_heads, 64)) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (c->idx_dim != 64 && c->idx_dim != 128) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (c->seq_len * (int64_t)c->idx_heads > ((int64_t)1 << 31) - 512)
+      return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (c->chunk_q > 4096) return DSA_ERR_UNSUPPORTED_SHAPE;
+  }
+  if (need_attn) {
+    if (c->attn_heads > 128) return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (c->d_qk != 64 && c->d_qk != 128 && c->d_qk != 256 && c->d_qk != 512)
+      return DSA_ERR_UNSUPPORTED_SHAPE;
+    if (c->d_v != c->d_qk) return DSA_ERR_UNSUPPORTED_SHAPE;
+  }
+  return DSA_OK;
+}
+
+int64_t score_ld(const dsa_config_t* c) {
+  int64_t P = c->seq_len / 4;
+  if (P < 1) P = 1;
+  return (int64_t)round_up((size_t)P, kPoolTile);
+}
+
+int64_t chunk_rows(const dsa_config_t* c) {
+  return c->chunk_q < c->seq_len ? c->chunk_q : c->seq_len;
+}
+
+size_t ws_bytes_for(const dsa_config_t* c, int which) {
+  const int64_t S = c->seq_len;
+  switch (which) {
+    case DSA_WS_INDEX: {
+      const size_t kp = round_up((size_t)(S / 4) * c->idx_dim * 2, 256);
+      const size_t sc = (size_t)chunk_rows(c) * score_ld(c) * 4;
+      return kHeader + kp + sc;
+    }
+    case DSA_WS_FWD:
+    case DSA_WS_STATUS:
+      return kHeader;
+    case DSA_WS_BWD: {
+      const size_t dl = round_up((size_t)S * c->attn_heads * 4, 256);
+      const size_t acc = round_up((size_t)S * c->d_qk * 4, 256);
+      return kHeader + dl + 2 * acc;
+    }
+    default:
+      return 0;
+  }
+}
+
+dsa_status_t make_ctx(void* ws, void* stream, LaunchCtx* ctx) {
+  DeviceInfo d;
+  dsa_status_t st = device_info(&d);
+  if (st != DSA_OK) return st;
+  ctx->stream = reinterpret_cast<cudaStream_t>(stream);
+  ctx->status = reinterpret_cast<uint32_t*>(ws);
+  ctx->timeout_ns = timeout_ns();
+  ctx->num_sms = d.num_sms;
+  return DSA_OK;
+}
+
+dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+
+dsa_status_t check_ws(const dsa_config_t* cfg, int which, void* ws, size_t ws_bytes) {
+  if (!ws) return DSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DSA_ERR_MISALIGNED;
+  if (ws_bytes < ws_bytes_for(cfg, which)) return DSA_ERR_WORKSPACE_TOO_SMALL;
+  return DSA_OK;
+}
+
+AttnShape attn_shape(const dsa_config_t* c) {
+  AttnShape s;
+  s.S = c->seq_len;
+  s.H = c->attn_heads;
+  s.D = c->d_qk;
+  s.K_p = c->topk_pools;
+  s.n_loc = c->n_local;
+  s.scale = c->sm_scale > 0.f ? c->sm_scale : 1.0f / sqrtf((float)c->d_qk);
+  return s;
+}
+
+}  // namespace
+}  // namespace dsa
+
+using namespace dsa;
+
+extern "C" {
+
+int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_status_string(dsa_status_t s) {
+  switch (s) {
+    case DSA_OK: return "DSA_OK";
+    case DSA_ERR_INVALID_ARG: return "DSA_ERR_INVALID_ARG";
+    case DSA_ERR_UNSUPPORTED_SHAPE: return "DSA_ERR_UNSUPPORTED_SHAPE";
+    case DSA_ERR_WORKSPACE_TOO_SMALL: return "DSA_ERR_WORKSPACE_TOO_SMALL";
+    case DSA_ERR_MISALIGNED: return "DSA_ERR_MISALIGNED";
+    case DSA_ERR_CUDA: return "DSA_ERR_CUDA";
+    case DSA_ERR_DEVICE_TIMEOUT: return "DSA_ERR_DEVICE_TIMEOUT";
+    case DSA_ERR_DEVICE_BAD_INDEX: return "DSA_ERR_DEVICE_BAD_INDEX";
+    case DSA_ERR_SCRATCH_CAP: return "DSA_ERR_SCRATCH_CAP";
+  }
+  return "DSA_ERR_UNKNOWN";
+}
+
+dsa_status_t dsa_workspace_size(const dsa_config_t* cfg, int32_t which, size_t* bytes) {
+  if (!bytes) return DSA_ERR_INVALID_ARG;
+  if (which < DSA_WS_INDEX || which > DSA_WS_STATUS) return DSA_ERR_INVALID_ARG;
+  dsa_status_t st = check_cfg(cfg, which == DSA_WS_INDEX, which == DSA_WS_FWD ||
+                                                               which == DSA_WS_BWD);
+  if (st != DSA_OK) return st;
+  *bytes = ws_bytes_for(cfg, which);
+  return DSA_OK;
+}
+
+dsa_status_t dsa_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < kHeader) return DSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DSA_ERR_MISALIGNED;
+  return cuda_status(
+      cudaMemsetAsync(ws, 0, kHeader, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+dsa_status_t dsa_pool_keys(const dsa_config_t* cfg, const void* k_idx, void* k_pool,
+                           void* stream) {
+  dsa_status_t st = check_cfg(cfg, true, false);
+  if (st != DSA_OK) return st;
+  if (!k_idx || (!k_pool && cfg->seq_len >= 4)) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(k_idx) || !aligned16(k_pool)) return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  st = make_ctx(nullptr, stream, &ctx);
+  if (st != DSA_OK) return st;
+  return cuda_status(launch_pool(ctx, static_cast<const __nv_bfloat16*>(k_idx),
+                                 static_cast<__nv_bfloat16*>(k_pool), cfg->seq_len,
+                                 cfg->idx_dim));
+}
+
+dsa_status_t dsa_index_scores(const dsa_config_t* cfg, const void* q_idx,
+                              const void* k_pool, const float* w, int64_t t0,
+                              int64_t rows, float* scores, int64_t ld, void* ws,
+                              size_t ws_bytes, void* stream) {
+  dsa_status_t st = check_cfg(cfg, true, false);
+  if (st != DSA_OK) return st;
+  if (!q_idx || !w || !scores || t0 < 0 || rows < 0 || t0 + rows > cfg->seq_len ||
+      ld < 1 || (ld & 3) != 0)
+    return DSA_ERR_INVALID_ARG;
+  if (rows > 4096) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if ((st = check_ws(cfg, DSA_WS_STATUS, ws, ws_bytes)) != DSA_OK) return st;
+  if (rows == 0) return DSA_OK;
+  const int64_t p_lim = n_full(t0 + rows - 1);
+  if (p_lim > ld) return DSA_ERR_INVALID_ARG;
+  if (p_lim == 0) return DSA_OK;
+  if (!k_pool) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(q_idx) || !aligned16(k_pool) || !aligned16(w) || !aligned16(scores))
+    return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  CUtensorMap qm, km;
+  const int64_t S = cfg->seq_len;
+  if ((st = encode_2d(&qm, q_idx, (uint64_t)(S * cfg->idx_heads), cfg->idx_dim, 256)) !=
+      DSA_OK)
+    return st;
+  if ((st = encode_2d(&km, k_pool, (uint64_t)(S / 4), cfg->idx_dim, 128)) != DSA_OK)
+    return st;
+  return cuda_status(launch_indexer(ctx, qm, km, w, cfg->idx_heads, cfg->idx_dim, t0,
+                                    rows, p_lim, scores, ld));
+}
+
+dsa_status_t dsa_topk_from_scores(const dsa_config_t* cfg, const float* scores,
+                                  int64_t ld, int64_t row0, int64_t rows,
+                                  int32_t* topk_idx, void* ws, size_t ws_bytes,
+                                  void* stream) {
+  dsa_status_t st = check_cfg(cfg, false, false);
+  if (st != DSA_OK) return st;
+  if (!scores || !topk_idx || ld < 1 || row0 < 0 || rows < 0 ||
+      row0 + rows > cfg->seq_len)
+    return DSA_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, DSA_WS_STATUS, ws, ws_bytes)) != DSA_OK) return st;
+  if (!aligned16(scores) || !aligned16(topk_idx)) return DSA_ERR_MISALIGNED;
+  if (rows == 0) return DSA_OK;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  return cuda_status(
+      launch_topk(ctx, scores, ld, row0, rows, cfg->topk_pools, topk_idx));
+}
+
+dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg, const void* q_idx,
+                                   const void* k_idx, const float* w,
+                                   int32_t* topk_idx, void* ws, size_t ws_bytes,
+                                   void* stream) {
+  dsa_status_t st = check_cfg(cfg, true, false);
+  if (st != DSA_OK) return st;
+  if (!q_idx || !k_idx || !w || !topk_idx) return DSA_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, DSA_WS_INDEX, ws, ws_bytes)) != DSA_OK) return st;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx))
+    return DSA_ERR_MISALIGNED;
+  const int64_t S = cfg->seq_len, P = S / 4, C = chunk_rows(cfg), ld = score_ld(cfg);
+  if ((uint64_t)C * (uint64_t)ld * 4u > cfg->scratch_cap) return DSA_ERR_SCRATCH_CAP;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  __nv_bfloat16* k_pool = reinterpret_cast<__nv_bfloat16*>(base + kHeader);
+  float* scores = reinterpret_cast<float*>(
+      base + kHeader + round_up((size_t)P * cfg->idx_dim * 2, 256));
+  CUtensorMap qm, km;
+  if (P > 0) {
+    cudaError_t e = launch_pool(ctx, static_cast<const __nv_bfloat16*>(k_idx), k_pool,
+                                S, cfg->idx_dim);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    if ((st = encode_2d(&qm, q_idx, (uint64_t)(S * cfg->idx_heads), cfg->idx_dim,
+                        256)) != DSA_OK)
+      return st;
+    if ((st = encode_2d(&km, k_pool, (uint64_t)P, cfg->idx_dim, 128)) != DSA_OK)
+      return st;
+  }
+  for (int64_t t0 = 0; t0 < S; t0 += C) {
+    const int64_t rows = (S - t0) < C ? (S - t0) : C;
+    const int64_t p_lim = n_full(t0 + rows - 1);
+    if (p_lim > cfg->topk_pools) {  // some row has more pools than K_p: score
+      cudaError_t e = launch_indexer(ctx, qm, km, w, cfg->idx_heads, cfg->idx_dim, t0,
+                                     rows, p_lim, scores, ld);
+      if (e != cudaSuccess) return DSA_ERR_CUDA;
+    }
+    cudaError_t e = launch_topk(ctx, scores, ld, t0, rows, cfg->topk_pools,
+                                topk_idx + t0 * cfg->topk_pools);
+    if (e != cudaSuccess) return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
+}
+
+dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q, const void* k,
+                                 const void* v, const int32_t* topk_idx, void* o,
+                                 float* lse, void* ws, size_t ws_bytes, void* stream) {
+  dsa_status_t st = check_cfg(cfg, false, true);
+  if (st != DSA_OK) return st;
+  if (!q || !k || !v || !topk_idx || !o || !lse) return DSA_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, DSA_WS_FWD, ws, ws_bytes)) != DSA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(topk_idx) ||
+      !aligned16(o) || !aligned16(lse))
+    return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  cudaError_t e = launch_attn_fwd(ctx, attn_shape(cfg), static_cast<const __nv_bfloat16*>(q),
+                                  static_cast<const __nv_bfloat16*>(k),
+                                  static_cast<const __nv_bfloat16*>(v), topk_idx,
+                                  static_cast<__nv_bfloat16*>(o), lse);
+  return e == cudaErrorInvalidValue ? DSA_ERR_UNSUPPORTED_SHAPE : cuda_status(e);
+}
+
+dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q, const void* k,
+                                 const void* v, const void* o, const float* lse,
+                                 const void* dO, const int32_t* topk_idx, void* dq,
+                                 void* dk, void* dv, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  dsa_status_t st = check_cfg(cfg, false, true);
+  if (st != DSA_OK) return st;
+  if (!q || !k || !v || !o || !lse || !dO || !topk_idx || !dq || !dk || !dv)
+    return DSA_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, DSA_WS_BWD, ws, ws_bytes)) != DSA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      !aligned16(lse) || !aligned16(dO) || !aligned16(topk_idx) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv))
+    return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  const AttnShape s = attn_shape(cfg);
+  uint8_t* base = static_cast<uint8_t*>(ws);
+  float* delta = reinterpret_cast<float*>(base + kHeader);
+  float* dk_acc = reinterpret_cast<float*>(
+      base + kHeader + round_up((size_t)s.S * s.H * 4, 256));
+  float* dv_acc = dk_acc + round_up((size_t)s.S * s.D * 4, 256) / 4;
+  cudaError_t e = launch_attn_bwd_pre(ctx, s, static_cast<const __nv_bfloat16*>(o),
+                                      static_cast<const __nv_bfloat16*>(dO), delta,
+                                      dk_acc, dv_acc);
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  e = launch_attn_bwd(ctx, s, static_cast<const __nv_bfloat16*>(q),
+                      static_cast<const __nv_bfloat16*>(k),
+                      static_cast<const __nv_bfloat16*>(v),
+                      static_cast<const __nv_bfloat16*>(dO), lse, delta, topk_idx,
+                      static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc);
+  if (e == cudaErrorInvalidValue) return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  e = launch_attn_bwd_finalize(ctx, s, dk_acc, dv_acc, static_cast<__nv_bfloat16*>(dk),
+                               static_cast<__nv_bfloat16*>(dv));
+  return cuda_status(e);
+}
+
+dsa_status_t dsa_get_device_status(void* ws, void* stream, uint32_t* device_status) {
+  if (!ws || !device_status) return DSA_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  uint32_t v = 0;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaMemcpyAsync(&v, ws, sizeof v, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return DSA_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof v, s) != cudaSuccess) return DSA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return DSA_ERR_CUDA;
+  *device_status = v;
+  return DSA_OK;
+}
+
+}  // extern "C"

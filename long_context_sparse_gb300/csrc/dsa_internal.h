@@ -1,0 +1,69 @@
+// dsa_internal.h -- launchers shared between the C-ABI layer and the kernel
+// translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dsa {
+
+struct LaunchCtx {
+  cudaStream_t stream;
+  uint32_t* status;     // device status word (workspace header)
+  uint64_t timeout_ns;  // bounded-wait limit for every spin in the kernels
+  int num_sms;
+};
+
+// a1: k_pool[p] = bf16(((k0 + k1) + (k2 + k3)) * 0.25), fp32.
+cudaError_t launch_pool(const LaunchCtx& c, const __nv_bfloat16* k_idx,
+                        __nv_bfloat16* k_pool, int64_t S, int D_I);
+
+// a4: per-row top-k over fp32 scores (row r <-> query row0 + r).
+cudaError_t launch_topk(const LaunchCtx& c, const float* scores, int64_t ld,
+                        int64_t row0, int64_t rows, int K_p, int32_t* out);
+
+// a2: indexer scores for queries t0 .. t0+rows-1 against pools < p_lim.
+// q_map: q_idx viewed as [S*H_I, D_I] bf16, box {64, 256};
+// k_map: k_pool [P, D_I] bf16, box {64, 128}.
+cudaError_t launch_indexer(const LaunchCtx& c, const CUtensorMap& q_map,
+                           const CUtensorMap& k_map, const float* w, int H_I,
+                           int D_I, int64_t t0, int64_t rows, int64_t p_lim,
+                           float* scores, int64_t ld);
+
+struct AttnShape {
+  int64_t S;
+  int H;
+  int D;        // d_qk == d_v
+  int K_p;
+  int n_loc;
+  float scale;
+};
+
+// a5 + a6: sparse attention forward.
+cudaError_t launch_attn_fwd(const LaunchCtx& c, const AttnShape& s,
+                            const __nv_bfloat16* q, const __nv_bfloat16* k,
+                            const __nv_bfloat16* v, const int32_t* idx,
+                            __nv_bfloat16* o, float* lse);
+
+// a7: delta = rowsum(dO * O); zero the fp32 dK/dV accumulators.
+cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
+                                const __nv_bfloat16* o,
+                                const __nv_bfloat16* dO, float* delta,
+                                float* dk_acc, float* dv_acc);
+
+// a8: sparse attention backward (dQ direct, dK/dV fp32 scatter).
+cudaError_t launch_attn_bwd(const LaunchCtx& c, const AttnShape& s,
+                            const __nv_bfloat16* q, const __nv_bfloat16* k,
+                            const __nv_bfloat16* v, const __nv_bfloat16* dO,
+                            const float* lse, const float* delta,
+                            const int32_t* idx, __nv_bfloat16* dq,
+                            float* dk_acc, float* dv_acc);
+
+// a9: fp32 accumulators -> bf16 dK, dV.
+cudaError_t launch_attn_bwd_finalize(const LaunchCtx& c, const AttnShape& s,
+                                     const float* dk_acc, const float* dv_acc,
+                                     __nv_bfloat16* dk, __nv_bfloat16* dv);
+
+}  // namespace dsa

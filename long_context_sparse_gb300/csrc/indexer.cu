@@ -1,0 +1,300 @@
+// indexer.cu -- the DSA lightning indexer on 5th-generation tensor cores.
+//
+//   I[t,p] = sum_h w[t,h] * max(0, q_idx[t,h,:] . k_pool[p,:])
+//
+// "A lightweight indexer ... scores every query against every earlier pool
+// of 4 tokens" -- the dense, quadratic part of DSA ("Scaling Training to 1M
+// Token Context on GLM-5.3-Flash", section "DeepSeek Sparse Attention (DSA)
+// Optimizations"), run one chunk of queries at a time (section "Splitting
+// the DSA Indexer / Over Time: Chunking").
+//
+// GEMM mapping (one CTA per SM, persistent over tiles):
+//   M = 128 pools      -> TMEM lanes; A = k_pool tile [128 x D_I], K-major
+//   N = 256 columns    -> (query, head) pairs, 256/H_I queries x H_I heads;
+//                         B = q_idx rows [256 x D_I], K-major
+//   K = D_I            -> D_I/16 tcgen05.mma (kind::f16, bf16 -> fp32)
+// Each epilogue thread owns one pool (one TMEM lane) and reads the H_I
+// columns of each query: ReLU, times w[t,h], summed over heads in fp32, then
+// one coalesced store per query.  No cross-lane traffic.
+//
+// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// MMA issuer, warps 2-5 epilogue.  A tiles stream through a 4-stage TMA ring;
+// the B tile stays resident while consecutive tiles share it; accumulators
+// are double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
+// overlaps the MMAs of the next.
+#include "dsa_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kBM = 128;  // pools per tile
+constexpr int kBN = 256;  // (query, head) columns per tile
+constexpr int kThreads = 192;
+
+template <int DI>
+struct IdxCfg {
+  static constexpr int KB = DI / 64;                 // 128-byte k-boxes
+  static constexpr int kStages = DI == 64 ? 8 : 4;
+  static constexpr uint32_t kABytes = kBM * DI * 2;  // one pool tile
+  static constexpr uint32_t kBBytes = kBN * DI * 2;  // one query tile
+  static constexpr uint32_t kSmem =
+      kBBytes + kStages * kABytes + kBN * 4 + 256 + 1024;
+};
+
+__device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
+                                           uint64_t timeout_ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (globaltimer_ns() - t0 > timeout_ns) return false;
+  }
+  return true;
+}
+
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+template <int HI, int DI>
+__global__ void __launch_bounds__(kThreads, 1)
+    indexer_kernel(const __grid_constant__ CUtensorMap q_map,
+                   const __grid_constant__ CUtensorMap k_map,
+                   const float* __restrict__ w, int64_t t0, int64_t rows,
+                   int64_t p_lim, float* __restrict__ scores, int64_t ld,
+                   int n_ptiles, int64_t n_items, uint32_t* status,
+                   uint64_t timeout_ns) {
+  using C = IdxCfg<DI>;
+  constexpr int QT = kBN / HI;  // queries per N tile
+  constexpr uint32_t IDESC = idesc_bf16(kBM, kBN, 0, 0);
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sB = base;
+  const uint32_t sA = base + C::kBBytes;
+  float* w_s = reinterpret_cast<float*>(gbase + C::kBBytes + C::kStages * C::kABytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + kBN);
+  // barrier slots
+  const uint32_t bar0 = smem_u32(bars);
+  auto a_full = [&](int s) { return bar0 + 8u * s; };
+  auto a_empty = [&](int s) { return bar0 + 8u * (C::kStages + s); };
+  const uint32_t b_full = bar0 + 8u * (2 * C::kStages);
+  const uint32_t b_empty = b_full + 8u;
+  auto acc_full = [&](int a) { return b_full + 16u + 8u * a; };
+  auto acc_empty = [&](int a) { return b_full + 32u + 8u * a; };
+  const uint32_t done_bar = b_full + 48u;
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * C::kStages + 7);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 8);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const Waiter W{abort_flag, status, timeout_ns};
+
+  const int64_t beg = (int64_t)blockIdx.x * n_items / gridDim.x;
+  const int64_t end = (int64_t)(blockIdx.x + 1) * n_items / gridDim.x;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::kStages; ++s) {
+      mbar_init(a_full(s), 1);
+      mbar_init(a_empty(s), 1);
+    }
+    mbar_init(b_full, 1);
+    mbar_init(b_empty, 1);
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(acc_full(a), 1);
+      mbar_init(acc_empty(a), 4);
+    }
+    mbar_init(done_bar, 1);
+    *abort_flag = 0u;
+    fence_mbar_init();
+    prefetch_tensormap(&q_map);
+    prefetch_tensormap(&k_map);
+  }
+  if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------------ TMA producer
+    if (lane == 0) {
+      int64_t it = 0;
+      int bcount = 0;
+      int64_t cur_nt = -1;
+      for (int64_t item = beg; item < end; ++item) {
+        const int64_t nt = item / n_ptiles, pt = item - nt * n_ptiles;
+        if (nt != cur_nt) {
+          if (!W.wait(b_empty, (bcount & 1) ^ 1)) break;
+          mbar_expect_tx(b_full, C::kBBytes);
+          const int32_t row = (int32_t)(t0 * HI + nt * kBN);
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb)
+            tma_load_2d(sB + kb * (kBN * 128), &q_map, kb * 64, row, b_full);
+          cur_nt = nt;
+          ++bcount;
+        }
+        const int s = (int)(it % C::kStages);
+        const uint32_t u = (uint32_t)(it / C::kStages);
+        if (!W.wait(a_empty(s), (u & 1u) ^ 1u)) break;
+        mbar_expect_tx(a_full(s), C::kABytes);
+        const uint32_t dst = sA + s * C::kABytes;
+#pragma unroll
+        for (int kb = 0; kb < C::KB; ++kb)
+          tma_load_2d(dst + kb * (kBM * 128), &k_map, kb * 64, (int32_t)(pt * kBM),
+                      a_full(s));
+        ++it;
+      }
+      // Let every copy this thread issued land before the CTA can exit.
+      for (int64_t j = it > C::kStages ? it - C::kStages : 0; j < it; ++j)
+        drain_wait(a_full((int)(j % C::kStages)), (uint32_t)(j / C::kStages) & 1u,
+                   timeout_ns);
+      if (bcount > 0) drain_wait(b_full, (uint32_t)(bcount - 1) & 1u, timeout_ns);
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------- MMA issuer
+    if (lane == 0) {
+      int64_t it = 0, local = 0;
+      int bcount = 0;
+      int64_t cur_nt = -1;
+      bool issued = false;
+      for (int64_t item = beg; item < end; ++item) {
+        const int64_t nt = item / n_ptiles;
+        if (nt != cur_nt) {
+          if (!W.wait(b_full, bcount & 1)) break;
+          ++bcount;
+          cur_nt = nt;
+        }
+        const int a = (int)(local & 1);
+        const uint32_t v = (uint32_t)(local >> 1);
+        if (!W.wait(acc_empty(a), (v & 1u) ^ 1u)) break;
+        const int s = (int)(it % C::kStages);
+        const uint32_t u = (uint32_t)(it / C::kStages);
+        if (!W.wait(a_full(s), u & 1u)) break;
+        tc_fence_after();
+        const uint32_t d = tmem + (uint32_t)(a * kBN);
+        const uint32_t a_tile = sA + s * C::kABytes;
+#pragma unroll
+        for (int ks = 0; ks < DI / 16; ++ks) {
+          const int kb = ks >> 2, kin = ks & 3;
+          const uint64_t ad = sdesc_sw128(a_tile + kb * (kBM * 128) + kin * 32, 16, 1024);
+          const uint64_t bd = sdesc_sw128(sB + kb * (kBN * 128) + kin * 32, 16, 1024);
+          tc_mma(d, ad, bd, IDESC, ks > 0 ? 1u : 0u);
+        }
+        issued = true;
+        tc_commit(a_empty(s));
+        tc_commit(acc_full(a));
+        const int64_t next_nt = (item + 1 < end) ? (item + 1) / n_ptiles : -1;
+        if (next_nt != nt) tc_commit(b_empty);
+        ++it;
+        ++local;
+      }
+      if (issued) {
+        tc_commit(done_bar);
+        drain_wait(done_bar, 0, timeout_ns);
+      }
+    }
+  } else {
+    // --------------------------------------------------------- epilogue
+    const int quad = warp & 3;
+    const int etid = threadIdx.x - 64;  // 0..127
+    int64_t cur_nt = -1, local = 0;
+    for (int64_t item = beg; item < end; ++item) {
+      const int64_t nt = item / n_ptiles, pt = item - nt * n_ptiles;
+      if (nt != cur_nt) {
+        named_bar_sync(1, 128);
+        for (int j = etid; j < kBN; j += 128) {
+          const int64_t qrow = nt * QT + j / HI;
+          w_s[j] = qrow < rows ? __ldg(w + (t0 + qrow) * HI + (j % HI)) : 0.f;
+        }
+        named_bar_sync(1, 128);
+        cur_nt = nt;
+      }
+      const int a = (int)(local & 1);
+      const uint32_t v = (uint32_t)(local >> 1);
+      if (!W.wait(acc_full(a), v & 1u)) break;
+      tc_fence_after();
+      const int64_t p = pt * kBM + quad * 32 + lane;
+      const bool p_ok = p < p_lim;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kBN);
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < kBN / 32; ++c) {
+        uint32_t r0[16], r1[16];
+        tmem_ld16(taddr + c * 32, r0);
+        tmem_ld16(taddr + c * 32 + 16, r1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const int col = c * 32 + j;
+          const float x = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
+          acc = fmaf(w_s[col], fmaxf(x, 0.f), acc);
+          if (col % HI == HI - 1) {
+            const int64_t qrow = nt * QT + col / HI;
+            if (p_ok && qrow < rows) scores[qrow * ld + p] = acc;
+            acc = 0.f;
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acc_empty(a));
+      ++local;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, 512);
+}
+
+template <int HI, int DI>
+cudaError_t launch_indexer_t(const LaunchCtx& c, const CUtensorMap& q_map,
+                             const CUtensorMap& k_map, const float* w,
+                             int64_t t0, int64_t rows, int64_t p_lim,
+                             float* scores, int64_t ld) {
+  using C = IdxCfg<DI>;
+  constexpr int QT = kBN / HI;
+  const int64_t n_ntiles = (rows + QT - 1) / QT;
+  const int n_ptiles = (int)((p_lim + kBM - 1) / kBM);
+  const int64_t n_items = n_ntiles * n_ptiles;
+  if (n_items == 0) return cudaSuccess;
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
+    cudaError_t e = cudaFuncSetAttribute(indexer_kernel<HI, DI>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         (int)C::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_dev = dev;
+  }
+  int64_t grid = n_items < c.num_sms ? n_items : c.num_sms;
+  indexer_kernel<HI, DI><<<(unsigned)grid, kThreads, C::kSmem, c.stream>>>(
+      q_map, k_map, w, t0, rows, p_lim, scores, ld, n_ptiles, n_items, c.status,
+      c.timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_indexer(const LaunchCtx& c, const CUtensorMap& q_map,
+                           const CUtensorMap& k_map, const float* w, int H_I,
+                           int D_I, int64_t t0, int64_t rows, int64_t p_lim,
+                           float* scores, int64_t ld) {
+#define DSA_IDX_CASE(HI, DI)                                                   \
+  if (H_I == HI && D_I == DI)                                                  \
+    return launch_indexer_t<HI, DI>(c, q_map, k_map, w, t0, rows, p_lim, scores, \
+                                    ld);
+  DSA_IDX_CASE(1, 64) DSA_IDX_CASE(2, 64) DSA_IDX_CASE(4, 64)
+  DSA_IDX_CASE(8, 64) DSA_IDX_CASE(16, 64) DSA_IDX_CASE(32, 64)
+  DSA_IDX_CASE(64, 64)
+  DSA_IDX_CASE(1, 128) DSA_IDX_CASE(2, 128) DSA_IDX_CASE(4, 128)
+  DSA_IDX_CASE(8, 128) DSA_IDX_CASE(16, 128) DSA_IDX_CASE(32, 128)
+  DSA_IDX_CASE(64, 128)
+#undef DSA_IDX_CASE
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa

@@ -79,7 +79,7 @@ def _load():
             lib.oracle_attn_bwd.restype = ctypes.c_int
             lib.oracle_attn_bwd.argtypes = [_i64, _i32, _i32, _i32, _i32, _i32,
                                             _dbl, _p, _p, _p, _p, _p, _i64,
-                                            _p, _p, _p, _p]
+                                            _p, _p, _i64, _p, _p, _p]
             lib.oracle_dense_masked_attn.restype = None
             lib.oracle_dense_masked_attn.argtypes = [_i64, _i32, _i32, _i32,
                                                      _dbl, _p, _p, _p, _p, _p,
@@ -146,17 +146,23 @@ def pool_f64(k_idx: np.ndarray) -> np.ndarray:
 
 
 def index_scores(q_idx: np.ndarray, k_pool: np.ndarray, w: np.ndarray,
-                 rows=None) -> np.ndarray:
+                 rows=None, S: int = None) -> np.ndarray:
     """I[t,p] in fp64 for the given query rows; -inf where p >= n_full(t).
-    q_idx [S,H_I,D_I] bf16 bits, k_pool [S//4, D_I] bf16 bits, w [S,H_I] f32.
-    """
+    k_pool [S//4, D_I] bf16 bits.  Without `rows`: q_idx [S,H_I,D_I] bf16
+    bits and w [S,H_I] f32 cover every query.  With `rows`: q_idx and w hold
+    those rows only, in that order (then S defaults to 4 * len(k_pool))."""
     q = _c(q_idx, np.uint16)
     kp = _c(k_pool, np.uint16)
     ww = _c(w, np.float32)
-    S, H, D = q.shape
+    n, H, D = q.shape
+    if rows is None:
+        S = n
+        r = np.arange(S, dtype=np.int64)
+    else:
+        r = _c(rows, np.int64)
+        S = 4 * kp.shape[0] if S is None else S
     P = S // 4
-    assert kp.shape == (P, D) and ww.shape == (S, H)
-    r = np.arange(S, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    assert kp.shape == (P, D) and ww.shape == (r.size, H) and n == r.size
     out = np.empty((r.size, P), np.float64)
     _load().oracle_index_scores(S, H, D, _ptr(q), _ptr(kp), _ptr(ww), r.size,
                                 _ptr(r), _ptr(out))
@@ -190,10 +196,14 @@ def topk(scores: np.ndarray, rows, K_p: int) -> np.ndarray:
 def index_topk(q_idx, k_idx, w, K_p: int, rows=None):
     """Pool + fp64 indexer + top-k for the given rows.
     Returns (topk [nrows, K_p] int32, scores [nrows, P] fp64)."""
-    S = q_idx.shape[0]
-    r = np.arange(S, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    S = k_idx.shape[0]
     kp = pool(k_idx)
-    sc = index_scores(q_idx, kp, w, r)
+    if rows is None:
+        r = np.arange(S, dtype=np.int64)
+        sc = index_scores(q_idx, kp, w)
+    else:
+        r = _c(rows, np.int64)
+        sc = index_scores(np.asarray(q_idx)[r], kp, np.asarray(w)[r], r, S)
     return topk(sc, r, K_p), sc
 
 
@@ -215,14 +225,16 @@ def key_set(t: int, K_p: int, n_loc: int, idx_row: np.ndarray) -> np.ndarray:
 def attn_fwd(q, k, v, topk_idx, K_p: int, n_loc: int, scale: float,
              rows=None):
     """fp64 sparse attention forward on the listed rows.
-    q [S,H,d_qk], k [S,d_qk], v [S,d_v] bf16 bits; topk_idx [S,K_p] int32.
+    k [S,d_qk], v [S,d_v] bf16 bits; topk_idx [S,K_p] int32.  Without
+    `rows`, q is [S,H,d_qk]; with `rows`, q holds those rows only, in order.
     Returns (o [nrows,H,d_v], lse [nrows,H])."""
     qq, kk, vv = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
     ii = _c(topk_idx, np.int32)
-    S, H, dqk = qq.shape
-    dv = vv.shape[1]
-    assert kk.shape == (S, dqk) and vv.shape[0] == S and ii.shape == (S, K_p)
+    n, H, dqk = qq.shape
+    S, dv = vv.shape
+    assert kk.shape == (S, dqk) and ii.shape == (S, K_p)
     r = np.arange(S, dtype=np.int64) if rows is None else _c(rows, np.int64)
+    assert n == r.size
     o = np.empty((r.size, H, dv), np.float64)
     lse = np.empty((r.size, H), np.float64)
     rc = _load().oracle_attn_fwd(S, H, dqk, dv, K_p, n_loc, float(scale),
@@ -237,24 +249,34 @@ def attn_fwd(q, k, v, topk_idx, K_p: int, n_loc: int, scale: float,
 
 
 def attn_bwd(q, k, v, dO_rows, topk_idx, K_p: int, n_loc: int, scale: float,
-             rows=None):
+             rows=None, keys=None):
     """fp64 analytic backward with upstream gradient dO_rows [nrows,H,d_v]
-    (bf16 bits) on the listed rows and zero elsewhere.
-    Returns (dq [nrows,H,d_qk], dk [S,d_qk], dv [S,d_v])."""
+    (bf16 bits) on the listed rows and zero elsewhere.  q is [S,H,d_qk]
+    without `rows`, else the listed rows only, in order.
+    Returns (dq [nrows,H,d_qk], dk, dv): dk/dv are [S, d] or, when `keys`
+    (token ids) is given, [len(keys), d] holding only those tokens' rows."""
     qq, kk, vv = _c(q, np.uint16), _c(k, np.uint16), _c(v, np.uint16)
     gg = _c(dO_rows, np.uint16)
     ii = _c(topk_idx, np.int32)
-    S, H, dqk = qq.shape
-    dv = vv.shape[1]
+    n, H, dqk = qq.shape
+    S, dv = vv.shape
     r = np.arange(S, dtype=np.int64) if rows is None else _c(rows, np.int64)
-    assert gg.shape == (r.size, H, dv)
+    assert gg.shape == (r.size, H, dv) and n == r.size
+    if keys is None:
+        slot, n_slots = None, S
+    else:
+        keys = _c(keys, np.int64)
+        slot = np.full(S, -1, np.int64)
+        slot[keys] = np.arange(keys.size)
+        n_slots = keys.size
     dq = np.empty((r.size, H, dqk), np.float64)
-    dk = np.empty((S, dqk), np.float64)
-    dvv = np.empty((S, dv), np.float64)
+    dk = np.empty((n_slots, dqk), np.float64)
+    dvv = np.empty((n_slots, dv), np.float64)
     rc = _load().oracle_attn_bwd(S, H, dqk, dv, K_p, n_loc, float(scale),
                                  _ptr(qq), _ptr(kk), _ptr(vv), _ptr(gg),
-                                 _ptr(ii), r.size, _ptr(r), _ptr(dq), _ptr(dk),
-                                 _ptr(dvv))
+                                 _ptr(ii), r.size, _ptr(r),
+                                 None if slot is None else _ptr(slot),
+                                 n_slots, _ptr(dq), _ptr(dk), _ptr(dvv))
     if rc != 0:
         raise MemoryError("oracle attn_bwd: allocation failed")
     return dq, dk, dvv

@@ -109,7 +109,8 @@ void oracle_pool_f64(int64_t S, int32_t D_I, const uint16_t* k_idx,
 /* ------------------------------------------------------- indexer (a2,a3) */
 
 /* Scores of the listed query rows against every pool, fp64.
- *   q_idx  [S, H_I, D_I] bf16, k_pool [P, D_I] bf16, w [S, H_I] fp32
+ *   q_idx  [nrows, H_I, D_I] bf16 and w [nrows, H_I] fp32 hold the listed
+ *          rows (row r is query t = rows[r]); k_pool [P, D_I] bf16
  *   out    [nrows, P]: I[t,p] for p < n_full(t), -inf for later pools
  *          (those are never candidates). */
 void oracle_index_scores(int64_t S, int32_t H_I, int32_t D_I,
@@ -128,12 +129,12 @@ void oracle_index_scores(int64_t S, int32_t H_I, int32_t D_I,
       }
       double acc = 0.0;
       for (int32_t h = 0; h < H_I; ++h) {
-        const uint16_t* qv = q_idx + (t * H_I + h) * D_I;
+        const uint16_t* qv = q_idx + (r * H_I + h) * D_I;
         const uint16_t* kv = k_pool + p * D_I;
         double dot = 0.0;
         for (int32_t d = 0; d < D_I; ++d) dot += bf(qv[d]) * bf(kv[d]);
         double relu = dot > 0.0 ? dot : 0.0;
-        acc += (double)w[t * H_I + h] * relu;
+        acc += (double)w[r * H_I + h] * relu;
       }
       o[p] = acc;
     }
@@ -265,8 +266,9 @@ int64_t oracle_key_set(int64_t t, int32_t K_p, int32_t n_loc,
  *   s_j   = scale * q[t,h] . k_j            for j in K(t)
  *   O     = sum_j softmax_j(s) v_j,  LSE = log sum_j exp(s_j)
  * An empty key set gives O = 0 and LSE = -inf.
- * q [S,H,d_qk], k [S,d_qk], v [S,d_v] bf16 (one K and one V shared by all
- * heads); topk_idx [S,K_p] int32; o [nrows,H,d_v], lse [nrows,H] fp64. */
+ * q [nrows,H,d_qk] bf16 holds the listed rows (row r is query t = rows[r]);
+ * k [S,d_qk], v [S,d_v] bf16 (one K and one V shared by all heads);
+ * topk_idx [S,K_p] int32; o [nrows,H,d_v], lse [nrows,H] fp64. */
 int oracle_attn_fwd(int64_t S, int32_t H, int32_t d_qk, int32_t d_v,
                     int32_t K_p, int32_t n_loc, double scale,
                     const uint16_t* q, const uint16_t* k, const uint16_t* v,
@@ -291,7 +293,7 @@ int oracle_attn_fwd(int64_t S, int32_t H, int32_t d_qk, int32_t d_v,
         lse[r * H + h] = -INFINITY;
         continue;
       }
-      const uint16_t* qv = q + (t * H + h) * (int64_t)d_qk;
+      const uint16_t* qv = q + (r * H + h) * (int64_t)d_qk;
       double mx = -INFINITY;
       for (int64_t i = 0; i < n; ++i) {
         const uint16_t* kv = k + keys[i] * d_qk;
@@ -328,14 +330,17 @@ int oracle_attn_fwd(int64_t S, int32_t H, int32_t d_qk, int32_t d_v,
  *   dK_j += scale * dS_j q[t,h]
  *   dV_j += P_j dO
  * ([MTraining] section 3.2: every backward GEMM depends on A = P.)
- * dO [nrows,H,d_v] bf16; dq [nrows,H,d_qk]; dk [S,d_qk], dv [S,d_v] are
- * overwritten with the contributions of the listed rows. */
+ * q [nrows,H,d_qk] and dO [nrows,H,d_v] bf16 hold the listed rows;
+ * dq [nrows,H,d_qk].  dk [n_slots,d_qk] and
+ * dv [n_slots,d_v] are overwritten with the contributions of the listed rows:
+ * token j lands in row key_slot[j] (skipped when -1), or in row j when
+ * key_slot is NULL (then n_slots = S).  Only the addressing differs. */
 int oracle_attn_bwd(int64_t S, int32_t H, int32_t d_qk, int32_t d_v,
                     int32_t K_p, int32_t n_loc, double scale,
                     const uint16_t* q, const uint16_t* k, const uint16_t* v,
                     const uint16_t* dO, const int32_t* topk_idx,
-                    int64_t nrows, const int64_t* rows, double* dq,
-                    double* dk, double* dv) {
+                    int64_t nrows, const int64_t* rows, const int64_t* key_slot,
+                    int64_t n_slots, double* dq, double* dk, double* dv) {
   int64_t cap = 4 * (int64_t)K_p + n_loc + 1;
   int64_t* keys = (int64_t*)malloc((size_t)cap * sizeof(int64_t));
   double* s = (double*)malloc((size_t)cap * sizeof(double));
@@ -346,8 +351,9 @@ int oracle_attn_bwd(int64_t S, int32_t H, int32_t d_qk, int32_t d_v,
     free(dp);
     return -1;
   }
-  memset(dk, 0, (size_t)S * d_qk * sizeof(double));
-  memset(dv, 0, (size_t)S * d_v * sizeof(double));
+  if (!key_slot) n_slots = S;
+  memset(dk, 0, (size_t)n_slots * d_qk * sizeof(double));
+  memset(dv, 0, (size_t)n_slots * d_v * sizeof(double));
   for (int64_t r = 0; r < nrows; ++r) {
     int64_t t = rows[r];
     int64_t n = oracle_key_set(t, K_p, n_loc, topk_idx + t * K_p, keys);
@@ -355,7 +361,7 @@ int oracle_attn_bwd(int64_t S, int32_t H, int32_t d_qk, int32_t d_v,
       double* dqrow = dq + (r * H + h) * (int64_t)d_qk;
       for (int32_t d = 0; d < d_qk; ++d) dqrow[d] = 0.0;
       if (n == 0) continue;
-      const uint16_t* qv = q + (t * H + h) * (int64_t)d_qk;
+      const uint16_t* qv = q + (r * H + h) * (int64_t)d_qk;
       const uint16_t* gv = dO + (r * H + h) * (int64_t)d_v;
       double mx = -INFINITY;
       for (int64_t i = 0; i < n; ++i) {
@@ -380,12 +386,12 @@ int oracle_attn_bwd(int64_t S, int32_t H, int32_t d_qk, int32_t d_v,
         double pw = exp(s[i] - lse);
         double ds = pw * (dp[i] - delta);
         const uint16_t* kv = k + keys[i] * d_qk;
-        double* dkrow = dk + keys[i] * d_qk;
-        double* dvrow = dv + keys[i] * d_v;
-        for (int32_t d = 0; d < d_qk; ++d) {
-          dqrow[d] += scale * ds * bf(kv[d]);
-          dkrow[d] += scale * ds * bf(qv[d]);
-        }
+        int64_t slot = key_slot ? key_slot[keys[i]] : keys[i];
+        for (int32_t d = 0; d < d_qk; ++d) dqrow[d] += scale * ds * bf(kv[d]);
+        if (slot < 0) continue;
+        double* dkrow = dk + slot * d_qk;
+        double* dvrow = dv + slot * d_v;
+        for (int32_t d = 0; d < d_qk; ++d) dkrow[d] += scale * ds * bf(qv[d]);
         for (int32_t e = 0; e < d_v; ++e) dvrow[e] += pw * bf(gv[e]);
       }
     }

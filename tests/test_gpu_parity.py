@@ -1,0 +1,266 @@
+"""GPU parity: the CUDA library (called through its C ABI) against the fp64
+CPU oracle on the same seeded inputs."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import long_context_sparse_gb300 as dsa
+import oracle
+from long_context_sparse_gb300 import synth
+from tests.helpers import ATOL_OUT, bits, check_index_rows, f64
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+def _cfg(wl, **over):
+    return dsa.config_for(wl, **over)
+
+
+def _status_ok(ws):
+    st = dsa.get_device_status(ws)
+    assert st == 0, dsa.STATUS_NAMES.get(st, st)
+
+
+# ------------------------------------------------------------------ pool
+
+
+@pytest.mark.parametrize("S,D", [(4, 64), (7, 128), (1024, 64), (16387, 128)])
+def test_pool_bit_exact(S, D):
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], S, D_I=D)
+    _, k_idx, _ = synth.indexer_inputs(wl, 1, "cpu")
+    got = dsa.pool_keys(_cfg(wl), k_idx.to(DEV))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(got), oracle.pool(bits(k_idx)))
+
+
+# ----------------------------------------------------------------- top-k
+
+
+def _craft_scores(rows, ld, seed):
+    g = np.random.default_rng(seed)
+    s = g.standard_normal((rows, ld)).astype(np.float32)
+    s[:, ::5] = s[:, 1:2]                      # many exact ties
+    s[0::3, ::2] = 0.0
+    s[0::3, 1::4] = -0.0                       # +-0 ties
+    s[1::7, :] = 1.5                           # whole row equal
+    s[2::11, :] = np.abs(s[2::11, :])          # non-negative (like ReLU sums)
+    return s
+
+
+@pytest.mark.parametrize("row0,rows,ld,K", [
+    (0, 300, 80, 8), (0, 2048, 512, 64), (16000, 384, 4096, 512),
+    (131000, 64, 32768, 512), (400000, 4, 100000, 512), (37, 5, 16, 1),
+    (2000, 17, 600, 2048)])
+def test_topk_bit_exact_on_shared_scores(row0, rows, ld, K):
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], max(row0 + rows, 4 * ld),
+                      K_p=K)
+    cfg = _cfg(wl)
+    s = _craft_scores(rows, ld, row0 + K)
+    st = torch.from_numpy(s).to(DEV)
+    ws = dsa.workspace(cfg, dsa.WS_STATUS, DEV)
+    got = dsa.topk_from_scores(cfg, st, row0, ws=ws).cpu().numpy()
+    _status_ok(ws)
+    ref = oracle.topk(s, np.arange(row0, row0 + rows), K)
+    np.testing.assert_array_equal(got, ref)
+
+
+# --------------------------------------------------------------- indexer
+
+
+@pytest.mark.parametrize("name,S,t0,rows", [
+    ("tiny_fwd_s1k", 1024, 0, 1024), ("glm_s16k", 4099, 3000, 300),
+    ("glm_s16k", 16384, 15000, 256), ("padded2051_s64k", 2600, 1, 700)])
+def test_index_scores_match_oracle(name, S, t0, rows):
+    wl = synth.scaled(synth.WORKLOADS[name], S)
+    cfg = _cfg(wl)
+    q_idx, k_idx, w = synth.indexer_inputs(wl, 3, "cpu")
+    kp = oracle.pool(bits(k_idx))
+    kp_dev = torch.from_numpy(kp.view(np.int16)).view(torch.bfloat16).to(DEV)
+    ws = dsa.workspace(cfg, dsa.WS_STATUS, DEV)
+    sc = dsa.index_scores(cfg, q_idx.to(DEV), kp_dev, w.to(DEV), t0, rows,
+                          ws=ws).cpu().numpy()
+    _status_ok(ws)
+    r = np.arange(t0, t0 + rows)
+    pick = r[:: max(1, rows // 64)]
+    ref = oracle.index_scores(bits(q_idx)[pick], kp, w.numpy()[pick], pick, S)
+    for i, t in enumerate(pick):
+        n = (t + 1) // 4
+        got = sc[t - t0, :n].astype(np.float64)
+        # bf16 products are exact in fp32; fp32 sums over D_I and H_I
+        tol = 1e-5 * np.abs(ref[i, :n]).max(initial=1e-3) + 1e-7
+        np.testing.assert_allclose(got, ref[i, :n], rtol=2e-5, atol=tol)
+
+
+def test_index_scores_independent_of_chunking_bit_exact():
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], 9000)
+    cfg = _cfg(wl)
+    q_idx, k_idx, w = (x.to(DEV) for x in synth.indexer_inputs(wl, 5, "cpu"))
+    kp = dsa.pool_keys(cfg, k_idx)
+    whole = dsa.index_scores(cfg, q_idx, kp, w, 8000, 1000)
+    parts = [dsa.index_scores(cfg, q_idx, kp, w, t0, n)
+             for t0, n in [(8000, 1), (8001, 255), (8256, 500), (8756, 244)]]
+    torch.cuda.synchronize()
+    rows = [whole[0:1], whole[1:256], whole[256:756], whole[756:1000]]
+    for a, b, t0 in zip(parts, rows, [8000, 8001, 8256, 8756]):
+        n = (t0 + a.shape[0]) // 4 - 1          # valid for every row of a
+        assert torch.equal(a[:, :n], b[:, :n])
+
+
+# ------------------------------------------------------ index + top-k
+
+
+@pytest.mark.parametrize("name,S,nrows", [
+    ("tiny_fwd_s1k", 1024, 0), ("glm_s16k", 2051, 0), ("glm_s16k", 16384, 40),
+    ("padded2051_s64k", 9000, 40)])
+def test_index_topk_matches_oracle(name, S, nrows):
+    wl = synth.scaled(synth.WORKLOADS[name], S)
+    cfg = _cfg(wl)
+    q_idx, k_idx, w = synth.indexer_inputs(wl, 7, "cpu")
+    ws = dsa.workspace(cfg, dsa.WS_INDEX, DEV)
+    got = dsa.index_scores_topk(cfg, q_idx.to(DEV), k_idx.to(DEV), w.to(DEV),
+                                ws=ws).cpu().numpy()
+    _status_ok(ws)
+    rows = (np.arange(S) if nrows == 0 else
+            synth.sample_rows(wl, nrows, 11).numpy())
+    ref, sc = oracle.index_topk(bits(q_idx), bits(k_idx), w.numpy(), wl.K_p,
+                                rows)
+    eq, ex = check_index_rows(got[rows], ref, sc, rows, wl.K_p)
+    assert eq + ex == rows.size and eq >= 0.9 * rows.size
+
+
+def test_index_topk_chunked_equals_unchunked_bit_exact():
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], 6000)
+    q_idx, k_idx, w = (x.to(DEV) for x in synth.indexer_inputs(wl, 9, "cpu"))
+    outs = []
+    for C in (1, 37, 256, 4096):
+        cfg = _cfg(wl, chunk_q=C)
+        outs.append(dsa.index_scores_topk(cfg, q_idx, k_idx, w))
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+def test_index_topk_full_budget_selects_every_pool():
+    wl = synth.scaled(synth.WORKLOADS["tiny_fwd_s1k"], 256, K_p=64)
+    cfg = _cfg(wl)
+    q_idx, k_idx, w = (x.to(DEV) for x in synth.indexer_inputs(wl, 2, "cpu"))
+    got = dsa.index_scores_topk(cfg, q_idx, k_idx, w).cpu().numpy()
+    for t in range(256):
+        n = (t + 1) // 4
+        np.testing.assert_array_equal(got[t, :n], np.arange(n))
+        assert (got[t, n:] == -1).all()
+
+
+# ------------------------------------------------------------ attention
+
+
+def _attn_case(name, S, seed, **over):
+    wl = synth.scaled(synth.WORKLOADS[name], S, **over)
+    q, k, v, dO = synth.attention_inputs(wl, seed, "cpu")
+    idx = synth.random_selection(wl, seed, "cpu")
+    return wl, q, k, v, dO, idx
+
+
+@pytest.mark.parametrize("name,S,over", [
+    ("tiny_fwd_s1k", 1024, {}),
+    ("tiny_fwd_s1k", 77, dict(K_p=5, n_loc=3)),
+    ("glm_s16k", 3000, {}),
+    ("glm_s16k", 300, dict(H=80)),          # two head blocks
+    ("padded2051_s64k", 2300, {}),          # 16 heads, 2051 keys
+    ("glm_s16k", 13, dict(n_loc=3)),        # tiny, empty rows
+])
+def test_attn_fwd_bwd_match_oracle(name, S, over):
+    wl, q, k, v, dO, idx = _attn_case(name, S, 21, **over)
+    cfg = _cfg(wl)
+    qd, kd, vd, dOd, idd = (x.to(DEV) for x in (q, k, v, dO, idx))
+    wsf = dsa.workspace(cfg, dsa.WS_FWD, DEV)
+    o, lse = dsa.sparse_attn_fwd(cfg, qd, kd, vd, idd, ws=wsf)
+    _status_ok(wsf)
+    rows = np.arange(S) if S <= 700 else synth.sample_rows(wl, 48, 3).numpy()
+    ro, rl = oracle.attn_fwd(bits(q)[rows], bits(k), bits(v), idx.numpy(),
+                             wl.K_p, wl.n_loc, cfg.scale, rows)
+    go, gl = f64(o)[rows], f64(lse)[rows]
+    fin = np.isfinite(rl)
+    assert np.array_equal(fin, np.isfinite(gl))
+    assert (gl[~fin] == -np.inf).all() and (go[~fin.any(1)] == 0).all()
+    assert np.abs(go - ro).max() <= ATOL_OUT
+    assert np.abs(gl[fin] - rl[fin]).max() <= ATOL_OUT
+    if not wl.backward and S > 200:
+        return
+    wsb = dsa.workspace(cfg, dsa.WS_BWD, DEV)
+    dq, dk, dv = dsa.sparse_attn_bwd(cfg, qd, kd, vd, o, lse, dOd, idd, ws=wsb)
+    _status_ok(wsb)
+    if S <= 700:
+        rdq, rdk, rdv = oracle.attn_bwd(bits(q), bits(k), bits(v), bits(dO),
+                                        idx.numpy(), wl.K_p, wl.n_loc,
+                                        cfg.scale)
+        assert np.abs(f64(dq) - rdq).max() <= ATOL_OUT
+        assert np.abs(f64(dk) - rdk).max() <= ATOL_OUT
+        assert np.abs(f64(dv) - rdv).max() <= ATOL_OUT
+    else:
+        rdq, _, _ = oracle.attn_bwd(bits(q)[rows], bits(k), bits(v),
+                                    bits(dO)[rows], idx.numpy(), wl.K_p,
+                                    wl.n_loc, cfg.scale, rows)
+        assert np.abs(f64(dq)[rows] - rdq).max() <= ATOL_OUT
+
+
+def _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, rows):
+    """dK/dV are not row-local: rerun the GPU backward with dO zeroed outside
+    the sampled rows and compare with the oracle's contributions of those
+    rows only, on every token they touch."""
+    dOz = torch.zeros_like(dO)
+    rt = torch.from_numpy(rows).to(dO.device)
+    dOz[rt] = dO[rt]
+    dq, dk, dv = dsa.sparse_attn_bwd(cfg, q, k, v, o, lse, dOz, idx)
+    idx_h = idx.cpu().numpy()
+    keys = sorted({int(s) for t in rows
+                   for s in oracle.key_set(int(t), wl.K_p, wl.n_loc, idx_h[t])})
+    keys = np.array(keys, np.int64)
+    rdq, rdk, rdv = oracle.attn_bwd(bits(q[rt]), bits(k), bits(v),
+                                    bits(dO[rt]), idx_h, wl.K_p, wl.n_loc,
+                                    cfg.scale, rows, keys)
+    assert np.abs(f64(dq[rt]) - rdq).max() <= ATOL_OUT
+    kt = torch.from_numpy(keys).to(dO.device)
+    assert np.abs(f64(dk[kt]) - rdk).max() <= ATOL_OUT
+    assert np.abs(f64(dv[kt]) - rdv).max() <= ATOL_OUT
+    # tokens nobody in `rows` attends get exactly zero
+    untouched = torch.ones(wl.S, dtype=torch.bool, device=dO.device)
+    untouched[kt] = False
+    assert not dk[untouched].any() and not dv[untouched].any()
+
+
+@pytest.mark.parametrize("name,S", [("glm_s16k", 16384),
+                                    ("padded2051_s64k", 16500)])
+def test_attn_large_sampled_rows(name, S):
+    wl, q, k, v, dO, idx = _attn_case(name, S, 33)
+    cfg = _cfg(wl)
+    qd, kd, vd, dOd, idd = (x.to(DEV) for x in (q, k, v, dO, idx))
+    o, lse = dsa.sparse_attn_fwd(cfg, qd, kd, vd, idd)
+    rows = synth.sample_rows(wl, 12, 5).numpy()
+    ro, rl = oracle.attn_fwd(bits(q)[rows], bits(k), bits(v), idx.numpy(),
+                             wl.K_p, wl.n_loc, cfg.scale, rows)
+    assert np.abs(f64(o)[rows] - ro).max() <= ATOL_OUT
+    assert np.abs(f64(lse)[rows] - rl).max() <= ATOL_OUT
+    _masked_dkdv_check(wl, cfg, qd, kd, vd, dOd, idd, o, lse, rows[-6:])
+
+
+def test_bad_index_is_latched_not_read():
+    wl, q, k, v, dO, idx = _attn_case("tiny_fwd_s1k", 256, 4)
+    cfg = _cfg(wl)
+    bad = idx.clone()
+    bad[100, 0] = 1000          # pool beyond n_full(100) = 25
+    ws = dsa.workspace(cfg, dsa.WS_FWD, DEV)
+    dsa.sparse_attn_fwd(cfg, q.to(DEV), k.to(DEV), v.to(DEV), bad.to(DEV),
+                        ws=ws)
+    assert dsa.get_device_status(ws) == 7
+    assert dsa.get_device_status(ws) == 0      # read clears
+
+
+def test_unsupported_shapes_raise_before_launch():
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], 64)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.workspace(_cfg(wl, d_qk=576, d_v=512), dsa.WS_FWD, DEV)
+    assert e.value.code == 2

@@ -170,8 +170,10 @@ def test_indexer_rows_are_independent_of_chunking():
     kp = oracle.pool(k)
     full = oracle.index_scores(q, kp, w)
     for C in (1, 7, 16, 64):
-        parts = [oracle.index_scores(q, kp, w, np.arange(r0, min(S, r0 + C)))
-                 for r0 in range(0, S, C)]
+        parts = []
+        for r0 in range(0, S, C):
+            r = np.arange(r0, min(S, r0 + C))
+            parts.append(oracle.index_scores(q[r], kp, w[r], r, S))
         np.testing.assert_array_equal(np.concatenate(parts), full)
 
 
@@ -453,14 +455,24 @@ def test_bwd_row_subset_equals_zeroed_upstream_gradient():
         sel = np.sort(rng.choice(n, size=min(n, K_p), replace=False))
         idx[t, :sel.size] = sel
     rows = np.array([3, 17, 18, 39])
-    dq_r, dk_r, dv_r = oracle.attn_bwd(q, k, v, dO[rows], idx, K_p, 3, 0.5,
-                                       rows)
+    dq_r, dk_r, dv_r = oracle.attn_bwd(q[rows], k, v, dO[rows], idx, K_p, 3,
+                                       0.5, rows)
     dOz = np.zeros_like(dO)
     dOz[rows] = dO[rows]
     dq_f, dk_f, dv_f = oracle.attn_bwd(q, k, v, dOz, idx, K_p, 3, 0.5)
     np.testing.assert_array_equal(dq_r, dq_f[rows])
     np.testing.assert_allclose(dk_r, dk_f, rtol=0, atol=0)
     np.testing.assert_allclose(dv_r, dv_f, rtol=0, atol=0)
+    # compact key addressing returns the same rows
+    keys = np.array([0, 5, 9, 17, 30])
+    _, dk_c, dv_c = oracle.attn_bwd(q[rows], k, v, dO[rows], idx, K_p, 3, 0.5,
+                                    rows, keys)
+    np.testing.assert_array_equal(dk_c, dk_f[keys])
+    np.testing.assert_array_equal(dv_c, dv_f[keys])
+    o_r, l_r = oracle.attn_fwd(q[rows], k, v, idx, K_p, 3, 0.5, rows)
+    o_f, l_f = oracle.attn_fwd(q, k, v, idx, K_p, 3, 0.5)
+    np.testing.assert_array_equal(o_r, o_f[rows])
+    np.testing.assert_array_equal(l_r, l_f[rows])
 
 
 def test_bwd_scatter_identity_and_finite_difference():
