@@ -7,7 +7,27 @@ import torch
 
 # Acceptance tolerances for bf16 I/O with fp32 accumulation.
 ATOL_OUT = 2e-2          # O, LSE, dQ, dK, dV: max-abs
+# Outputs are stored in bf16, whose rounding alone moves x by up to
+# 2^-9 |x|; one bf16 ulp (2^-8 |x|) also covers fp32 summation order and the
+# bf16-rounded P / dS operands of the tensor-core products.  For the
+# workloads' magnitudes (|O|, |dQ|, |dK|, |dV| <~ 1) the bound is the 2e-2.
+RTOL_BF16 = 2.0 ** -8
 TIE_BAND = 1e-3          # relative gap below which index sets may differ
+
+
+def assert_close(got, ref, name="", atol=ATOL_OUT, rtol=RTOL_BF16):
+    """max |got - ref| - rtol |ref| <= atol, with equal infinities allowed."""
+    got = np.asarray(got, np.float64)
+    ref = np.asarray(ref, np.float64)
+    assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    inf = np.isinf(ref)
+    assert np.array_equal(got[inf], ref[inf]), f"{name}: infinities differ"
+    g, r = got[~inf], ref[~inf]
+    assert np.isfinite(g).all(), f"{name}: non-finite values"
+    if g.size:
+        excess = (np.abs(g - r) - rtol * np.abs(r)).max()
+        err = np.abs(g - r).max()
+        assert excess <= atol, f"{name}: max err {err:.3g} (excess {excess:.3g})"
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
