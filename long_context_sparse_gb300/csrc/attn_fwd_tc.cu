@@ -1,0 +1,535 @@
+// attn_fwd_tc.cu -- causal sparse attention forward on 5th-generation tensor
+// cores (tcgen05 + TMEM), one query per CTA at a time, persistent.
+//
+// "the attention reads only those 2048 tokens, so attention cost grows
+// linearly" ("Scaling Training to 1M Token Context on GLM-5.3-Flash",
+// section "DeepSeek Sparse Attention (DSA) Optimizations"); NoPE q/k and the
+// 2,051-key variant (section "Making Sparse Attention Actually Sparse").
+//
+// One K row and one V row per token serve every head of the query, so a
+// gathered tile of 128 keys is the M dimension of both products and the
+// query's heads are N:
+//   S^T[key, h]   = K_tile[key, :] . Q[h, :]        M=128 keys, N=heads, K=D
+//   O^T[dv, h]   += V_tile[:, dv]^T . P^T[key, h]    M=128 dv,   N=heads,
+//                                                    K=128 keys (per 128 dv)
+// S^T and O^T live in TMEM (fp32).  Each softmax thread owns one key (one
+// TMEM lane): it reads its row of S^T, column maxima are taken across the
+// 128 lanes, and it writes its column of P (bf16) into shared memory as the
+// K-major B operand of the second product.  A running maximum is only
+// raised when a tile beats it by more than 2^8, so O^T is rarely rescaled
+// (the final normalisation uses the same maximum, so the result is exact).
+//
+// Warps: 0-3 softmax / epilogue (TMEM lane quadrants 0-3), 4-7 gather
+// producers (cp.async of the selected K/V rows into 128-byte-swizzled
+// stages, completion signalled on an mbarrier), 8 MMA issuer and TMEM
+// owner.  Q comes in by TMA.  Every wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
+#include "attn_common.cuh"
+#include "dsa_internal.h"
+
+namespace dsa {
+namespace {
+
+constexpr int kTileK = 128;            // keys per tile (MMA M)
+constexpr int kStages = 4;             // gather ring depth
+constexpr uint32_t kStageBytes = 32768;  // 128 keys x 128 dims (2 atoms)
+constexpr int kProdThreads = 128;
+constexpr float kMaxSlack = 8.0f;      // log2 headroom before raising a max
+constexpr int kMaskWords = (2048 * 4 + 3 + kTileK + 31) / 32;
+
+template <int D, int NH>
+struct TcFwdCfg {
+  // softmax warpgroups: each owns HPG heads of all 128 keys
+  static constexpr int kGroups = NH > 32 ? 2 : 1;
+  static constexpr int HPG = NH / kGroups;
+  static constexpr int kSoftmaxThreads = 128 * kGroups;
+  static constexpr int kProdWarp0 = 4 * kGroups;       // first producer warp
+  static constexpr int kMmaWarp = kProdWarp0 + 4;
+  static constexpr int kThreads = kSoftmaxThreads + kProdThreads + 32;
+  // registers per thread: the whole register file for one CTA per SM
+  static constexpr int kMaxReg = (65536 / kThreads) & ~7;
+  static constexpr int kChunks = D / 128;  // 128-wide d slices
+  static constexpr uint32_t kQBytes = NH * D * 2;
+  static constexpr uint32_t kPBytes = NH * kTileK * 2;
+  static constexpr uint32_t kTmemCols = NH + kChunks * NH <= 256 ? 256 : 512;
+  // dynamic shared memory for a key list of `cap` entries
+  static uint32_t smem(int cap) {
+    return 1024 + kQBytes + kPBytes + kStages * kStageBytes + cap * 4 +
+           2 * kMaskWords * 4 + (4 * NH + 3 * NH + 8) * 4 + 256;
+  }
+};
+
+__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// NH consecutive fp32 columns of this thread's TMEM lane.
+template <int NH>
+__device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[NH]) {
+  uint32_t r[NH];
+#pragma unroll
+  for (int c = 0; c < NH; c += 16)
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,"
+        "%10,%11,%12,%13,%14,%15}, [%16];"
+        : "=r"(r[c + 0]), "=r"(r[c + 1]), "=r"(r[c + 2]), "=r"(r[c + 3]),
+          "=r"(r[c + 4]), "=r"(r[c + 5]), "=r"(r[c + 6]), "=r"(r[c + 7]),
+          "=r"(r[c + 8]), "=r"(r[c + 9]), "=r"(r[c + 10]), "=r"(r[c + 11]),
+          "=r"(r[c + 12]), "=r"(r[c + 13]), "=r"(r[c + 14]), "=r"(r[c + 15])
+        : "r"(taddr + c));
+  tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < NH; ++c) v[c] = __uint_as_float(r[c]);
+}
+
+__device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, uint64_t ns) {
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > ns) return false;
+  return true;
+}
+
+template <int D, int NH>
+__global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap q_map,
+                       const __nv_bfloat16* __restrict__ k,
+                       const __nv_bfloat16* __restrict__ v,
+                       const int32_t* __restrict__ idx,
+                       __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
+                       int64_t S, int H, int K_p, int n_loc, float scale_log2,
+                       int n_hblk, int tok_cap, uint32_t* status,
+                       uint64_t timeout_ns) {
+  using C = TcFwdCfg<D, NH>;
+  constexpr int HPG = C::HPG;
+  constexpr int kSoftmaxThreads = C::kSoftmaxThreads;
+  constexpr uint32_t IDESC_S = idesc_bf16(128, NH, 0, 0);  // K-major A and B
+  constexpr uint32_t IDESC_O = idesc_bf16(128, NH, 1, 0);  // MN-major A
+
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gb = smem_raw + (base - raw);
+  const uint32_t sQ = base;
+  const uint32_t sP = sQ + C::kQBytes;
+  const uint32_t sStage = sP + C::kPBytes;  // 1024-aligned (sizes are)
+  int32_t* toks = reinterpret_cast<int32_t*>(gb + C::kQBytes + C::kPBytes +
+                                             kStages * kStageBytes);
+  uint32_t* vmask = reinterpret_cast<uint32_t*>(toks + tok_cap);  // [2][words]
+  float* red = reinterpret_cast<float*>(vmask + 2 * kMaskWords);  // [4][NH]
+  float* m_s = red + 4 * NH;                                      // [NH]
+  float* alpha_s = m_s + NH;                                      // [NH]
+  float* inv_s = alpha_s + NH;                                    // [NH]
+  int* misc = reinterpret_cast<int*>(inv_s + NH);  // ntok[2], last, nadd, flag[2]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(misc + 8) + 7) & ~uintptr_t(7));
+  const uint32_t bar0 = smem_u32(bars);
+  auto full = [&](int s) { return bar0 + 8u * s; };
+  auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
+  const uint32_t q_full = bar0 + 8u * (2 * kStages);
+  const uint32_t q_empty = q_full + 8u;
+  const uint32_t s_full = q_full + 16u;
+  const uint32_t p_full = q_full + 24u;
+  const uint32_t pv_done = q_full + 32u;
+  const uint32_t o_empty = q_full + 40u;
+  const uint32_t done_bar = q_full + 48u;
+  auto toks_full = [&](int b) { return q_full + 56u + 8u * b; };
+  auto toks_empty = [&](int b) { return q_full + 72u + 8u * b; };
+  volatile uint32_t* abort_flag =
+      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 11);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 12);
+  int* ntok = misc;
+  int* s_last = misc + 2;
+  int* s_nadd = misc + 3;
+  volatile int* flags = misc + 4;
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const Waiter W{abort_flag, status, timeout_ns};
+  const int64_t n_items = S * n_hblk;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full(s), kProdThreads);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(q_full, 1);
+    mbar_init(q_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(p_full, kSoftmaxThreads);
+    mbar_init(pv_done, 1);
+    mbar_init(o_empty, kSoftmaxThreads);
+    mbar_init(done_bar, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(toks_full(b), kProdThreads);
+      mbar_init(toks_empty(b), kSoftmaxThreads);
+    }
+    *abort_flag = 0u;
+    flags[0] = flags[1] = 0;
+    fence_mbar_init();
+    prefetch_tensormap(&q_map);
+  }
+  if (warp == C::kMmaWarp) tmem_alloc(smem_u32(tmem_slot), C::kTmemCols);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS = tmem;       // S^T: NH columns
+  const uint32_t tO = tmem + NH;  // O^T: kChunks x NH columns
+
+  if (warp >= C::kProdWarp0 && warp < C::kMmaWarp) {
+    // ============================================ gather producers (128)
+    const int ptid = tid - kSoftmaxThreads;
+    uint32_t u = 0, nq = 0;
+    int qi = 0;
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++qi) {
+      if (W.aborted()) break;
+      const int64_t t = S - 1 - item / n_hblk;
+      const int hb = (int)(item % n_hblk);
+      const int buf = qi & 1;
+      if (!W.wait(toks_empty(buf), ((qi >> 1) & 1) ^ 1)) break;
+      // ---- key list of query t: tokens of the selected pools, then the
+      // local tokens no selected pool covers; validity bits for softmax
+      const int32_t* row = idx + t * K_p;
+      const int64_t nf = n_full(t);
+      uint32_t* vm = vmask + buf * kMaskWords;
+      if (ptid == 0) {
+        *s_last = -1;
+        *s_nadd = 0;
+      }
+      for (int w = ptid; w < kMaskWords; w += kProdThreads) vm[w] = 0u;
+      named_sync(2, kProdThreads);
+      for (int i = ptid; i < K_p; i += kProdThreads) {
+        const int32_t p = __ldg(row + i);
+        const bool okp = p >= 0 && (int64_t)p < nf;
+        if (p >= 0) {
+          atomicMax(s_last, i);
+          if (!okp) latch_error(status, DSA_ERR_DEVICE_BAD_INDEX);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) toks[4 * i + j] = okp ? 4 * p + j : -1;
+        if (okp) atomicOr(&vm[(4 * i) >> 5], 0xFu << ((4 * i) & 31));
+      }
+      named_sync(2, kProdThreads);
+      const int npool = 4 * (*s_last + 1);
+      if (n_loc > 0 && ptid < 32) {
+        int nadd = 0;
+        for (int j = n_loc - 1; j >= 0; --j) {
+          const int64_t s = t - j;
+          if (s < 0) continue;
+          const int32_t ps = (int32_t)(s >> 2);
+          bool mine = false;
+          if ((int64_t)ps < nf)
+            for (int i = ptid; i < K_p; i += 32) mine |= __ldg(row + i) == ps;
+          if (!__any_sync(0xffffffffu, mine)) {
+            if (ptid == 0) {
+              toks[npool + nadd] = (int32_t)s;
+              atomicOr(&vm[(npool + nadd) >> 5], 1u << ((npool + nadd) & 31));
+            }
+            ++nadd;
+          }
+        }
+        if (ptid == 0) *s_nadd = nadd;
+      }
+      named_sync(2, kProdThreads);
+      const int n = npool + *s_nadd;
+      const int ntiles = (n + kTileK - 1) / kTileK;
+      for (int i = n + ptid; i < ntiles * kTileK; i += kProdThreads) toks[i] = -1;
+      named_sync(2, kProdThreads);
+      if (ptid == 0) ntok[buf] = n;
+      mbar_arrive(toks_full(buf));  // release: list, mask and count
+      if (ntiles == 0) continue;
+      // ---- Q rows of this head block by TMA (box {64, NH} per 64-wide d)
+      if (ptid == 0 && W.wait(q_empty, (nq & 1u) ^ 1u)) {
+        mbar_expect_tx(q_full, C::kQBytes);
+#pragma unroll
+        for (int a = 0; a < D / 64; ++a)
+          tma_load_2d(sQ + a * (NH * 128), &q_map, a * 64,
+                      (int32_t)(t * H + hb * 64), q_full);
+      }
+      ++nq;
+      // ---- K then V slices of every tile through the stage ring; thread
+      // ptid copies key row ptid of the tile (256 bytes per slice)
+      bool ok = true;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int32_t my_tok = toks[j * kTileK + ptid];
+        const int64_t src_row = my_tok >= 0 ? my_tok : 0;
+        const uint32_t nbytes = my_tok >= 0 ? 16u : 0u;
+        for (int kv = 0; kv < 2 && ok; ++kv) {
+          const __nv_bfloat16* srcb = (kv == 0 ? k : v) + src_row * D;
+          for (int c = 0; c < C::kChunks; ++c, ++u) {
+            const int s = (int)(u % kStages);
+            if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
+            const uint32_t st = sStage + s * kStageBytes;
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+              for (int ch = 0; ch < 8; ++ch)
+                cp_async16(st + a * 16384 + ptid * 128 + ((ch ^ (ptid & 7)) << 4),
+                           srcb + c * 128 + a * 64 + ch * 8, nbytes);
+            cp_async_mbar_arrive(full(s));
+          }
+        }
+      }
+      if (!ok) break;
+    }
+    asm volatile("cp.async.wait_all;" ::: "memory");
+  } else if (warp == C::kMmaWarp) {
+    // ================================================== MMA issuer
+    if (lane == 0) {
+      uint32_t u = 0, ntile_all = 0, nq = 0;
+      int qi = 0;
+      bool issued = false, ok = true;
+      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
+        const int buf = qi & 1;
+        if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
+        const int n = ntok[buf];
+        const int ntiles = (n + kTileK - 1) / kTileK;
+        if (ntiles == 0) continue;
+        if (!(ok = W.wait(q_full, nq & 1u))) break;
+        for (int j = 0; j < ntiles && ok; ++j, ++ntile_all) {
+          // ---- S^T = K_tile Q^T (accumulated over the D/128 slices)
+          for (int c = 0; c < C::kChunks; ++c, ++u) {
+            const int s = (int)(u % kStages);
+            if (!(ok = W.wait(full(s), (u / kStages) & 1u))) break;
+            fence_proxy_async();  // cp.async (generic) -> tensor core (async)
+            tc_fence_after();
+            const uint32_t st = sStage + s * kStageBytes;
+#pragma unroll
+            for (int a = 0; a < 2; ++a)
+#pragma unroll
+              for (int kin = 0; kin < 4; ++kin) {
+                const uint64_t ad = sdesc_sw128(st + a * 16384 + kin * 32, 16, 1024);
+                const uint64_t bd =
+                    sdesc_sw128(sQ + (2 * c + a) * (NH * 128) + kin * 32, 16, 1024);
+                tc_mma(tS, ad, bd, IDESC_S, (c | a | kin) != 0 ? 1u : 0u);
+              }
+            issued = true;
+            tc_commit(empty(s));
+          }
+          if (!ok) break;
+          if (j == ntiles - 1) tc_commit(q_empty);
+          tc_commit(s_full);
+          // ---- O^T += V_tile^T P^T
+          if (!(ok = W.wait(p_full, ntile_all & 1u))) break;
+          if (j == 0 && !(ok = W.wait(o_empty, (nq & 1u) ^ 1u))) break;
+          tc_fence_after();
+          for (int c = 0; c < C::kChunks; ++c, ++u) {
+            const int s = (int)(u % kStages);
+            if (!(ok = W.wait(full(s), (u / kStages) & 1u))) break;
+            fence_proxy_async();
+            tc_fence_after();
+            const uint32_t st = sStage + s * kStageBytes;
+#pragma unroll
+            for (int ks = 0; ks < kTileK / 16; ++ks) {
+              // A = V^T [128 dv x 16 keys], MN-major: two 64-dv atoms 16 KB
+              // apart (LBO), 8-key groups 1024 B apart (SBO)
+              const uint64_t ad = sdesc_sw128(st + ks * 2048, 16384, 1024);
+              // B = P^T [NH heads x 16 keys], K-major rows of 128 keys
+              const uint64_t bd =
+                  sdesc_sw128(sP + (ks >> 2) * (NH * 128) + (ks & 3) * 32, 16, 1024);
+              tc_mma(tO + c * NH, ad, bd, IDESC_O, (j | ks) != 0 ? 1u : 0u);
+            }
+            tc_commit(empty(s));
+          }
+          if (ok && j == ntiles - 1) tc_commit(pv_done);
+        }
+        ++nq;
+      }
+      if (issued) {
+        tc_commit(done_bar);
+        drain(done_bar, 0, timeout_ns);
+      }
+    }
+  } else {
+    // ============================== softmax + epilogue (128 per group)
+    const int i = tid & 127;  // key lane while scoring, dv lane in epilogue
+    const int grp = tid >> 7;  // heads grp*HPG .. grp*HPG+HPG-1
+    const int h0g = grp * HPG;
+    const int wq = warp & 3;   // TMEM lane quadrant
+    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    uint32_t ntile_all = 0, nq = 0;
+    int qi = 0;
+    // address pieces of P^T element (h, key i), K-major 128-byte rows
+    const uint32_t p_off = (uint32_t)(i >> 6) * (NH * 128) + (uint32_t)(i & 7) * 2;
+    const uint32_t p_chunk = (uint32_t)((i & 63) >> 3);
+    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++qi) {
+      const int64_t t = S - 1 - item / n_hblk;
+      const int hb = (int)(item % n_hblk);
+      const int hcount = min(NH, H - hb * 64);
+      const int buf = qi & 1;
+      if (!W.wait(toks_full(buf), (qi >> 1) & 1)) break;
+      const int n = ntok[buf];
+      const uint32_t* vm = vmask + buf * kMaskWords;
+      const int ntiles = (n + kTileK - 1) / kTileK;
+      __nv_bfloat16* orow = o + (t * H + hb * 64) * (int64_t)D;
+      if (ntiles == 0) {  // empty key set: O = 0, LSE = -inf
+        for (int e = tid; e < hcount * D; e += kSoftmaxThreads)
+          orow[e] = __float2bfloat16_rn(0.f);
+        if (tid < hcount) lse[t * H + hb * 64 + tid] = -INFINITY;
+        mbar_arrive(toks_empty(buf));
+        continue;
+      }
+      if (tid < NH) m_s[tid] = -INFINITY;
+      float l[HPG];
+#pragma unroll
+      for (int h = 0; h < HPG; ++h) l[h] = 0.f;
+      bool ok = true;
+      for (int j = 0; j < ntiles; ++j, ++ntile_all) {
+        if (!(ok = W.wait(s_full, ntile_all & 1u))) break;
+        tc_fence_after();
+        float s[HPG];
+        tmem_ld_row<HPG>(tS + lane_base + h0g, s);
+        const int slot = j * kTileK + i;
+        const bool valid = (vm[slot >> 5] >> (slot & 31)) & 1u;
+#pragma unroll
+        for (int h = 0; h < HPG; ++h) {
+          s[h] = valid ? s[h] * scale_log2 : -INFINITY;
+          float x = s[h];
+#pragma unroll
+          for (int sh = 16; sh > 0; sh >>= 1)
+            x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
+          if (lane == 0) red[wq * NH + h0g + h] = x;
+        }
+        named_sync(1, kSoftmaxThreads);
+        if (tid == 0) flags[(j + 1) & 1] = 0;
+        if (tid < NH) {
+          const float tm = fmaxf(fmaxf(red[tid], red[NH + tid]),
+                                 fmaxf(red[2 * NH + tid], red[3 * NH + tid]));
+          const float mo = m_s[tid];
+          // raise the running max only when this tile beats it by > 2^8
+          const bool raise = tm > mo + kMaxSlack || (mo == -INFINITY && tm > mo);
+          alpha_s[tid] = raise && mo != -INFINITY ? exp2f(mo - tm) : 1.f;
+          if (raise) {
+            m_s[tid] = tm;
+            if (j > 0) flags[j & 1] = 1;
+          }
+        }
+        named_sync(1, kSoftmaxThreads);
+        const bool rescale = flags[j & 1] != 0;
+        if (rescale) {
+          // PV of the previous tile has completed (it precedes this S^T)
+#pragma unroll 1
+          for (int c = 0; c < C::kChunks; ++c) {
+#pragma unroll
+            for (int hh = 0; hh < HPG; hh += 16) {
+              uint32_t r[16];
+              const uint32_t ta = tO + lane_base + c * NH + h0g + hh;
+              tmem_ld16(ta, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha_s[h0g + hh + e]);
+              tmem_st16(ta, r);
+            }
+          }
+          tmem_wait_st();
+        }
+        // P = exp2(s - m) -> row sums and P^T (bf16) in shared memory
+#pragma unroll
+        for (int h = 0; h < HPG; ++h) {
+          const int hh = h0g + h;
+          const float mh = m_s[hh];
+          const float p = exp2f(s[h] - (mh == -INFINITY ? 0.f : mh));
+          l[h] = l[h] * alpha_s[hh] + p;
+          const uint32_t addr = sP + p_off + (uint32_t)hh * 128u +
+                                ((p_chunk ^ (uint32_t)(hh & 7)) << 4);
+          const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
+                       "h"(*reinterpret_cast<const uint16_t*>(&pb))
+                       : "memory");
+        }
+        fence_proxy_async();  // P^T writes -> tensor core reads
+        tc_fence_before();
+        mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      // ---- epilogue: last PV done -> row sums, LSE, O = O^T / l
+      if (!W.wait(pv_done, nq & 1u)) break;
+      tc_fence_after();
+#pragma unroll
+      for (int h = 0; h < HPG; ++h) {
+        float x = l[h];
+#pragma unroll
+        for (int sh = 16; sh > 0; sh >>= 1) x += __shfl_xor_sync(0xffffffffu, x, sh);
+        if (lane == 0) red[wq * NH + h0g + h] = x;
+      }
+      named_sync(1, kSoftmaxThreads);
+      if (tid < NH) {
+        const float lt =
+            red[tid] + red[NH + tid] + red[2 * NH + tid] + red[3 * NH + tid];
+        inv_s[tid] = lt > 0.f ? 1.f / lt : 0.f;
+        if (tid < hcount)
+          lse[t * H + hb * 64 + tid] =
+              lt > 0.f ? (m_s[tid] + log2f(lt)) * kLn2 : -INFINITY;
+      }
+      named_sync(1, kSoftmaxThreads);
+#pragma unroll 1
+      for (int c = 0; c < C::kChunks; ++c) {
+        float ov[HPG];
+        tmem_ld_row<HPG>(tO + lane_base + c * NH + h0g, ov);
+        const int d = c * 128 + i;
+#pragma unroll
+        for (int h = 0; h < HPG; ++h)
+          if (h0g + h < hcount)
+            orow[(h0g + h) * (int64_t)D + d] = __float2bfloat16_rn(ov[h] * inv_s[h0g + h]);
+      }
+      tc_fence_before();
+      mbar_arrive(o_empty);
+      mbar_arrive(toks_empty(buf));
+      ++nq;
+    }
+  }
+
+  // ---- teardown: every role has left its loop, no MMA or copy in flight
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == C::kMmaWarp) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+template <int D, int NH>
+cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& qm,
+                     const __nv_bfloat16* k, const __nv_bfloat16* v,
+                     const int32_t* idx, __nv_bfloat16* o, float* lse) {
+  using C = TcFwdCfg<D, NH>;
+  const int cap = (4 * s.K_p + s.n_loc + kTileK - 1) / kTileK * kTileK;
+  const uint32_t smem = C::smem(cap);
+  if (smem > 232448) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, NH>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  const int n_hblk = (s.H + 63) / 64;
+  const int64_t items = s.S * n_hblk;
+  int64_t grid = c.num_sms;
+  if (grid > items) grid = items;
+  attn_fwd_tc_kernel<D, NH><<<(unsigned)grid, C::kThreads, smem, c.stream>>>(
+      qm, k, v, idx, o, lse, s.S, s.H, s.K_p, s.n_loc, s.scale * kLog2e, n_hblk,
+      cap, c.status, c.timeout_ns);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int attn_tc_heads(int H) {
+  const int hb = H >= 64 ? 64 : H;
+  return hb <= 16 ? 16 : (hb <= 32 ? 32 : 64);
+}
+
+cudaError_t launch_attn_fwd_tc(const LaunchCtx& c, const AttnShape& s,
+                               const CUtensorMap& q_map, const __nv_bfloat16* k,
+                               const __nv_bfloat16* v, const int32_t* idx,
+                               __nv_bfloat16* o, float* lse) {
+  const int nh = attn_tc_heads(s.H);
+#define DSA_TCF(DD, NN) \
+  if (s.D == DD && nh == NN) return launch_t<DD, NN>(c, s, q_map, k, v, idx, o, lse);
+  DSA_TCF(128, 16) DSA_TCF(128, 32) DSA_TCF(128, 64)
+  DSA_TCF(256, 16) DSA_TCF(256, 32) DSA_TCF(256, 64)
+  DSA_TCF(512, 16) DSA_TCF(512, 32) DSA_TCF(512, 64)
+#undef DSA_TCF
+  return cudaErrorInvalidValue;
+}
+
+}  // namespace dsa

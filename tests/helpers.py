@@ -15,19 +15,32 @@ RTOL_BF16 = 2.0 ** -8
 TIE_BAND = 1e-3          # relative gap below which index sets may differ
 
 
-def assert_close(got, ref, name="", atol=ATOL_OUT, rtol=RTOL_BF16):
-    """max |got - ref| - rtol |ref| <= atol, with equal infinities allowed."""
+def assert_close(got, ref, name="", mag=None, atol=ATOL_OUT, rtol=RTOL_BF16):
+    """|got - ref| <= atol + rtol * mag elementwise, infinities equal.
+
+    mag is the magnitude the result is built from: |ref| by default, or,
+    where the oracle can give it, the sum of the absolute values of the
+    summed terms (e.g. sum_j P_j |v_j| for O, sum P |dO| for dV).  A
+    tensor-core product rounds its bf16 operands (P, dS) by up to 2^-9 each,
+    so its error scales with that sum, not with the (possibly cancelling)
+    result."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref, np.float64)
     assert got.shape == ref.shape, (name, got.shape, ref.shape)
+    m = np.abs(ref) if mag is None else np.maximum(np.abs(ref), np.abs(mag))
     inf = np.isinf(ref)
     assert np.array_equal(got[inf], ref[inf]), f"{name}: infinities differ"
-    g, r = got[~inf], ref[~inf]
+    g, r, m = got[~inf], ref[~inf], m[~inf]
     assert np.isfinite(g).all(), f"{name}: non-finite values"
     if g.size:
-        excess = (np.abs(g - r) - rtol * np.abs(r)).max()
+        excess = (np.abs(g - r) - rtol * m).max()
         err = np.abs(g - r).max()
         assert excess <= atol, f"{name}: max err {err:.3g} (excess {excess:.3g})"
+
+
+def abs_bits(b: np.ndarray) -> np.ndarray:
+    """|x| of bf16 bit patterns (clear the sign bit; exact)."""
+    return np.asarray(b, np.uint16) & np.uint16(0x7FFF)
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
