@@ -77,7 +77,7 @@ typedef struct dsa_config {
   int32_t idx_heads;   /* H_I in {1,2,4,8,16,32,64} */
   int32_t idx_dim;     /* D_I in {64,128} */
   int32_t attn_heads;  /* H, 1..128 */
-  int32_t d_qk;        /* NoPE q/k dim in {64,128,256,512} */
+  int32_t d_qk;        /* NoPE q/k dim in {128,256,512} */
   int32_t d_v;         /* must equal d_qk */
   int32_t chunk_q;     /* C, queries scored per indexer chunk, >= 1 */
   float sm_scale;      /* softmax scale; 0 -> 1/sqrt(d_qk) */
@@ -178,6 +178,10 @@ DSA_API const char* dsa_status_string(dsa_status_t status);
 
 /* DSA_ABI_VERSION of the loaded library. */
 DSA_API int32_t dsa_abi_version(void);
+
+/* Name of the CUDA runtime error behind the calling thread's most recent
+ * DSA_ERR_CUDA (static string; "no error" if there was none). */
+DSA_API const char* dsa_last_cuda_error(void);
 
 #ifdef __cplusplus
 }

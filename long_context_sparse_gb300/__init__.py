@@ -48,14 +48,15 @@ EXPORTS = [
     "dsa_workspace_size", "dsa_workspace_init", "dsa_pool_keys",
     "dsa_index_scores", "dsa_topk_from_scores", "dsa_index_scores_topk",
     "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_get_device_status",
-    "dsa_status_string", "dsa_abi_version",
+    "dsa_status_string", "dsa_abi_version", "dsa_last_cuda_error",
 ]
 
 
 class DsaError(RuntimeError):
-    def __init__(self, code: int, where: str):
+    def __init__(self, code: int, where: str, detail: str = ""):
         self.code = int(code)
-        super().__init__(f"{where}: {STATUS_NAMES.get(self.code, self.code)}")
+        msg = f"{where}: {STATUS_NAMES.get(self.code, self.code)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
 
 
 class _CConfig(ctypes.Structure):
@@ -145,6 +146,8 @@ def _load():
         lib.dsa_status_string.restype = ctypes.c_char_p
         lib.dsa_abi_version.argtypes = []
         lib.dsa_abi_version.restype = ctypes.c_int32
+        lib.dsa_last_cuda_error.argtypes = []
+        lib.dsa_last_cuda_error.restype = ctypes.c_char_p
         _lib = lib
         return lib
 
@@ -155,7 +158,8 @@ def status_string(code: int) -> str:
 
 def _check(rc: int, where: str):
     if rc != 0:
-        raise DsaError(rc, where)
+        detail = _load().dsa_last_cuda_error().decode() if rc == 5 else ""
+        raise DsaError(rc, where, detail)
 
 
 def _stream(dev: torch.device):

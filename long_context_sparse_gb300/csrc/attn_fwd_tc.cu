@@ -19,10 +19,11 @@
 // raised when a tile beats it by more than 2^8, so O^T is rarely rescaled
 // (the final normalisation uses the same maximum, so the result is exact).
 //
-// Warps: 0-3 softmax / epilogue (TMEM lane quadrants 0-3), 4-7 gather
-// producers (cp.async of the selected K/V rows into 128-byte-swizzled
-// stages, completion signalled on an mbarrier), 8 MMA issuer and TMEM
-// owner.  Q comes in by TMA.  Every wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
+// Warps: 4 or 8 softmax / epilogue warps (one warpgroup per 32 heads; warp
+// w reads TMEM lane quadrant w % 4), 2 gather producers (cp.async of the
+// selected K/V rows into 128-byte-swizzled stages, completion signalled on
+// an mbarrier), 1 MMA issuer and TMEM owner.  Q comes in by TMA.  Every
+// wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
 #include "attn_common.cuh"
 #include "dsa_internal.h"
 
@@ -32,7 +33,7 @@ namespace {
 constexpr int kTileK = 128;            // keys per tile (MMA M)
 constexpr int kStages = 4;             // gather ring depth
 constexpr uint32_t kStageBytes = 32768;  // 128 keys x 128 dims (2 atoms)
-constexpr int kProdThreads = 128;
+constexpr int kProdThreads = 64;     // 2 gather warps, 2 key rows each
 constexpr float kMaxSlack = 8.0f;      // log2 headroom before raising a max
 constexpr int kMaskWords = (2048 * 4 + 3 + kTileK + 31) / 32;
 
@@ -43,17 +44,19 @@ struct TcFwdCfg {
   static constexpr int HPG = NH / kGroups;
   static constexpr int kSoftmaxThreads = 128 * kGroups;
   static constexpr int kProdWarp0 = 4 * kGroups;       // first producer warp
-  static constexpr int kMmaWarp = kProdWarp0 + 4;
+  static constexpr int kMmaWarp = kProdWarp0 + kProdThreads / 32;
   static constexpr int kThreads = kSoftmaxThreads + kProdThreads + 32;
-  // registers per thread: the whole register file for one CTA per SM
-  static constexpr int kMaxReg = (65536 / kThreads) & ~7;
+  // registers per thread: warps are spread over the SM's 4 sub-partitions
+  // of 16K registers each, so the fullest one holds ceil(warps/4) warps
+  static constexpr int kMaxReg = (16384 / (((kThreads / 32) + 3) / 4 * 32)) & ~7;
   static constexpr int kChunks = D / 128;  // 128-wide d slices
   static constexpr uint32_t kQBytes = NH * D * 2;
   static constexpr uint32_t kPBytes = NH * kTileK * 2;
   static constexpr uint32_t kTmemCols = NH + kChunks * NH <= 256 ? 256 : 512;
   // dynamic shared memory for a key list of `cap` entries
-  static uint32_t smem(int cap) {
-    return 1024 + kQBytes + kPBytes + kStages * kStageBytes + cap * 4 +
+  // dynamic shared memory: the selected pool ids (K_p) + 4 local tokens
+  static uint32_t smem(int K_p) {
+    return 1024 + kQBytes + kPBytes + kStages * kStageBytes + (K_p + 4) * 4 +
            2 * kMaskWords * 4 + (4 * NH + 3 * NH + 8) * 4 + 256;
   }
 };
@@ -62,6 +65,12 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar)
                : "memory");
 }
+// Bring `bytes` (multiple of 16) at a 16-byte aligned address into L2.
+__device__ __forceinline__ void l2_prefetch_row(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes)
+               : "memory");
+}
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -85,6 +94,20 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[NH]) {
   for (int c = 0; c < NH; ++c) v[c] = __uint_as_float(r[c]);
 }
 
+// A barrier among the threads of one role built on an mbarrier, so that a
+// thread whose wait gave up cannot leave its peers blocked: every wait here
+// is bounded like the others.
+struct GroupBar {
+  uint32_t bar;
+  uint32_t phase;
+  __device__ __forceinline__ bool sync(const Waiter& W) {
+    mbar_arrive(bar);
+    const bool ok = W.wait(bar, phase & 1u);
+    ++phase;
+    return ok;
+  }
+};
+
 __device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, uint64_t ns) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, parity))
@@ -100,7 +123,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
                        const int32_t* __restrict__ idx,
                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                        int64_t S, int H, int K_p, int n_loc, float scale_log2,
-                       int n_hblk, int tok_cap, uint32_t* status,
+                       int n_hblk, uint32_t* status,
                        uint64_t timeout_ns) {
   using C = TcFwdCfg<D, NH>;
   constexpr int HPG = C::HPG;
@@ -115,9 +138,12 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   const uint32_t sQ = base;
   const uint32_t sP = sQ + C::kQBytes;
   const uint32_t sStage = sP + C::kPBytes;  // 1024-aligned (sizes are)
-  int32_t* toks = reinterpret_cast<int32_t*>(gb + C::kQBytes + C::kPBytes +
-                                             kStages * kStageBytes);
-  uint32_t* vmask = reinterpret_cast<uint32_t*>(toks + tok_cap);  // [2][words]
+  // key list of the current query as pool ids (slot 4i+j <-> token
+  // 4*pools[i]+j, -1 = empty) followed by up to 3 local tokens
+  int32_t* pools = reinterpret_cast<int32_t*>(gb + C::kQBytes + C::kPBytes +
+                                              kStages * kStageBytes);
+  int32_t* locs = pools + K_p;
+  uint32_t* vmask = reinterpret_cast<uint32_t*>(locs + 4);  // [2][words]
   float* red = reinterpret_cast<float*>(vmask + 2 * kMaskWords);  // [4][NH]
   float* m_s = red + 4 * NH;                                      // [NH]
   float* alpha_s = m_s + NH;                                      // [NH]
@@ -137,9 +163,11 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   const uint32_t done_bar = q_full + 48u;
   auto toks_full = [&](int b) { return q_full + 56u + 8u * b; };
   auto toks_empty = [&](int b) { return q_full + 72u + 8u * b; };
+  const uint32_t sm_grp = q_full + 88u;    // softmax group barrier
+  const uint32_t prod_grp = q_full + 96u;  // producer group barrier
   volatile uint32_t* abort_flag =
-      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 11);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 12);
+      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 13);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 14);
   int* ntok = misc;
   int* s_last = misc + 2;
   int* s_nadd = misc + 3;
@@ -165,6 +193,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       mbar_init(toks_full(b), kProdThreads);
       mbar_init(toks_empty(b), kSoftmaxThreads);
     }
+    mbar_init(sm_grp, kSoftmaxThreads);
+    mbar_init(prod_grp, kProdThreads);
     *abort_flag = 0u;
     flags[0] = flags[1] = 0;
     fence_mbar_init();
@@ -181,6 +211,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   if (warp >= C::kProdWarp0 && warp < C::kMmaWarp) {
     // ============================================ gather producers (128)
     const int ptid = tid - kSoftmaxThreads;
+    GroupBar G{prod_grp, 0u};
     uint32_t u = 0, nq = 0;
     int qi = 0;
     for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++qi) {
@@ -199,7 +230,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         *s_nadd = 0;
       }
       for (int w = ptid; w < kMaskWords; w += kProdThreads) vm[w] = 0u;
-      named_sync(2, kProdThreads);
+      if (!G.sync(W)) break;
       for (int i = ptid; i < K_p; i += kProdThreads) {
         const int32_t p = __ldg(row + i);
         const bool okp = p >= 0 && (int64_t)p < nf;
@@ -207,11 +238,10 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
           atomicMax(s_last, i);
           if (!okp) latch_error(status, DSA_ERR_DEVICE_BAD_INDEX);
         }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) toks[4 * i + j] = okp ? 4 * p + j : -1;
+        pools[i] = okp ? p : -1;
         if (okp) atomicOr(&vm[(4 * i) >> 5], 0xFu << ((4 * i) & 31));
       }
-      named_sync(2, kProdThreads);
+      if (!G.sync(W)) break;
       const int npool = 4 * (*s_last + 1);
       if (n_loc > 0 && ptid < 32) {
         int nadd = 0;
@@ -224,7 +254,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             for (int i = ptid; i < K_p; i += 32) mine |= __ldg(row + i) == ps;
           if (!__any_sync(0xffffffffu, mine)) {
             if (ptid == 0) {
-              toks[npool + nadd] = (int32_t)s;
+              locs[nadd] = (int32_t)s;
               atomicOr(&vm[(npool + nadd) >> 5], 1u << ((npool + nadd) & 31));
             }
             ++nadd;
@@ -232,11 +262,10 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         }
         if (ptid == 0) *s_nadd = nadd;
       }
-      named_sync(2, kProdThreads);
+      if (!G.sync(W)) break;
       const int n = npool + *s_nadd;
       const int ntiles = (n + kTileK - 1) / kTileK;
-      for (int i = n + ptid; i < ntiles * kTileK; i += kProdThreads) toks[i] = -1;
-      named_sync(2, kProdThreads);
+      if (!G.sync(W)) break;
       if (ptid == 0) ntok[buf] = n;
       mbar_arrive(toks_full(buf));  // release: list, mask and count
       if (ntiles == 0) continue;
@@ -250,24 +279,56 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       }
       ++nq;
       // ---- K then V slices of every tile through the stage ring; thread
-      // ptid copies key row ptid of the tile (256 bytes per slice)
+      // ptid copies key rows ptid and ptid+64 of the tile (256 B per slice)
+      auto tok_of = [&](int slot) -> int32_t {
+        if (slot < npool) {
+          const int32_t p = pools[slot >> 2];
+          return p >= 0 ? 4 * p + (slot & 3) : -1;
+        }
+        return slot < n ? locs[slot - npool] : -1;
+      };
+      // rows of tile 0 go to L2 ahead of their gather
+#pragma unroll
+      for (int rr = 0; rr < 2; ++rr) {
+        const int32_t tk0 = tok_of(ptid + 64 * rr);
+        if (tk0 >= 0) {
+          l2_prefetch_row(k + (int64_t)tk0 * D, D * 2);
+          l2_prefetch_row(v + (int64_t)tk0 * D, D * 2);
+        }
+      }
       bool ok = true;
       for (int j = 0; j < ntiles && ok; ++j) {
-        const int32_t my_tok = toks[j * kTileK + ptid];
-        const int64_t src_row = my_tok >= 0 ? my_tok : 0;
-        const uint32_t nbytes = my_tok >= 0 ? 16u : 0u;
+        int64_t src_row[2];
+        uint32_t nbytes[2];
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+          const int32_t tok = tok_of(j * kTileK + ptid + 64 * rr);
+          src_row[rr] = tok >= 0 ? tok : 0;
+          nbytes[rr] = tok >= 0 ? 16u : 0u;
+          // the next tile's rows: HBM -> L2 while this tile is gathered
+          const int32_t nxt = j + 1 < ntiles ? tok_of((j + 1) * kTileK + ptid + 64 * rr) : -1;
+          if (nxt >= 0) {
+            l2_prefetch_row(k + (int64_t)nxt * D, D * 2);
+            l2_prefetch_row(v + (int64_t)nxt * D, D * 2);
+          }
+        }
         for (int kv = 0; kv < 2 && ok; ++kv) {
-          const __nv_bfloat16* srcb = (kv == 0 ? k : v) + src_row * D;
+          const __nv_bfloat16* src = kv == 0 ? k : v;
           for (int c = 0; c < C::kChunks; ++c, ++u) {
             const int s = (int)(u % kStages);
             if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
             const uint32_t st = sStage + s * kStageBytes;
 #pragma unroll
-            for (int a = 0; a < 2; ++a)
+            for (int rr = 0; rr < 2; ++rr) {
+              const int r = ptid + 64 * rr;
+              const __nv_bfloat16* srcb = src + src_row[rr] * D + c * 128;
 #pragma unroll
-              for (int ch = 0; ch < 8; ++ch)
-                cp_async16(st + a * 16384 + ptid * 128 + ((ch ^ (ptid & 7)) << 4),
-                           srcb + c * 128 + a * 64 + ch * 8, nbytes);
+              for (int a = 0; a < 2; ++a)
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                  cp_async16(st + a * 16384 + r * 128 + ((ch ^ (r & 7)) << 4),
+                             srcb + a * 64 + ch * 8, nbytes[rr]);
+            }
             cp_async_mbar_arrive(full(s));
           }
         }
@@ -349,6 +410,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
     const int h0g = grp * HPG;
     const int wq = warp & 3;   // TMEM lane quadrant
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    GroupBar G{sm_grp, 0u};
     uint32_t ntile_all = 0, nq = 0;
     int qi = 0;
     // address pieces of P^T element (h, key i), K-major 128-byte rows
@@ -392,7 +454,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
           if (lane == 0) red[wq * NH + h0g + h] = x;
         }
-        named_sync(1, kSoftmaxThreads);
+        if (!(ok = G.sync(W))) break;
         if (tid == 0) flags[(j + 1) & 1] = 0;
         if (tid < NH) {
           const float tm = fmaxf(fmaxf(red[tid], red[NH + tid]),
@@ -406,7 +468,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             if (j > 0) flags[j & 1] = 1;
           }
         }
-        named_sync(1, kSoftmaxThreads);
+        if (!(ok = G.sync(W))) break;
         const bool rescale = flags[j & 1] != 0;
         if (rescale) {
           // PV of the previous tile has completed (it precedes this S^T)
@@ -455,7 +517,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         for (int sh = 16; sh > 0; sh >>= 1) x += __shfl_xor_sync(0xffffffffu, x, sh);
         if (lane == 0) red[wq * NH + h0g + h] = x;
       }
-      named_sync(1, kSoftmaxThreads);
+      if (!G.sync(W)) break;
       if (tid < NH) {
         const float lt =
             red[tid] + red[NH + tid] + red[2 * NH + tid] + red[3 * NH + tid];
@@ -464,7 +526,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
           lse[t * H + hb * 64 + tid] =
               lt > 0.f ? (m_s[tid] + log2f(lt)) * kLn2 : -INFINITY;
       }
-      named_sync(1, kSoftmaxThreads);
+      if (!G.sync(W)) break;
 #pragma unroll 1
       for (int c = 0; c < C::kChunks; ++c) {
         float ov[HPG];
@@ -494,20 +556,36 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
                      const __nv_bfloat16* k, const __nv_bfloat16* v,
                      const int32_t* idx, __nv_bfloat16* o, float* lse) {
   using C = TcFwdCfg<D, NH>;
-  const int cap = (4 * s.K_p + s.n_loc + kTileK - 1) / kTileK * kTileK;
-  const uint32_t smem = C::smem(cap);
+  const uint32_t smem = C::smem(s.K_p);
   if (smem > 232448) return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(attn_fwd_tc_kernel<D, NH>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_fwd_tc_kernel<D, NH>,
+                                                    C::kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) {
+    cudaFuncAttributes fa;
+    cudaFuncGetAttributes(&fa, attn_fwd_tc_kernel<D, NH>);
+    int dev = 0, optin = 0, per_smem = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    cudaDeviceGetAttribute(&per_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+    set_error_detail("attn_fwd_tc occupancy 0: regs=%d threads=%d static_smem=%zu "
+                     "dyn_smem=%u optin=%d smem_per_sm=%d max_threads=%d",
+                     fa.numRegs, C::kThreads, fa.sharedSizeBytes, smem, optin,
+                     per_smem, fa.maxThreadsPerBlock);
+    return cudaErrorLaunchOutOfResources;
+  }
   const int n_hblk = (s.H + 63) / 64;
   const int64_t items = s.S * n_hblk;
   int64_t grid = c.num_sms;
   if (grid > items) grid = items;
   attn_fwd_tc_kernel<D, NH><<<(unsigned)grid, C::kThreads, smem, c.stream>>>(
       qm, k, v, idx, o, lse, s.S, s.H, s.K_p, s.n_loc, s.scale * kLog2e, n_hblk,
-      cap, c.status, c.timeout_ns);
+      c.status, c.timeout_ns);
   return cudaGetLastError();
 }
 

@@ -3,6 +3,8 @@
 // code only; every step of the path runs in this library's kernels.
 #include <cudaTypedefs.h>
 #include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
 #include <stdlib.h>
 #include <string.h>
 
@@ -21,6 +23,11 @@ constexpr int kMaxDevices = 64;
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Name of the CUDA error behind the last DSA_ERR_CUDA of this thread.
+thread_local const char* t_last_cuda_error = "no error";
+thread_local char t_detail[512] = "";
+thread_local bool t_detail_set = false;
 
 struct DeviceInfo {
   int num_sms = 0;
@@ -59,8 +66,10 @@ dsa_status_t get_encoder(PFN_cuTensorMapEncodeTiled_v12000* fn) {
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
                                          cudaEnableDefault, &q) != cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || !p)
+        q != cudaDriverEntryPointSuccess || !p) {
+      t_last_cuda_error = "cudaGetDriverEntryPointByVersion";
       return DSA_ERR_CUDA;
+    }
     g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
   }
   *fn = g_encode;
@@ -81,7 +90,11 @@ dsa_status_t encode_2d(CUtensorMap* map, const void* base, uint64_t rows,
                   dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                   CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS ? DSA_OK : DSA_ERR_CUDA;
+  if (r != CUDA_SUCCESS) {
+    t_last_cuda_error = "cuTensorMapEncodeTiled";
+    return DSA_ERR_CUDA;
+  }
+  return DSA_OK;
 }
 
 uint64_t timeout_ns() {
@@ -118,7 +131,7 @@ dsa_status_t check_cfg(const dsa_config_t* c, bool need_index, bool need_attn) {
   }
   if (need_attn) {
     if (c->attn_heads > 128) return DSA_ERR_UNSUPPORTED_SHAPE;
-    if (c->d_qk != 64 && c->d_qk != 128 && c->d_qk != 256 && c->d_qk != 512)
+    if (c->d_qk != 128 && c->d_qk != 256 && c->d_qk != 512)
       return DSA_ERR_UNSUPPORTED_SHAPE;
     if (c->d_v != c->d_qk) return DSA_ERR_UNSUPPORTED_SHAPE;
   }
@@ -167,7 +180,16 @@ dsa_status_t make_ctx(void* ws, void* stream, LaunchCtx* ctx) {
   return DSA_OK;
 }
 
-dsa_status_t cuda_status(cudaError_t e) { return e == cudaSuccess ? DSA_OK : DSA_ERR_CUDA; }
+dsa_status_t cuda_status(cudaError_t e) {
+  if (e == cudaSuccess) return DSA_OK;
+  if (t_detail_set) {
+    t_last_cuda_error = t_detail;
+    t_detail_set = false;
+  } else {
+    t_last_cuda_error = cudaGetErrorName(e);
+  }
+  return DSA_ERR_CUDA;
+}
 
 dsa_status_t check_ws(const dsa_config_t* cfg, int which, void* ws, size_t ws_bytes) {
   if (!ws) return DSA_ERR_INVALID_ARG;
@@ -188,6 +210,15 @@ AttnShape attn_shape(const dsa_config_t* c) {
 }
 
 }  // namespace
+
+void set_error_detail(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(t_detail, sizeof t_detail, fmt, ap);
+  va_end(ap);
+  t_detail_set = true;
+}
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -195,6 +226,8 @@ using namespace dsa;
 extern "C" {
 
 int32_t dsa_abi_version(void) { return DSA_ABI_VERSION; }
+
+const char* dsa_last_cuda_error(void) { return t_last_cuda_error; }
 
 const char* dsa_status_string(dsa_status_t s) {
   switch (s) {
@@ -313,7 +346,7 @@ dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg, const void* q_idx,
   if (P > 0) {
     cudaError_t e = launch_pool(ctx, static_cast<const __nv_bfloat16*>(k_idx), k_pool,
                                 S, cfg->idx_dim);
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
     if ((st = encode_2d(&qm, q_idx, (uint64_t)(S * cfg->idx_heads), cfg->idx_dim,
                         256)) != DSA_OK)
       return st;
@@ -326,11 +359,11 @@ dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg, const void* q_idx,
     if (p_lim > cfg->topk_pools) {  // some row has more pools than K_p: score
       cudaError_t e = launch_indexer(ctx, qm, km, w, cfg->idx_heads, cfg->idx_dim, t0,
                                      rows, p_lim, scores, ld);
-      if (e != cudaSuccess) return DSA_ERR_CUDA;
+      if (e != cudaSuccess) return cuda_status(e);
     }
     cudaError_t e = launch_topk(ctx, scores, ld, t0, rows, cfg->topk_pools,
                                 topk_idx + t0 * cfg->topk_pools);
-    if (e != cudaSuccess) return DSA_ERR_CUDA;
+    if (e != cudaSuccess) return cuda_status(e);
   }
   return DSA_OK;
 }
@@ -347,10 +380,14 @@ dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q, const v
     return DSA_ERR_MISALIGNED;
   LaunchCtx ctx;
   if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
-  cudaError_t e = launch_attn_fwd(ctx, attn_shape(cfg), static_cast<const __nv_bfloat16*>(q),
-                                  static_cast<const __nv_bfloat16*>(k),
-                                  static_cast<const __nv_bfloat16*>(v), topk_idx,
-                                  static_cast<__nv_bfloat16*>(o), lse);
+  const AttnShape s = attn_shape(cfg);
+  CUtensorMap qm;
+  if ((st = encode_2d(&qm, q, (uint64_t)(s.S * s.H), (uint64_t)s.D,
+                      (uint32_t)attn_tc_heads(s.H))) != DSA_OK)
+    return st;
+  cudaError_t e = launch_attn_fwd_tc(ctx, s, qm, static_cast<const __nv_bfloat16*>(k),
+                                     static_cast<const __nv_bfloat16*>(v), topk_idx,
+                                     static_cast<__nv_bfloat16*>(o), lse);
   return e == cudaErrorInvalidValue ? DSA_ERR_UNSUPPORTED_SHAPE : cuda_status(e);
 }
 
@@ -379,14 +416,14 @@ dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q, const v
   cudaError_t e = launch_attn_bwd_pre(ctx, s, static_cast<const __nv_bfloat16*>(o),
                                       static_cast<const __nv_bfloat16*>(dO), delta,
                                       dk_acc, dv_acc);
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   e = launch_attn_bwd(ctx, s, static_cast<const __nv_bfloat16*>(q),
                       static_cast<const __nv_bfloat16*>(k),
                       static_cast<const __nv_bfloat16*>(v),
                       static_cast<const __nv_bfloat16*>(dO), lse, delta, topk_idx,
                       static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc);
   if (e == cudaErrorInvalidValue) return DSA_ERR_UNSUPPORTED_SHAPE;
-  if (e != cudaSuccess) return DSA_ERR_CUDA;
+  if (e != cudaSuccess) return cuda_status(e);
   e = launch_attn_bwd_finalize(ctx, s, dk_acc, dv_acc, static_cast<__nv_bfloat16*>(dk),
                                static_cast<__nv_bfloat16*>(dv));
   return cuda_status(e);

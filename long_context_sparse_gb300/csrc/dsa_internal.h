@@ -9,6 +9,10 @@
 
 namespace dsa {
 
+// Record a printf-style detail for the calling thread's next DSA_ERR_CUDA
+// (returned by dsa_last_cuda_error).
+void set_error_detail(const char* fmt, ...);
+
 struct LaunchCtx {
   cudaStream_t stream;
   uint32_t* status;     // device status word (workspace header)
@@ -41,11 +45,16 @@ struct AttnShape {
   float scale;
 };
 
-// a5 + a6: sparse attention forward.
-cudaError_t launch_attn_fwd(const LaunchCtx& c, const AttnShape& s,
-                            const __nv_bfloat16* q, const __nv_bfloat16* k,
-                            const __nv_bfloat16* v, const int32_t* idx,
-                            __nv_bfloat16* o, float* lse);
+// Heads per tensor-core tile (N) of the attention kernels: H, or 64 per
+// head block, rounded up to 16, 32 or 64.
+int attn_tc_heads(int H);
+
+// a5 + a6: sparse attention forward (tcgen05).  q_map: q viewed as
+// [S*H, D] bf16, box {64, attn_tc_heads(H)}, 128-byte swizzle.
+cudaError_t launch_attn_fwd_tc(const LaunchCtx& c, const AttnShape& s,
+                               const CUtensorMap& q_map, const __nv_bfloat16* k,
+                               const __nv_bfloat16* v, const int32_t* idx,
+                               __nv_bfloat16* o, float* lse);
 
 // a7: delta = rowsum(dO * O); zero the fp32 dK/dV accumulators.
 cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,

@@ -59,6 +59,7 @@ constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 // Rows of up to this many candidates are staged in shared memory once.
 constexpr int kTopkCacheMax = 48 * 1024;
+constexpr int kBins = 2048;  // 11-bit digits: bits 31-21, 20-10, 9-0
 
 // Order-preserving image of an fp32 score: larger float -> larger key.
 // -0.0 is first made +0.0 so the two compare equal (lower index wins).
@@ -68,12 +69,45 @@ __device__ __forceinline__ uint32_t order_key(float f) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Digit d of the highest bins that holds the kk-th largest key; *above =
+// number of keys in higher bins.  Warp 0 only; lane l owns 64 bins.
+__device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t kk,
+                                           uint32_t* sel_digit, uint32_t* sel_above) {
+  const int lane = threadIdx.x & 31;
+  const int base = kBins - 64 * (lane + 1);  // lane 0: the top 64 bins
+  uint32_t s = 0u;
+#pragma unroll
+  for (int j = 0; j < 64; j += 4) {
+    const uint4 v = *reinterpret_cast<const uint4*>(hist + base + j);
+    s += v.x + v.y + v.z + v.w;
+  }
+  uint32_t incl = s;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += x;
+  }
+  const uint32_t excl = incl - s;
+  if (excl < kk && kk <= incl) {
+    uint32_t acc = excl;
+    for (int j = 63; j >= 0; --j) {
+      const uint32_t c = hist[base + j];
+      if (acc + c >= kk) {
+        *sel_digit = (uint32_t)(base + j);
+        *sel_above = acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kTopkThreads, 1)
     topk_rows_kernel(const float* __restrict__ scores, int64_t ld, int64_t row0,
                      int64_t rows, int K_p, int32_t* __restrict__ out,
                      int cache_cap) {
   extern __shared__ uint32_t cache[];
-  __shared__ uint32_t hist[256];
+  __shared__ __align__(16) uint32_t hist[kBins];
   __shared__ uint32_t wcnt[2][kTopkWarps];
   __shared__ uint32_t sel_digit, sel_above;
 
@@ -93,104 +127,79 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     }
     const bool cached = n <= cache_cap;
 
-    // ---- radix select of the K_p-th largest key, 8 bits per pass
+    // ---- radix select of the K_p-th largest key: digits of 11, 11, 10 bits
     uint32_t prefix = 0u, pmask = 0u, kk = (uint32_t)K_p;
-    for (int pass = 0; pass < 4; ++pass) {
-      const int shift = 24 - 8 * pass;
-      for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
+#pragma unroll 1
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+      const uint32_t dmask = pass == 2 ? 1023u : 2047u;
+      for (int i = tid; i < kBins; i += kTopkThreads) hist[i] = 0u;
       __syncthreads();
-      for (int64_t b = 0; b < n; b += kTopkThreads) {
-        const int64_t i = b + tid;
-        uint32_t key = 0u;
-        bool live = i < n;
-        if (live) {
-          if (pass == 0) {
-            key = order_key(__ldg(row + i));
-            if (cached) cache[i] = key;
-          } else {
-            key = cached ? cache[i] : order_key(__ldg(row + i));
-          }
-          live = (key & pmask) == prefix;
+      if (pass == 0) {
+        // first touch of the row: load, map, cache, count
+        for (int64_t i = tid; i < n; i += kTopkThreads) {
+          const uint32_t key = order_key(__ldg(row + i));
+          if (cached) cache[i] = key;
+          atomicAdd(&hist[key >> 21], 1u);
         }
-        // warp-aggregated histogram update (scores share few exponents)
-        const uint32_t digit = live ? (key >> shift) & 255u : 256u;
-        const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-        if (live && (peers & lane_lt) == 0u) atomicAdd(&hist[digit], __popc(peers));
+      } else {
+        for (int64_t i = tid; i < n; i += kTopkThreads) {
+          const uint32_t key = cached ? cache[i] : order_key(__ldg(row + i));
+          if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+        }
       }
       __syncthreads();
-      if (warp == 0) {
-        // lane l owns bins 8*(31-l) .. 8*(31-l)+7 (lane 0 = highest bins)
-        const int base = 8 * (31 - lane);
-        uint32_t c[8], s = 0u;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          c[j] = hist[base + j];
-          s += c[j];
-        }
-        uint32_t incl = s;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-          const uint32_t x = __shfl_up_sync(0xffffffffu, incl, d);
-          if (lane >= d) incl += x;
-        }
-        const uint32_t excl = incl - s;
-        if (excl < kk && kk <= incl) {
-          uint32_t acc = excl;
-          for (int j = 7; j >= 0; --j) {
-            if (acc + c[j] >= kk) {
-              sel_digit = (uint32_t)(base + j);
-              sel_above = acc;
-              break;
-            }
-            acc += c[j];
-          }
-        }
-      }
+      if (warp == 0) find_digit(hist, kk, &sel_digit, &sel_above);
       __syncthreads();
       prefix |= sel_digit << shift;
-      pmask |= 255u << shift;
+      pmask |= dmask << shift;
       kk -= sel_above;
-      __syncthreads();
     }
     // prefix = key of the K_p-th best; take every key above it and the kk
-    // lowest-index keys equal to it.
+    // lowest-index keys equal to it, in index order.  Each warp owns one
+    // contiguous segment: count, one block-wide exclusive scan, write.
     const uint32_t T = prefix;
-    const uint32_t want_gt = (uint32_t)K_p - kk;
-    uint32_t base_gt = 0u, base_tie = 0u;
-    for (int64_t b = 0; b < n; b += kTopkThreads) {
-      if (base_gt == want_gt && base_tie >= kk) break;  // uniform
-      const int64_t i = b + tid;
+    const int64_t seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~int64_t(31);
+    const int64_t b0 = warp * seg;
+    const int64_t b1 = b0 + seg < n ? b0 + seg : n;
+    uint32_t cg = 0u, ct = 0u;
+    for (int64_t i0 = b0; i0 < b1; i0 += 32) {
+      const int64_t i = i0 + lane;
       uint32_t key = 0u;
-      if (i < n) key = cached ? cache[i] : order_key(__ldg(row + i));
-      const bool gt = i < n && key > T;
-      const bool tie = i < n && key == T;
+      if (i < b1) key = cached ? cache[i] : order_key(__ldg(row + i));
+      cg += __popc(__ballot_sync(0xffffffffu, i < b1 && key > T));
+      ct += __popc(__ballot_sync(0xffffffffu, i < b1 && key == T));
+    }
+    if (lane == 0) {
+      wcnt[0][warp] = cg;
+      wcnt[1][warp] = ct;
+    }
+    __syncthreads();
+    uint32_t g_base = 0u, t_base = 0u;
+#pragma unroll
+    for (int w = 0; w < kTopkWarps; ++w) {
+      if (w < warp) {
+        g_base += wcnt[0][w];
+        t_base += wcnt[1][w];
+      }
+    }
+    for (int64_t i0 = b0; i0 < b1; i0 += 32) {
+      if (t_base >= kk && g_base + kk >= (uint32_t)K_p) break;  // warp-uniform
+      const int64_t i = i0 + lane;
+      uint32_t key = 0u;
+      if (i < b1) key = cached ? cache[i] : order_key(__ldg(row + i));
+      const bool gt = i < b1 && key > T;
+      const bool tie = i < b1 && key == T;
       const uint32_t bg = __ballot_sync(0xffffffffu, gt);
       const uint32_t bt = __ballot_sync(0xffffffffu, tie);
-      if (lane == 0) {
-        wcnt[0][warp] = __popc(bg);
-        wcnt[1][warp] = __popc(bt);
-      }
-      __syncthreads();
-      uint32_t wg = 0u, wt = 0u, tg = 0u, tt = 0u;
-#pragma unroll
-      for (int w = 0; w < kTopkWarps; ++w) {
-        const uint32_t a = wcnt[0][w], e = wcnt[1][w];
-        if (w < warp) {
-          wg += a;
-          wt += e;
-        }
-        tg += a;
-        tt += e;
-      }
-      const uint32_t g_before = base_gt + wg + __popc(bg & lane_lt);
-      const uint32_t t_before = base_tie + wt + __popc(bt & lane_lt);
+      const uint32_t g_before = g_base + __popc(bg & lane_lt);
+      const uint32_t t_before = t_base + __popc(bt & lane_lt);
       // (positions are < K_p by construction; the guard keeps a corrupted
       // row from writing into its neighbour)
       const uint32_t pos = gt ? g_before + min(t_before, kk) : g_before + t_before;
       if ((gt || (tie && t_before < kk)) && pos < (uint32_t)K_p) o[pos] = (int32_t)i;
-      base_gt += tg;
-      base_tie += tt;
-      __syncthreads();
+      g_base += __popc(bg);
+      t_base += __popc(bt);
     }
     __syncthreads();
   }
@@ -203,13 +212,15 @@ cudaError_t launch_topk(const LaunchCtx& c, const float* scores, int64_t ld,
   if (nmax > ld) nmax = ld;
   int cache_cap = nmax <= kTopkCacheMax ? (int)nmax : 0;
   const size_t smem = (size_t)cache_cap * sizeof(uint32_t);
-  static bool attr_done = false;
-  if (!attr_done) {
+  static int attr_dev = -1;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (attr_dev != dev) {
     cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)(kTopkCacheMax * sizeof(uint32_t)));
     if (e != cudaSuccess) return e;
-    attr_done = true;
+    attr_dev = dev;
   }
   int64_t grid = rows;
   const int64_t cap = (int64_t)c.num_sms * 8;

@@ -82,7 +82,7 @@ def test_invalid_index_configs_rejected(lib, over, code):
 
 @pytest.mark.parametrize("over,code", [
     (dict(attn_heads=0), 1), (dict(attn_heads=256), 2), (dict(d_qk=576), 2),
-    (dict(d_v=256), 2), (dict(d_qk=32, d_v=32), 2),
+    (dict(d_v=256), 2), (dict(d_qk=64, d_v=64), 2),
 ])
 def test_invalid_attention_configs_rejected(lib, over, code):
     with pytest.raises(dsa.DsaError) as e:
