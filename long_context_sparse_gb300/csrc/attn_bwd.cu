@@ -164,15 +164,6 @@ __global__ void __launch_bounds__(64 * HG, 1)
         issue_kv(j + 1, (j + 1) & 1);
         cp_async_commit();
       }
-      if (j + 2 < ntiles && tid < 2 * kNK) {  // rows of tile j+2 -> L2
-        const int32_t tok = toks[(j + 2) * kNK + (tid % kNK)];
-        if (tok >= 0) {
-          const __nv_bfloat16* row = (tid < kNK ? k : v) + (int64_t)tok * D;
-          asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(row),
-                       "r"((uint32_t)(D * 2))
-                       : "memory");
-        }
-      }
       const uint32_t kb = sK + (j & 1) * C::kKVBytes;
       const uint32_t vb = sV + (j & 1) * C::kKVBytes;
 

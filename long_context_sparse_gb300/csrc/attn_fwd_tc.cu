@@ -56,7 +56,7 @@ struct TcFwdCfg {
   // dynamic shared memory for a key list of `cap` entries
   // dynamic shared memory: the selected pool ids (K_p) + 4 local tokens
   static uint32_t smem(int K_p) {
-    return 1024 + kQBytes + kPBytes + kStages * kStageBytes + (K_p + 4) * 4 +
+    return 1024 + kQBytes + kPBytes + kStages * kStageBytes + (K_p + 4 + 2 * kTileK) * 4 +
            2 * kMaskWords * 4 + (4 * NH + 3 * NH + 8) * 4 + 256;
   }
 };
@@ -65,12 +65,6 @@ __device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
   asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar)
                : "memory");
 }
-// Bring `bytes` (multiple of 16) at a 16-byte aligned address into L2.
-__device__ __forceinline__ void l2_prefetch_row(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes)
-               : "memory");
-}
-
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -143,7 +137,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   int32_t* pools = reinterpret_cast<int32_t*>(gb + C::kQBytes + C::kPBytes +
                                               kStages * kStageBytes);
   int32_t* locs = pools + K_p;
-  uint32_t* vmask = reinterpret_cast<uint32_t*>(locs + 4);  // [2][words]
+  int32_t* tile_tok = locs + 4;                              // [2][128]
+  uint32_t* vmask = reinterpret_cast<uint32_t*>(tile_tok + 2 * kTileK);  // [2][words]
   float* red = reinterpret_cast<float*>(vmask + 2 * kMaskWords);  // [4][NH]
   float* m_s = red + 4 * NH;                                      // [NH]
   float* alpha_s = m_s + NH;                                      // [NH]
@@ -287,47 +282,30 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         }
         return slot < n ? locs[slot - npool] : -1;
       };
-      // rows of tile 0 go to L2 ahead of their gather
-#pragma unroll
-      for (int rr = 0; rr < 2; ++rr) {
-        const int32_t tk0 = tok_of(ptid + 64 * rr);
-        if (tk0 >= 0) {
-          l2_prefetch_row(k + (int64_t)tk0 * D, D * 2);
-          l2_prefetch_row(v + (int64_t)tk0 * D, D * 2);
-        }
-      }
+      // Coalesced gather: one warp instruction copies 2 key rows x 256
+      // contiguous bytes (lanes 0-15 row r, lanes 16-31 row r+1; lane&15 =
+      // the 16-byte chunk).  Producer warp pw owns rows pw*64 .. pw*64+63.
+      const int pw = ptid >> 5, pl = ptid & 31;
+      const int sub = pl >> 4, c16 = pl & 15;     // row of the pair, chunk
+      const int a16 = c16 >> 3, ch8 = c16 & 7;    // 64-dim atom, 16B chunk
       bool ok = true;
       for (int j = 0; j < ntiles && ok; ++j) {
-        int64_t src_row[2];
-        uint32_t nbytes[2];
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-          const int32_t tok = tok_of(j * kTileK + ptid + 64 * rr);
-          src_row[rr] = tok >= 0 ? tok : 0;
-          nbytes[rr] = tok >= 0 ? 16u : 0u;
-          // the next tile's rows: HBM -> L2 while this tile is gathered
-          const int32_t nxt = j + 1 < ntiles ? tok_of((j + 1) * kTileK + ptid + 64 * rr) : -1;
-          if (nxt >= 0) {
-            l2_prefetch_row(k + (int64_t)nxt * D, D * 2);
-            l2_prefetch_row(v + (int64_t)nxt * D, D * 2);
-          }
-        }
+        int32_t* tt = tile_tok + (j & 1) * kTileK;
+        for (int r = ptid; r < kTileK; r += kProdThreads) tt[r] = tok_of(j * kTileK + r);
+        if (!(ok = G.sync(W))) break;
         for (int kv = 0; kv < 2 && ok; ++kv) {
           const __nv_bfloat16* src = kv == 0 ? k : v;
           for (int c = 0; c < C::kChunks; ++c, ++u) {
             const int s = (int)(u % kStages);
             if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
-            const uint32_t st = sStage + s * kStageBytes;
-#pragma unroll
-            for (int rr = 0; rr < 2; ++rr) {
-              const int r = ptid + 64 * rr;
-              const __nv_bfloat16* srcb = src + src_row[rr] * D + c * 128;
-#pragma unroll
-              for (int a = 0; a < 2; ++a)
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch)
-                  cp_async16(st + a * 16384 + r * 128 + ((ch ^ (r & 7)) << 4),
-                             srcb + a * 64 + ch * 8, nbytes[rr]);
+            const uint32_t st = sStage + s * kStageBytes + a16 * 16384;
+#pragma unroll 4
+            for (int i = 0; i < 32; ++i) {
+              const int r = pw * 64 + 2 * i + sub;
+              const int32_t tok = tt[r];
+              const __nv_bfloat16* sp =
+                  src + (int64_t)(tok >= 0 ? tok : 0) * D + c * 128 + c16 * 8;
+              cp_async16(st + r * 128 + ((ch8 ^ (r & 7)) << 4), sp, tok >= 0 ? 16u : 0u);
             }
             cp_async_mbar_arrive(full(s));
           }
