@@ -48,7 +48,8 @@ struct TcFwdCfg {
   static constexpr int kThreads = kSoftmaxThreads + kProdThreads + 32;
   // registers per thread: warps are spread over the SM's 4 sub-partitions
   // of 16K registers each, so the fullest one holds ceil(warps/4) warps
-  static constexpr int kMaxReg = (16384 / (((kThreads / 32) + 3) / 4 * 32)) & ~7;
+  static constexpr int kRegFit = (16384 / (((kThreads / 32) + 3) / 4 * 32)) & ~7;
+  static constexpr int kMaxReg = kRegFit > 255 ? 255 : kRegFit;
   static constexpr int kChunks = D / 128;  // 128-wide d slices
   static constexpr uint32_t kQBytes = NH * D * 2;
   static constexpr uint32_t kPBytes = NH * kTileK * 2;
@@ -412,73 +413,109 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         continue;
       }
       if (tid < NH) m_s[tid] = -INFINITY;
-      float l[HPG];
+      float l[HPG], mr[HPG];  // row-sum partials and the running maxima
 #pragma unroll
-      for (int h = 0; h < HPG; ++h) l[h] = 0.f;
+      for (int h = 0; h < HPG; ++h) {
+        l[h] = 0.f;
+        mr[h] = -INFINITY;
+      }
       bool ok = true;
       for (int j = 0; j < ntiles; ++j, ++ntile_all) {
         if (!(ok = W.wait(s_full, ntile_all & 1u))) break;
         tc_fence_after();
-        float s[HPG];
-        tmem_ld_row<HPG>(tS + lane_base + h0g, s);
         const int slot = j * kTileK + i;
         const bool valid = (vm[slot >> 5] >> (slot & 31)) & 1u;
+        // does any score beat its running max by more than 2^8?  (always
+        // true on the first tile; rare afterwards).  S^T is read from TMEM
+        // in groups of 16 columns to keep few scores live.
+        bool need = false;
 #pragma unroll
-        for (int h = 0; h < HPG; ++h) {
-          s[h] = valid ? s[h] * scale_log2 : -INFINITY;
-          float x = s[h];
+        for (int h0 = 0; h0 < HPG; h0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tS + lane_base + h0g + h0, r);
+          tmem_wait_ld();
 #pragma unroll
-          for (int sh = 16; sh > 0; sh >>= 1)
-            x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
-          if (lane == 0) red[wq * NH + h0g + h] = x;
-        }
-        if (!(ok = G.sync(W))) break;
-        if (tid == 0) flags[(j + 1) & 1] = 0;
-        if (tid < NH) {
-          const float tm = fmaxf(fmaxf(red[tid], red[NH + tid]),
-                                 fmaxf(red[2 * NH + tid], red[3 * NH + tid]));
-          const float mo = m_s[tid];
-          // raise the running max only when this tile beats it by > 2^8
-          const bool raise = tm > mo + kMaxSlack || (mo == -INFINITY && tm > mo);
-          alpha_s[tid] = raise && mo != -INFINITY ? exp2f(mo - tm) : 1.f;
-          if (raise) {
-            m_s[tid] = tm;
-            if (j > 0) flags[j & 1] = 1;
+          for (int e = 0; e < 16; ++e) {
+            const float x = valid ? __uint_as_float(r[e]) * scale_log2 : -INFINITY;
+            need |= x > mr[h0 + e] + kMaxSlack || (mr[h0 + e] == -INFINITY && x > mr[h0 + e]);
           }
         }
+        if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr((int*)&flags[j & 1], 1);
         if (!(ok = G.sync(W))) break;
-        const bool rescale = flags[j & 1] != 0;
-        if (rescale) {
-          // PV of the previous tile has completed (it precedes this S^T)
-#pragma unroll 1
-          for (int c = 0; c < C::kChunks; ++c) {
+        if (tid == 0) flags[(j + 1) & 1] = 0;  // next tile's flag (read two syncs ago)
+        if (flags[j & 1] != 0) {
+          // ---- slow path: exact column maxima, raise the beaten maxima
 #pragma unroll
-            for (int hh = 0; hh < HPG; hh += 16) {
-              uint32_t r[16];
-              const uint32_t ta = tO + lane_base + c * NH + h0g + hh;
-              tmem_ld16(ta, r);
-              tmem_wait_ld();
+          for (int h0 = 0; h0 < HPG; h0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(tS + lane_base + h0g + h0, r);
+            tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 16; ++e)
-                r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha_s[h0g + hh + e]);
-              tmem_st16(ta, r);
+            for (int e = 0; e < 16; ++e) {
+              float x = valid ? __uint_as_float(r[e]) * scale_log2 : -INFINITY;
+#pragma unroll
+              for (int sh = 16; sh > 0; sh >>= 1)
+                x = fmaxf(x, __shfl_xor_sync(0xffffffffu, x, sh));
+              if (lane == 0) red[wq * NH + h0g + h0 + e] = x;
             }
           }
-          tmem_wait_st();
+          if (!(ok = G.sync(W))) break;
+          if (tid < NH) {
+            const float tm = fmaxf(fmaxf(red[tid], red[NH + tid]),
+                                   fmaxf(red[2 * NH + tid], red[3 * NH + tid]));
+            const float mo = m_s[tid];
+            const bool raise = tm > mo + kMaxSlack || (mo == -INFINITY && tm > mo);
+            alpha_s[tid] = raise && mo != -INFINITY ? exp2f(mo - tm) : 1.f;
+            if (raise) m_s[tid] = tm;
+          }
+          if (!(ok = G.sync(W))) break;
+          bool rescale = false;
+#pragma unroll
+          for (int h = 0; h < HPG; ++h) {
+            const float a = alpha_s[h0g + h];
+            mr[h] = m_s[h0g + h];
+            l[h] *= a;
+            rescale |= a != 1.f;
+          }
+          if (j > 0 && __any_sync(0xffffffffu, rescale)) {
+            // O^T columns of raised maxima (the previous PV has completed:
+            // it precedes this S^T)
+#pragma unroll 1
+            for (int c = 0; c < C::kChunks; ++c) {
+#pragma unroll
+              for (int hh = 0; hh < HPG; hh += 16) {
+                uint32_t r[16];
+                const uint32_t ta = tO + lane_base + c * NH + h0g + hh;
+                tmem_ld16(ta, r);
+                tmem_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 16; ++e)
+                  r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha_s[h0g + hh + e]);
+                tmem_st16(ta, r);
+              }
+            }
+            tmem_wait_st();
+          }
         }
         // P = exp2(s - m) -> row sums and P^T (bf16) in shared memory
 #pragma unroll
-        for (int h = 0; h < HPG; ++h) {
-          const int hh = h0g + h;
-          const float mh = m_s[hh];
-          const float p = exp2f(s[h] - (mh == -INFINITY ? 0.f : mh));
-          l[h] = l[h] * alpha_s[hh] + p;
-          const uint32_t addr = sP + p_off + (uint32_t)hh * 128u +
-                                ((p_chunk ^ (uint32_t)(hh & 7)) << 4);
-          const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-          asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
-                       "h"(*reinterpret_cast<const uint16_t*>(&pb))
-                       : "memory");
+        for (int h0 = 0; h0 < HPG; h0 += 16) {
+          uint32_t r[16];
+          tmem_ld16(tS + lane_base + h0g + h0, r);
+          tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int h = h0 + e, hh = h0g + h;
+            const float x = valid ? __uint_as_float(r[e]) * scale_log2 : -INFINITY;
+            const float p = exp2f(x - (mr[h] == -INFINITY ? 0.f : mr[h]));
+            l[h] += p;
+            const uint32_t addr = sP + p_off + (uint32_t)hh * 128u +
+                                  ((p_chunk ^ (uint32_t)(hh & 7)) << 4);
+            const __nv_bfloat16 pb = __float2bfloat16_rn(p);
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
+                         "h"(*reinterpret_cast<const uint16_t*>(&pb))
+                         : "memory");
+          }
         }
         fence_proxy_async();  // P^T writes -> tensor core reads
         tc_fence_before();

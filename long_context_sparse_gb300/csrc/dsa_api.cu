@@ -417,11 +417,14 @@ dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q, const v
                                       static_cast<const __nv_bfloat16*>(dO), delta,
                                       dk_acc, dv_acc);
   if (e != cudaSuccess) return cuda_status(e);
-  e = launch_attn_bwd(ctx, s, static_cast<const __nv_bfloat16*>(q),
-                      static_cast<const __nv_bfloat16*>(k),
-                      static_cast<const __nv_bfloat16*>(v),
-                      static_cast<const __nv_bfloat16*>(dO), lse, delta, topk_idx,
-                      static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc);
+  CUtensorMap qm, gm;
+  if ((st = encode_2d(&qm, q, (uint64_t)(s.S * s.H), (uint64_t)s.D, 64)) != DSA_OK)
+    return st;
+  if ((st = encode_2d(&gm, dO, (uint64_t)(s.S * s.H), (uint64_t)s.D, 64)) != DSA_OK)
+    return st;
+  e = launch_attn_bwd_tc(ctx, s, qm, gm, static_cast<const __nv_bfloat16*>(k),
+                         static_cast<const __nv_bfloat16*>(v), lse, delta, topk_idx,
+                         static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc);
   if (e == cudaErrorInvalidValue) return DSA_ERR_UNSUPPORTED_SHAPE;
   if (e != cudaSuccess) return cuda_status(e);
   e = launch_attn_bwd_finalize(ctx, s, dk_acc, dv_acc, static_cast<__nv_bfloat16*>(dk),

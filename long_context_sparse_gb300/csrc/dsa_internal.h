@@ -62,13 +62,14 @@ cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
                                 const __nv_bfloat16* dO, float* delta,
                                 float* dk_acc, float* dv_acc);
 
-// a8: sparse attention backward (dQ direct, dK/dV fp32 scatter).
-cudaError_t launch_attn_bwd(const LaunchCtx& c, const AttnShape& s,
-                            const __nv_bfloat16* q, const __nv_bfloat16* k,
-                            const __nv_bfloat16* v, const __nv_bfloat16* dO,
-                            const float* lse, const float* delta,
-                            const int32_t* idx, __nv_bfloat16* dq,
-                            float* dk_acc, float* dv_acc);
+// a8: sparse attention backward on tcgen05 (dQ direct, dK/dV fp32 scatter).
+// q_map / g_map: q and dO viewed as [S*H, D] bf16, box {64, 64}.
+cudaError_t launch_attn_bwd_tc(const LaunchCtx& c, const AttnShape& s,
+                               const CUtensorMap& q_map, const CUtensorMap& g_map,
+                               const __nv_bfloat16* k, const __nv_bfloat16* v,
+                               const float* lse, const float* delta,
+                               const int32_t* idx, __nv_bfloat16* dq, float* dk_acc,
+                               float* dv_acc);
 
 // a9: fp32 accumulators -> bf16 dK, dV.
 cudaError_t launch_attn_bwd_finalize(const LaunchCtx& c, const AttnShape& s,
