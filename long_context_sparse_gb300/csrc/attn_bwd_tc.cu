@@ -49,26 +49,14 @@ struct BwdTcCfg {
   static constexpr uint32_t kBufBytes = kTileK * NH * 2;  // P / dS [key x 64 h]
   static uint32_t smem(int K_p) {
     return 1024 + 2 * kQBytes + kBufBytes + kStages * kStageBytes +
-           2 * (K_p + 8) * 4 + 2 * kTileK * 4 + 2 * kMaskWords * 4 +
-           4 * NH * 4 + 64 + 256;
+           carved(2 * (K_p + 8) * 4) + 2 * carved(2 * kTileK * 4) +
+           carved(2 * kMaskWords * 4) + 2 * carved(2 * NH * 4) + carved(32) +
+           carved(32 * 8);
   }
 };
 
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
-}
-__device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, uint64_t ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > ns) return false;
-  return true;
 }
 // 32 consecutive fp32 TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -82,17 +70,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     v[16 + e] = __uint_as_float(b[e]);
   }
 }
-
-struct GroupBar {
-  uint32_t bar;
-  uint32_t phase;
-  __device__ __forceinline__ bool sync(const Waiter& W) {
-    mbar_arrive(bar);
-    const bool ok = W.wait(bar, phase & 1u);
-    ++phase;
-    return ok;
-  }
-};
 
 template <int D>
 __global__ void __maxnreg__(kMaxReg)
@@ -120,15 +97,16 @@ __global__ void __maxnreg__(kMaxReg)
   const uint32_t sG = sQ + C::kQBytes;           // dO  [64 h x D]
   const uint32_t sB = sG + C::kQBytes;           // P / dS [128 key x 64 h]
   const uint32_t sStage = sB + C::kBufBytes;     // ring, 1024-aligned
-  int32_t* pools = reinterpret_cast<int32_t*>(gb + 2 * C::kQBytes + C::kBufBytes +
-                                              kStages * kStageBytes);  // [2][K_p+8]
-  int32_t* tile_tok = pools + 2 * (K_p + 8);                           // [2][128]
-  uint32_t* vmask = reinterpret_cast<uint32_t*>(tile_tok + 2 * kTileK);  // [2][words]
-  float* lse2_s = reinterpret_cast<float*>(vmask + 2 * kMaskWords);   // [2][NH]
-  float* delta_s = lse2_s + 2 * NH;                                   // [2][NH]
-  int* misc = reinterpret_cast<int*>(delta_s + 2 * NH);  // ntok[2], npool[2], last, nadd
-  uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(misc + 8) + 7) & ~uintptr_t(7));
+  // tail regions, each starting on a 128-byte boundary (vector accesses)
+  uint8_t* tail = gb + 2 * C::kQBytes + C::kBufBytes + kStages * kStageBytes;
+  int32_t* pools = carve<int32_t>(tail, 2 * (K_p + 8));      // [2][K_p+8]
+  int32_t* tile_tok = carve<int32_t>(tail, 2 * kTileK);      // [2][128]
+  uint32_t* vmask = carve<uint32_t>(tail, 2 * kMaskWords);   // [2][words]
+  int32_t* sm_tok = carve<int32_t>(tail, 2 * kTileK);        // [2][128]
+  float* lse2_s = carve<float>(tail, 2 * NH);                // [2][NH]
+  float* delta_s = carve<float>(tail, 2 * NH);               // [2][NH]
+  int* misc = carve<int>(tail, 8);                 // ntok[2], npool[2], last, nadd
+  uint64_t* bars = carve<uint64_t>(tail, 32);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
@@ -407,6 +385,7 @@ __global__ void __maxnreg__(kMaxReg)
     const int grp = tid >> 7;             // heads grp*32 .. +31, keys grp*32 ..
     const int wq = warp & 3;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
+    GroupBar G{sm_grp, 0u};
     uint32_t T = 0, nq = 0, chunk = 0;
     int qi = 0;
     bool ok = true;
@@ -446,6 +425,8 @@ __global__ void __maxnreg__(kMaxReg)
         tmem_ld32(tP + lane_base + grp * 32, pv);
         const int slot = j * kTileK + i;
         const bool valid = (vm[slot >> 5] >> (slot & 31)) & 1u;
+        int32_t* stt = sm_tok + (T & 1u) * kTileK;  // scatter targets of this tile
+        if (grp == 0) stt[i] = tok_of(slot);
         uint32_t pb[16], db[16];
 #pragma unroll
         for (int e = 0; e < 32; e += 2) {
@@ -467,19 +448,23 @@ __global__ void __maxnreg__(kMaxReg)
         fence_proxy_async();
         tc_fence_before();
         mbar_arrive(pbuf_full);
-        if (!(ok = W.wait(pbuf_free, T & 1u))) break;           // dV^T read P
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                           rowa + (((uint32_t)(grp * 4 + c) ^ (uint32_t)(i & 7)) << 4)),
-                       "r"(db[4 * c]), "r"(db[4 * c + 1]), "r"(db[4 * c + 2]),
-                       "r"(db[4 * c + 3])
-                       : "memory");
-        fence_proxy_async();
-        tc_fence_before();
-        mbar_arrive(dsbuf_full);
-        // ---- scatter the dV^T chunks, then the dK^T chunks
+        if (!(ok = G.sync(W))) break;  // stt[] complete
+        // ---- scatter the dV^T chunks, then (after dS is in place) dK^T
         for (int which = 0; which < 2 && ok; ++which) {
+          if (which == 1) {
+            // dV^T has read every P: put dS in the buffer for dK^T and dQ^T
+            if (!(ok = W.wait(pbuf_free, T & 1u))) break;
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
+                               rowa + (((uint32_t)(grp * 4 + c) ^ (uint32_t)(i & 7)) << 4)),
+                           "r"(db[4 * c]), "r"(db[4 * c + 1]), "r"(db[4 * c + 2]),
+                           "r"(db[4 * c + 3])
+                           : "memory");
+            fence_proxy_async();
+            tc_fence_before();
+            mbar_arrive(dsbuf_full);
+          }
           float* acc = which == 0 ? dv_acc : dk_acc;
           const float f = which == 0 ? 1.f : scale;
           for (int q = 0; q < 2 * C::kDChunks; ++q, ++chunk) {
@@ -492,11 +477,14 @@ __global__ void __maxnreg__(kMaxReg)
             tc_fence_before();
             mbar_arrive(chunk_empty(b));
             float* dst = acc + dc * 128 + i;
-            const int key0 = j * kTileK + kh * 64 + grp * 32;
+            const int4* tk4 = reinterpret_cast<const int4*>(stt + kh * 64 + grp * 32);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int32_t tok = tok_of(key0 + e);  // warp-uniform
-              if (tok >= 0) red_add_f32(dst + (int64_t)tok * D, f * cv[e]);
+            for (int e4 = 0; e4 < 8; ++e4) {
+              const int4 tk = tk4[e4];  // warp-uniform tokens of 4 keys
+              const int32_t tks[4] = {tk.x, tk.y, tk.z, tk.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                if (tks[e] >= 0) red_add_f32(dst + (int64_t)tks[e] * D, f * cv[4 * e4 + e]);
             }
           }
         }

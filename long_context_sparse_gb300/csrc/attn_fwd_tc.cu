@@ -57,18 +57,12 @@ struct TcFwdCfg {
   // dynamic shared memory for a key list of `cap` entries
   // dynamic shared memory: the selected pool ids (K_p) + 4 local tokens
   static uint32_t smem(int K_p) {
-    return 1024 + kQBytes + kPBytes + kStages * kStageBytes + (K_p + 4 + 2 * kTileK) * 4 +
-           2 * kMaskWords * 4 + (4 * NH + 3 * NH + 8) * 4 + 256;
+    return 1024 + kQBytes + kPBytes + kStages * kStageBytes + carved((K_p + 4) * 4) +
+           carved(2 * kTileK * 4) + carved(2 * kMaskWords * 4) + carved(4 * NH * 4) +
+           3 * carved(NH * 4) + carved(32) + carved(32 * 8);
   }
 };
 
-__device__ __forceinline__ void cp_async_mbar_arrive(uint32_t bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar)
-               : "memory");
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 
 // NH consecutive fp32 columns of this thread's TMEM lane.
 template <int NH>
@@ -89,26 +83,6 @@ __device__ __forceinline__ void tmem_ld_row(uint32_t taddr, float (&v)[NH]) {
   for (int c = 0; c < NH; ++c) v[c] = __uint_as_float(r[c]);
 }
 
-// A barrier among the threads of one role built on an mbarrier, so that a
-// thread whose wait gave up cannot leave its peers blocked: every wait here
-// is bounded like the others.
-struct GroupBar {
-  uint32_t bar;
-  uint32_t phase;
-  __device__ __forceinline__ bool sync(const Waiter& W) {
-    mbar_arrive(bar);
-    const bool ok = W.wait(bar, phase & 1u);
-    ++phase;
-    return ok;
-  }
-};
-
-__device__ __forceinline__ bool drain(uint32_t bar, uint32_t parity, uint64_t ns) {
-  const uint64_t t0 = globaltimer_ns();
-  while (!mbar_try_wait(bar, parity))
-    if (globaltimer_ns() - t0 > ns) return false;
-  return true;
-}
 
 template <int D, int NH>
 __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
@@ -134,19 +108,19 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   const uint32_t sP = sQ + C::kQBytes;
   const uint32_t sStage = sP + C::kPBytes;  // 1024-aligned (sizes are)
   // key list of the current query as pool ids (slot 4i+j <-> token
-  // 4*pools[i]+j, -1 = empty) followed by up to 3 local tokens
-  int32_t* pools = reinterpret_cast<int32_t*>(gb + C::kQBytes + C::kPBytes +
-                                              kStages * kStageBytes);
+  // 4*pools[i]+j, -1 = empty) followed by up to 3 local tokens; each tail
+  // region starts on a 128-byte boundary
+  uint8_t* tail = gb + C::kQBytes + C::kPBytes + kStages * kStageBytes;
+  int32_t* pools = carve<int32_t>(tail, K_p + 4);
   int32_t* locs = pools + K_p;
-  int32_t* tile_tok = locs + 4;                              // [2][128]
-  uint32_t* vmask = reinterpret_cast<uint32_t*>(tile_tok + 2 * kTileK);  // [2][words]
-  float* red = reinterpret_cast<float*>(vmask + 2 * kMaskWords);  // [4][NH]
-  float* m_s = red + 4 * NH;                                      // [NH]
-  float* alpha_s = m_s + NH;                                      // [NH]
-  float* inv_s = alpha_s + NH;                                    // [NH]
-  int* misc = reinterpret_cast<int*>(inv_s + NH);  // ntok[2], last, nadd, flag[2]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(
-      (reinterpret_cast<uintptr_t>(misc + 8) + 7) & ~uintptr_t(7));
+  int32_t* tile_tok = carve<int32_t>(tail, 2 * kTileK);       // [2][128]
+  uint32_t* vmask = carve<uint32_t>(tail, 2 * kMaskWords);    // [2][words]
+  float* red = carve<float>(tail, 4 * NH);                    // [4][NH]
+  float* m_s = carve<float>(tail, NH);                        // [NH]
+  float* alpha_s = carve<float>(tail, NH);                    // [NH]
+  float* inv_s = carve<float>(tail, NH);                      // [NH]
+  int* misc = carve<int>(tail, 8);  // ntok[2], last, nadd, flag[2]
+  uint64_t* bars = carve<uint64_t>(tail, 32);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };

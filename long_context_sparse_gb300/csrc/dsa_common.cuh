@@ -54,6 +54,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As above, but the thread may sleep in the instruction for up to
+// `hint_ns` waiting for the phase (instead of spinning on the issue slots).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 
 // A CTA-wide abort flag in shared memory plus the status word and a time
 // limit.  Every wait gives up when the limit passes or another thread of the
@@ -71,17 +85,17 @@ struct Waiter {
     *abort_flag = 1u;
   }
 
+  // Sleeps inside try_wait (up to 20 us per attempt) rather than spinning;
+  // checks the abort flag and the time limit between attempts.
   __device__ __forceinline__ bool wait(uint32_t bar, uint32_t parity) const {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
-    for (uint32_t it = 1;; ++it) {
-      if (mbar_try_wait(bar, parity)) return true;
-      if ((it & 63u) == 0u) {
-        if (*abort_flag) return false;
-        if (globaltimer_ns() - t0 > timeout_ns) {
-          fail(DSA_ERR_DEVICE_TIMEOUT);
-          return false;
-        }
+    for (;;) {
+      if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > timeout_ns) {
+        fail(DSA_ERR_DEVICE_TIMEOUT);
+        return false;
       }
     }
   }
