@@ -168,6 +168,29 @@ DSA_API dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q,
                                  void* dv, void* ws, size_t ws_bytes,
                                  void* stream);
 
+/* Allocation-free variant of dsa_index_scores_topk (the pages have no
+ * counterpart: it exists for callers that cannot allocate device memory,
+ * such as a plugin whose host application has reserved all device memory
+ * for its own pool, or a service that forbids allocation after start-up).
+ * The workspace is a fixed DSA_STATIC_SCRATCH_BYTES array inside the
+ * library, held by every GPU that loads the library until the process
+ * exits; problems whose DSA_WS_INDEX workspace exceeds it return
+ * DSA_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The first call
+ * on a device looks up the array's device address (cudaGetSymbolAddress)
+ * and caches it; make that first call before any stream capture.  Every
+ * call shares the array: calls whose work overlaps on the GPU race, so
+ * serialise them (one stream, or events).  The status-word header is
+ * cleared at the start of each call; device-side errors latched there are
+ * not reported by this entry point.  Results equal dsa_index_scores_topk's.
+ * No device memory is allocated by the call. */
+#define DSA_STATIC_SCRATCH_BYTES (32u << 20)
+DSA_API dsa_status_t dsa_index_scores_topk_static(const dsa_config_t* cfg,
+                                                  const void* q_idx,
+                                                  const void* k_idx,
+                                                  const float* w,
+                                                  int32_t* topk_idx,
+                                                  void* stream);
+
 /* Synchronise `stream`, read the workspace status word into *device_status
  * (a dsa_status_t value, DSA_OK if nothing was latched) and clear it. */
 DSA_API dsa_status_t dsa_get_device_status(void* ws, void* stream,

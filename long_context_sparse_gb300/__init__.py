@@ -24,6 +24,7 @@ from .synth import Workload
 __all__ = [
     "Config", "DsaError", "config_for", "workspace_size", "workspace",
     "pool_keys", "index_scores", "topk_from_scores", "index_scores_topk",
+    "index_scores_topk_static",
     "sparse_attn_fwd", "sparse_attn_bwd", "get_device_status",
     "status_string", "library_path", "WS_INDEX", "WS_FWD", "WS_BWD",
     "WS_STATUS",
@@ -49,6 +50,7 @@ EXPORTS = [
     "dsa_index_scores", "dsa_topk_from_scores", "dsa_index_scores_topk",
     "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_get_device_status",
     "dsa_status_string", "dsa_abi_version", "dsa_last_cuda_error",
+    "dsa_index_scores_topk_static",
 ]
 
 
@@ -137,6 +139,7 @@ def _load():
             "dsa_sparse_attn_bwd": [CP, P, P, P, P, P, P, P, P, P, P, P, SZ,
                                     P],
             "dsa_get_device_status": [P, P, ctypes.POINTER(ctypes.c_uint32)],
+            "dsa_index_scores_topk_static": [CP, P, P, P, P, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -284,6 +287,27 @@ def index_scores_topk(cfg: Config, q_idx, k_idx, w, out=None,
                                          _ptr(k_idx), _ptr(w), _ptr(out),
                                          _ptr(ws), ws.numel(), _stream(dev)),
            "dsa_index_scores_topk")
+    return out
+
+
+def index_scores_topk_static(cfg: Config, q_idx, k_idx, w,
+                             out=None) -> torch.Tensor:
+    """As index_scores_topk, with the library's own fixed scratch instead of
+    a workspace (for callers that cannot allocate device memory; calls must
+    not overlap on the GPU)."""
+    S = cfg.seq_len
+    _need(q_idx, "q_idx", torch.bfloat16, (S, cfg.idx_heads, cfg.idx_dim))
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, (S, cfg.idx_dim), dev)
+    _need(w, "w", torch.float32, (S, cfg.idx_heads), dev)
+    if out is None:
+        out = torch.empty((S, cfg.topk_pools), dtype=torch.int32, device=dev)
+    _need(out, "topk_idx", torch.int32, (S, cfg.topk_pools), dev)
+    cc = cfg.c()
+    _check(_load().dsa_index_scores_topk_static(ctypes.byref(cc), _ptr(q_idx),
+                                                _ptr(k_idx), _ptr(w),
+                                                _ptr(out), _stream(dev)),
+           "dsa_index_scores_topk_static")
     return out
 
 

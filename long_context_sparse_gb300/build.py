@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa_gb300.so")
 SOURCES = ["select.cu", "indexer.cu", "attn_fwd_tc.cu", "attn_bwd.cu",
-           "attn_bwd_tc.cu", "dsa_api.cu"]
+           "attn_bwd_tc.cu", "dsa_api.cu",
+           "dsa_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
                 "-Xcompiler", "-fvisibility=hidden", "-I",
