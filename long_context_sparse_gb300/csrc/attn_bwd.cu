@@ -14,7 +14,9 @@ namespace {
 // delta[t,h] = sum_d dO[t,h,d] O[t,h,d] (fp32), one warp per (t,h) row.
 __global__ void __launch_bounds__(256) bwd_delta_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-    float* __restrict__ delta, int64_t n_rows, int D) {
+    float* __restrict__ delta, int64_t n_rows, int D, uint32_t* grid_ctr) {
+  // the backward's grid-barrier counter restarts at zero for every call
+  if (blockIdx.x == 0 && threadIdx.x == 0 && grid_ctr) *grid_ctr = 0u;
   const int lane = threadIdx.x & 31;
   const int64_t w0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
@@ -66,7 +68,7 @@ cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
                                 float* delta, float* dk_acc, float* dv_acc) {
   const int64_t rows = s.S * s.H;
   bwd_delta_kernel<<<(unsigned)grid_for(c, rows * 32), 256, 0, c.stream>>>(
-      o, dO, delta, rows, s.D);
+      o, dO, delta, rows, s.D, c.status ? c.status + 32 : nullptr);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   const int64_t n4 = s.S * s.D / 4;

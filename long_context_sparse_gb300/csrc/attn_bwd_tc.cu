@@ -13,6 +13,8 @@
 //   dQ^T [d, h]  += K_tile^T dS          (TMEM-resident over the tiles)
 //
 // with K/V rows gathered once per tile (K a second time for dQ, from L2).
+// Order per tile: S^T, dP^T; dS -> dQ^T, dK^T; P -> dV^T, so the gather
+// ring is free for the next tile while the dK/dV chunks are scattered.
 // dV^T / dK^T are produced in [128 d x 64 key] chunks with d on the TMEM
 // lanes, so each thread holds one d of a key row and a warp's fp32
 // reduction covers one contiguous 128-byte segment of that row: the scatter
@@ -37,6 +39,7 @@ constexpr int kSmThreads = 256;
 constexpr int kProdThreads = 64;
 constexpr int kThreads = kSmThreads + kProdThreads + 32;  // 11 warps
 constexpr int kMmaWarp = 10;
+constexpr int kBarEvery = 2;           // key tiles between grid-wide meetings
 constexpr int kMaskWords = (2048 * 4 + 3 + kTileK + 31) / 32;
 // the fullest SM sub-partition holds 3 of the 11 warps
 constexpr int kMaxReg = (16384 / (((kThreads / 32) + 3) / 4 * 32)) & ~7;
@@ -83,7 +86,8 @@ __global__ void __maxnreg__(kMaxReg)
                        __nv_bfloat16* __restrict__ dq, float* __restrict__ dk_acc,
                        float* __restrict__ dv_acc, int64_t S, int H, int K_p,
                        int n_loc, float scale, int n_hblk, uint32_t* status,
-                       uint64_t timeout_ns) {
+                       uint64_t timeout_ns, uint32_t* grid_ctr, int bar_every,
+                       int bar_points) {
   using C = BwdTcCfg<D>;
   constexpr uint32_t ID_KK = idesc_bf16(128, NH, 0, 0);  // S^T, dP^T
   constexpr uint32_t ID_MK = idesc_bf16(128, 64, 1, 0);  // dV^T, dK^T
@@ -322,30 +326,11 @@ __global__ void __maxnreg__(kMaxReg)
           }
           if (!ok) break;
           tc_commit(sdp_full);
-          // ---- dV^T (P in sB), then dK^T (dS in sB): [128 d x 64 key] chunks
-          for (int which = 0; which < 2 && ok; ++which) {
-            if (!(ok = W.wait(which == 0 ? pbuf_full : dsbuf_full, T & 1u))) break;
-            tc_fence_after();
-            const uint32_t asrc = which == 0 ? sG : sQ;
-            for (int q = 0; q < 2 * C::kDChunks; ++q, ++chunk) {
-              const int dc = q >> 1, kh = q & 1;
-              const int b = (int)(chunk & 1u);
-              if (!(ok = W.wait(chunk_empty(b), ((chunk >> 1) & 1u) ^ 1u))) break;
-              tc_fence_after();
-#pragma unroll
-              for (int ks = 0; ks < NH / 16; ++ks)
-                tc_mma(tC + b * 64,
-                       // A = X^T [128 d x 16 h]: MN-major, 64-dim atoms 8 KB apart
-                       sdesc_sw128(asrc + (2 * dc) * (NH * 128) + ks * 2048, NH * 128, 1024),
-                       // B = P or dS [64 key x 16 h]: K-major rows of 64 heads
-                       sdesc_sw128(sB + kh * 64 * 128 + ks * 32, 16, 1024), ID_MK,
-                       ks > 0 ? 1u : 0u);
-              tc_commit(chunk_full(b));
-            }
-            if (which == 0) tc_commit(pbuf_free);
-          }
-          if (!ok) break;
-          // ---- dQ^T += K^T dS^T (K re-gathered: two atoms per 128-dim chunk)
+          // ---- dS in sB: dQ^T += K^T dS^T first (K re-gathered, two atoms
+          // per 128-dim chunk), so the stage ring is free for the next tile's
+          // gather while the chunks below are scattered
+          if (!(ok = W.wait(dsbuf_full, T & 1u))) break;
+          tc_fence_after();
           if (j == 0 && !(ok = W.wait(tq_empty, (nq & 1u) ^ 1u))) break;
           for (int dc = 0; dc < C::kDChunks && ok; ++dc, u += 2) {
             const int s0 = (int)(u % kStages);  // u is even: s0, s0+1 adjacent
@@ -366,7 +351,32 @@ __global__ void __maxnreg__(kMaxReg)
             tc_commit(empty(s0 + 1));
           }
           if (!ok) break;
-          tc_commit(dsbuf_free);
+          // ---- dK^T (dS in sB), then dV^T (P in sB): [128 d x 64 key] chunks
+          for (int which = 0; which < 2 && ok; ++which) {
+            if (which == 1) {
+              tc_commit(dsbuf_free);  // dQ^T and dK^T have read dS
+              if (!(ok = W.wait(pbuf_full, T & 1u))) break;
+              tc_fence_after();
+            }
+            const uint32_t asrc = which == 0 ? sQ : sG;
+            for (int q = 0; q < 2 * C::kDChunks; ++q, ++chunk) {
+              const int dc = q >> 1, kh = q & 1;
+              const int b = (int)(chunk & 1u);
+              if (!(ok = W.wait(chunk_empty(b), ((chunk >> 1) & 1u) ^ 1u))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int ks = 0; ks < NH / 16; ++ks)
+                tc_mma(tC + b * 64,
+                       // A = X^T [128 d x 16 h]: MN-major, 64-dim atoms 8 KB apart
+                       sdesc_sw128(asrc + (2 * dc) * (NH * 128) + ks * 2048, NH * 128, 1024),
+                       // B = dS or P [64 key x 16 h]: K-major rows of 64 heads
+                       sdesc_sw128(sB + kh * 64 * 128 + ks * 32, 16, 1024), ID_MK,
+                       ks > 0 ? 1u : 0u);
+              tc_commit(chunk_full(b));
+            }
+          }
+          if (!ok) break;
+          tc_commit(pbuf_free);  // dV^T has read P: the next tile's dS may go in
           if (j == ntiles - 1) {
             tc_commit(dq_done);
             tc_commit(qd_empty);
@@ -386,10 +396,45 @@ __global__ void __maxnreg__(kMaxReg)
     const int wq = warp & 3;
     const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
     GroupBar G{sm_grp, 0u};
-    uint32_t T = 0, nq = 0, chunk = 0;
+    uint32_t T = 0, nq = 0, chunk = 0, passed = 0;
     int qi = 0;
     bool ok = true;
-    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
+    // Grid-wide lock-step of the scatter (bar_every > 0): CTAs process
+    // generation g = their g-th query together (queries t of one generation
+    // lie within gridDim.x of each other, so tile j of each covers the same
+    // band of keys) and meet every bar_every tiles; the live band of the
+    // dK/dV accumulators then stays L2-resident.  bar_points barrier points
+    // per generation for every CTA, tiles or not (the grid is co-resident).
+    auto grid_sync = [&]() -> bool {
+      if (!G.sync(W)) return false;
+      bool okg = true;
+      if (tid == 0) {
+        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(grid_ctr) : "memory");
+        const uint32_t target = (passed + 1u) * gridDim.x;
+        const uint64_t t0 = globaltimer_ns();
+        for (;;) {
+          uint32_t cur;
+          asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(grid_ctr) : "memory");
+          if ((int32_t)(cur - target) >= 0) break;
+          if (*abort_flag) { okg = false; break; }
+          if (globaltimer_ns() - t0 > timeout_ns) {
+            W.fail(DSA_ERR_DEVICE_TIMEOUT);
+            okg = false;
+            break;
+          }
+          __nanosleep(256);
+        }
+      }
+      ++passed;
+      return G.sync(W) && okg && !W.aborted();
+    };
+    const int64_t n_gens = (n_items + gridDim.x - 1) / gridDim.x;
+    for (int64_t gen = 0; gen < n_gens && ok; ++gen) {
+      const int64_t item = blockIdx.x + gen * gridDim.x;
+      if (item >= n_items) {  // no query left here: keep the others moving
+        for (int k2 = 0; bar_every > 0 && k2 < bar_points && ok; ++k2) ok = grid_sync();
+        continue;
+      }
       const int64_t t = S - 1 - item / n_hblk;
       const int hb = (int)(item % n_hblk);
       const int buf = qi & 1;
@@ -413,10 +458,11 @@ __global__ void __maxnreg__(kMaxReg)
       if (ntiles == 0) {  // empty key set: dQ = 0, no dK/dV contribution
         for (int e = tid; e < hcount * D; e += kSmThreads)
           dq[(t * H + hb * 64) * (int64_t)D + e] = __float2bfloat16_rn(0.f);
-        mbar_arrive(toks_empty(buf));
-        continue;
       }
-      for (int j = 0; j < ntiles && ok; ++j, ++T) {
+      const int jmax = bar_every > 0 ? bar_points * bar_every : ntiles;
+      for (int j = 0; j < jmax && ok; ++j) {
+        if (bar_every > 0 && j > 0 && j % bar_every == 0 && !(ok = grid_sync())) break;
+        if (j >= ntiles) continue;
         // ---- P and dS for key i, heads grp*32 .. +31
         if (!(ok = W.wait(sdp_full, T & 1u))) break;
         tc_fence_after();
@@ -435,38 +481,39 @@ __global__ void __maxnreg__(kMaxReg)
           pb[e >> 1] = pack_bf16(p0, p1);
           db[e >> 1] = pack_bf16(p0 * (pv[e] - dl[e]), p1 * (pv[e + 1] - dl[e + 1]));
         }
-        // row i of the [key x 64 h] buffer: this group's 64 bytes = 4 chunks
+        // row i of the [key x 64 h] buffer: this group's 64 bytes = 4 chunks.
+        // dS goes in first (dQ^T, dK^T), then P (dV^T).
         const uint32_t rowa = sB + (uint32_t)i * 128u;
-        if (!(ok = W.wait(dsbuf_free, (T & 1u) ^ 1u))) break;  // previous dS read
+        if (!(ok = W.wait(pbuf_free, (T & 1u) ^ 1u))) break;  // previous P read
 #pragma unroll
         for (int c = 0; c < 4; ++c)
           asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
                            rowa + (((uint32_t)(grp * 4 + c) ^ (uint32_t)(i & 7)) << 4)),
-                       "r"(pb[4 * c]), "r"(pb[4 * c + 1]), "r"(pb[4 * c + 2]),
-                       "r"(pb[4 * c + 3])
+                       "r"(db[4 * c]), "r"(db[4 * c + 1]), "r"(db[4 * c + 2]),
+                       "r"(db[4 * c + 3])
                        : "memory");
         fence_proxy_async();
         tc_fence_before();
-        mbar_arrive(pbuf_full);
+        mbar_arrive(dsbuf_full);
         if (!(ok = G.sync(W))) break;  // stt[] complete
-        // ---- scatter the dV^T chunks, then (after dS is in place) dK^T
+        // ---- scatter the dK^T chunks, then (after P is in place) dV^T
         for (int which = 0; which < 2 && ok; ++which) {
           if (which == 1) {
-            // dV^T has read every P: put dS in the buffer for dK^T and dQ^T
-            if (!(ok = W.wait(pbuf_free, T & 1u))) break;
+            // dQ^T and dK^T have read every dS: put P in the buffer for dV^T
+            if (!(ok = W.wait(dsbuf_free, T & 1u))) break;
 #pragma unroll
             for (int c = 0; c < 4; ++c)
               asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
                                rowa + (((uint32_t)(grp * 4 + c) ^ (uint32_t)(i & 7)) << 4)),
-                           "r"(db[4 * c]), "r"(db[4 * c + 1]), "r"(db[4 * c + 2]),
-                           "r"(db[4 * c + 3])
+                           "r"(pb[4 * c]), "r"(pb[4 * c + 1]), "r"(pb[4 * c + 2]),
+                           "r"(pb[4 * c + 3])
                            : "memory");
             fence_proxy_async();
             tc_fence_before();
-            mbar_arrive(dsbuf_full);
+            mbar_arrive(pbuf_full);
           }
-          float* acc = which == 0 ? dv_acc : dk_acc;
-          const float f = which == 0 ? 1.f : scale;
+          float* acc = which == 0 ? dk_acc : dv_acc;
+          const float f = which == 0 ? scale : 1.f;
           for (int q = 0; q < 2 * C::kDChunks; ++q, ++chunk) {
             const int dc = q >> 1, kh = q & 1;
             const int b = (int)(chunk & 1u);
@@ -488,8 +535,15 @@ __global__ void __maxnreg__(kMaxReg)
             }
           }
         }
+        ++T;
       }
       if (!ok) break;
+      if (bar_every > 0 && !(ok = grid_sync())) break;  // last point of the generation
+      if (ntiles == 0) {
+        mbar_arrive(toks_empty(buf));
+        ++qi;
+        continue;
+      }
       // ---- dQ = scale * dQ^T -> bf16 (thread = d within each 128-d chunk)
       if (!(ok = W.wait(dq_done, nq & 1u))) break;
       tc_fence_after();
@@ -509,6 +563,7 @@ __global__ void __maxnreg__(kMaxReg)
       mbar_arrive(tq_empty);
       mbar_arrive(toks_empty(buf));
       ++nq;
+      ++qi;
     }
   }
 
@@ -548,10 +603,35 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
   const int64_t items = s.S * n_hblk;
   int64_t grid = c.num_sms;
   if (grid > items) grid = items;
-  attn_bwd_tc_kernel<D><<<(unsigned)grid, kThreads, smem, c.stream>>>(
-      qm, gm, k, v, lse, delta, idx, dq, dk_acc, dv_acc, s.S, s.H, s.K_p, s.n_loc,
-      s.scale, n_hblk, c.status, c.timeout_ns);
-  return cudaGetLastError();
+  // lock-step scatter only when the fp32 dK/dV accumulators outgrow L2
+  const int max_tiles = (4 * s.K_p + s.n_loc + kTileK - 1) / kTileK;
+  int bar_every = (double)s.S * s.D * 8.0 > 96.0 * (1 << 20) ? kBarEvery : 0;
+  if (grid < 2) bar_every = 0;
+  int bar_points = bar_every > 0 ? (max_tiles + bar_every - 1) / bar_every : 0;
+  uint32_t* grid_ctr = c.status + 32;  // zeroed by the delta kernel
+  if (bar_every == 0) {
+    attn_bwd_tc_kernel<D><<<(unsigned)grid, kThreads, smem, c.stream>>>(
+        qm, gm, k, v, lse, delta, idx, dq, dk_acc, dv_acc, s.S, s.H, s.K_p, s.n_loc,
+        s.scale, n_hblk, c.status, c.timeout_ns, grid_ctr, bar_every, bar_points);
+    return cudaGetLastError();
+  }
+  // the CTAs wait on one another: a cooperative launch guarantees that
+  // every CTA of the grid is resident at once (or refuses the launch)
+  const CUtensorMap q_arg = qm, g_arg = gm;
+  int64_t S_arg = s.S;
+  int H_arg = s.H, K_arg = s.K_p, nl_arg = s.n_loc, nh_arg = n_hblk;
+  float sc_arg = s.scale;
+  uint32_t* st_arg = c.status;
+  uint64_t to_arg = c.timeout_ns;
+  void* args[] = {(void*)&q_arg, (void*)&g_arg, (void*)&k, (void*)&v, (void*)&lse,
+                  (void*)&delta, (void*)&idx, (void*)&dq, (void*)&dk_acc,
+                  (void*)&dv_acc, (void*)&S_arg, (void*)&H_arg, (void*)&K_arg,
+                  (void*)&nl_arg, (void*)&sc_arg, (void*)&nh_arg, (void*)&st_arg,
+                  (void*)&to_arg, (void*)&grid_ctr, (void*)&bar_every,
+                  (void*)&bar_points};
+  return cudaLaunchCooperativeKernel((const void*)attn_bwd_tc_kernel<D>,
+                                     dim3((unsigned)grid), dim3(kThreads), args, smem,
+                                     c.stream);
 }
 
 }  // namespace
