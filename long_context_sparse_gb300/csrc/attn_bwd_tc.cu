@@ -9,22 +9,30 @@
 //
 //   S^T  [key, h] = K_tile Q^T          dP^T [key, h] = V_tile dO^T
 //   P = exp2(S c2 - LSE2), dS = P (dP - delta)      (thread = key lane)
-//   dV^T [d, key] = dO^T P^T            dK^T [d, key] = Q^T dS^T
 //   dQ^T [d, h]  += K_tile^T dS          (TMEM-resident over the tiles)
+//   dK^T [d, key] = Q^T dS^T            dV^T [d, key] = dO^T P^T
 //
-// with K/V rows gathered once per tile (K a second time for dQ, from L2).
-// Order per tile: S^T, dP^T; dS -> dQ^T, dK^T; P -> dV^T, so the gather
-// ring is free for the next tile while the dK/dV chunks are scattered.
-// dV^T / dK^T are produced in [128 d x 64 key] chunks with d on the TMEM
-// lanes, so each thread holds one d of a key row and a warp's fp32
-// reduction covers one contiguous 128-byte segment of that row: the scatter
-// into the fp32 dK/dV accumulators is fully coalesced.
+// dK^T / dV^T are produced in [128 d x 64 key] chunks with d on the TMEM
+// lanes, so a warp's fp32 reduction into the dK/dV accumulators covers one
+// contiguous 128-byte segment of a key row (fully coalesced).  That scatter
+// carries 4 KB per (query, key) pair at d = 512 and is the bound of the
+// whole backward, so the kernel is organised to keep it running without a
+// break: eight warps do nothing but drain chunks from TMEM into
+// red.global.add, while the products of the next chunks and tiles proceed
+// behind them.
 //
-// Heads are padded to N = 64 (padding heads get P = 0 through LSE = +inf).
-// Warps: 0-7 softmax / scatter / dQ epilogue (two warpgroups of 32 heads;
-// warp w reads TMEM lane quadrant w % 4), 8-9 gather producers (cp.async
-// into 128-byte-swizzled 16 KB stages), 10 MMA issuer and TMEM owner.  Q
-// and dO come in by TMA.  Every wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
+// Roles (16 warps):
+//   0-3   softmax: P and dS of a tile (thread = key lane), written to two
+//         separate shared buffers; the dQ epilogue of each query.
+//   4-11  scatter: TMEM chunk -> fp32 reductions (warp w reads lane quadrant
+//         w % 4, half the chunk's 64 key columns).
+//   12-13 producers: key lists, Q/dO by TMA, K/V rows gathered with cp.async
+//         into 128-byte-swizzled 16 KB stages.
+//   14    MMA issuer A (TMEM owner): S^T, dP^T and dQ^T, in ring order.
+//   15    MMA issuer B: the dK^T and dV^T chunks.
+// Two issuers keep the chunk stream independent of the gather ring: A runs
+// up to a tile ahead of B.  Heads are padded to N = 64 (padding heads get
+// P = 0 through LSE = +inf).  Every wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
 #include "attn_common.cuh"
 #include "dsa_internal.h"
 
@@ -33,26 +41,28 @@ namespace {
 
 constexpr int NH = 64;                 // heads per CTA tile (N), padded
 constexpr int kTileK = 128;            // keys per tile
-constexpr int kStages = 4;             // 16 KB stages: [128 keys x 64 dims]
+constexpr int kStages = 3;             // 16 KB gather stages
 constexpr uint32_t kStageBytes = 16384;
-constexpr int kSmThreads = 256;
-constexpr int kProdThreads = 64;
-constexpr int kThreads = kSmThreads + kProdThreads + 32;  // 11 warps
-constexpr int kMmaWarp = 10;
+constexpr int kSmThreads = 128;        // softmax warps 0-3
+constexpr int kScThreads = 256;        // scatter warps 4-11
+constexpr int kProdThreads = 64;       // producer warps 12-13
+constexpr int kScWarp0 = 4, kProdWarp0 = 12, kMmaA = 14, kMmaB = 15;
+constexpr int kThreads = 512;
 constexpr int kBarEvery = 2;           // key tiles between grid-wide meetings
 constexpr int kMaskWords = (2048 * 4 + 3 + kTileK + 31) / 32;
-// the fullest SM sub-partition holds 3 of the 11 warps
+// four warps on every SM sub-partition
 constexpr int kMaxReg = (16384 / (((kThreads / 32) + 3) / 4 * 32)) & ~7;
+static_assert(kMaxReg == 128, "register budget");
 
 template <int D>
 struct BwdTcCfg {
-  static constexpr int kAtoms = D / 64;   // 64-dim atoms (stages per pass)
+  static constexpr int kAtoms = D / 64;   // 64-dim atoms: S / dP stages per tile
   static constexpr int kDChunks = D / 128;
   static constexpr uint32_t kQBytes = NH * D * 2;
-  static constexpr uint32_t kBufBytes = kTileK * NH * 2;  // P / dS [key x 64 h]
+  static constexpr uint32_t kBufBytes = kTileK * NH * 2;  // P or dS [key x 64 h]
   static uint32_t smem(int K_p) {
-    return 1024 + 2 * kQBytes + kBufBytes + kStages * kStageBytes +
-           carved(2 * (K_p + 8) * 4) + 2 * carved(2 * kTileK * 4) +
+    return 1024 + 2 * kQBytes + 2 * kBufBytes + kStages * kStageBytes +
+           carved(2 * (K_p + 8) * 4) + carved(2 * kTileK * 4) +
            carved(2 * kMaskWords * 4) + 2 * carved(2 * NH * 4) + carved(32) +
            carved(32 * 8);
   }
@@ -99,14 +109,14 @@ __global__ void __maxnreg__(kMaxReg)
   uint8_t* gb = smem_raw + (base - raw);
   const uint32_t sQ = base;                      // Q   [64 h x D], atoms of 8 KB
   const uint32_t sG = sQ + C::kQBytes;           // dO  [64 h x D]
-  const uint32_t sB = sG + C::kQBytes;           // P / dS [128 key x 64 h]
-  const uint32_t sStage = sB + C::kBufBytes;     // ring, 1024-aligned
+  const uint32_t sDS = sG + C::kQBytes;          // dS  [128 key x 64 h]
+  const uint32_t sP = sDS + C::kBufBytes;        // P   [128 key x 64 h]
+  const uint32_t sStage = sP + C::kBufBytes;     // ring, 1024-aligned
   // tail regions, each starting on a 128-byte boundary (vector accesses)
-  uint8_t* tail = gb + 2 * C::kQBytes + C::kBufBytes + kStages * kStageBytes;
+  uint8_t* tail = gb + 2 * C::kQBytes + 2 * C::kBufBytes + kStages * kStageBytes;
   int32_t* pools = carve<int32_t>(tail, 2 * (K_p + 8));      // [2][K_p+8]
   int32_t* tile_tok = carve<int32_t>(tail, 2 * kTileK);      // [2][128]
   uint32_t* vmask = carve<uint32_t>(tail, 2 * kMaskWords);   // [2][words]
-  int32_t* sm_tok = carve<int32_t>(tail, 2 * kTileK);        // [2][128]
   float* lse2_s = carve<float>(tail, 2 * NH);                // [2][NH]
   float* delta_s = carve<float>(tail, 2 * NH);               // [2][NH]
   int* misc = carve<int>(tail, 8);                 // ntok[2], npool[2], last, nadd
@@ -116,15 +126,17 @@ __global__ void __maxnreg__(kMaxReg)
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
   const uint32_t b1 = bar0 + 8u * (2 * kStages);
   const uint32_t qd_full = b1, qd_empty = b1 + 8, sdp_full = b1 + 16,
-                 pbuf_full = b1 + 24, pbuf_free = b1 + 32, dsbuf_full = b1 + 40,
-                 dsbuf_free = b1 + 48, dq_done = b1 + 56, tq_empty = b1 + 64,
-                 done_bar = b1 + 72, sm_grp = b1 + 80, prod_grp = b1 + 88;
-  auto chunk_full = [&](int b) { return b1 + 96u + 8u * b; };
-  auto chunk_empty = [&](int b) { return b1 + 112u + 8u * b; };
-  auto toks_full = [&](int b) { return b1 + 128u + 8u * b; };
-  auto toks_empty = [&](int b) { return b1 + 144u + 8u * b; };
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 20);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 21);
+                 sdp_free = b1 + 24, ds_full = b1 + 32, ds_free = b1 + 40,
+                 p_full = b1 + 48, p_free = b1 + 56, dq_done = b1 + 64,
+                 tq_empty = b1 + 72, done_a = b1 + 80, done_b = b1 + 88,
+                 sm_grp = b1 + 96, sc_grp = b1 + 104, prod_grp = b1 + 112;
+  auto chunk_full = [&](int b) { return b1 + 120u + 8u * b; };
+  auto chunk_empty = [&](int b) { return b1 + 136u + 8u * b; };
+  auto toks_full = [&](int b) { return b1 + 152u + 8u * b; };
+  auto toks_empty = [&](int b) { return b1 + 168u + 8u * b; };
+  // 6 ring barriers + 23 above = 29 of the 32 slots; slot 30 abort, 31 TMEM
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 30);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 31);
   int* ntok = misc;        // [2]
   int* npool_s = misc + 2; // [2]
   int* s_last = misc + 4;
@@ -134,6 +146,8 @@ __global__ void __maxnreg__(kMaxReg)
   const Waiter W{abort_flag, status, timeout_ns};
   const int64_t n_items = S * n_hblk;
   const float c2 = scale * kLog2e;
+  // every consumer of a query's key list releases it once
+  constexpr uint32_t kToksUsers = kSmThreads + kScThreads + 2;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -143,27 +157,30 @@ __global__ void __maxnreg__(kMaxReg)
     mbar_init(qd_full, 1);
     mbar_init(qd_empty, 1);
     mbar_init(sdp_full, 1);
-    mbar_init(pbuf_full, kSmThreads);
-    mbar_init(pbuf_free, 1);
-    mbar_init(dsbuf_full, kSmThreads);
-    mbar_init(dsbuf_free, 1);
+    mbar_init(sdp_free, kSmThreads);
+    mbar_init(ds_full, kSmThreads);
+    mbar_init(ds_free, 2);              // issuer A (dQ^T) and issuer B (dK^T)
+    mbar_init(p_full, kSmThreads);
+    mbar_init(p_free, 1);
     mbar_init(dq_done, 1);
     mbar_init(tq_empty, kSmThreads);
-    mbar_init(done_bar, 1);
+    mbar_init(done_a, 1);
+    mbar_init(done_b, 1);
     mbar_init(sm_grp, kSmThreads);
+    mbar_init(sc_grp, kScThreads);
     mbar_init(prod_grp, kProdThreads);
     for (int b = 0; b < 2; ++b) {
       mbar_init(chunk_full(b), 1);
-      mbar_init(chunk_empty(b), kSmThreads);
+      mbar_init(chunk_empty(b), kScThreads);
       mbar_init(toks_full(b), kProdThreads);
-      mbar_init(toks_empty(b), kSmThreads);
+      mbar_init(toks_empty(b), kToksUsers);
     }
     *abort_flag = 0u;
     fence_mbar_init();
     prefetch_tensormap(&q_map);
     prefetch_tensormap(&g_map);
   }
-  if (warp == kMmaWarp) tmem_alloc(smem_u32(tmem_slot), 512);
+  if (warp == kMmaA) tmem_alloc(smem_u32(tmem_slot), 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -173,9 +190,19 @@ __global__ void __maxnreg__(kMaxReg)
   const uint32_t tQ = tmem + 128;      // dQ^T  [128 d x 64 h] x D/128
   const uint32_t tC = tmem + 384;      // 2 x [128 d x 64 key] chunk accumulators
 
-  if (warp == 8 || warp == 9) {
+  // token of key slot `slot` of a query's list (-1: empty or invalid)
+  auto tok_of = [&](const int32_t* pl, const int32_t* lc, int npool, int n,
+                    int slot) -> int32_t {
+    if (slot < npool) {
+      const int32_t p = pl[slot >> 2];
+      return p >= 0 ? 4 * p + (slot & 3) : -1;
+    }
+    return slot < n ? lc[slot - npool] : -1;
+  };
+
+  if (warp >= kProdWarp0 && warp < kMmaA) {
     // ============================================ gather producers (64)
-    const int ptid = tid - kSmThreads;
+    const int ptid = tid - kProdWarp0 * 32;
     GroupBar G{prod_grp, 0u};
     uint32_t u = 0, nq = 0;
     int qi = 0;
@@ -255,21 +282,16 @@ __global__ void __maxnreg__(kMaxReg)
         }
       }
       ++nq;
-      // ---- per tile: K (for S^T), V (for dP^T), K again (for dQ^T), one
-      // 64-dim atom per stage.  A warp instruction copies 4 rows x 128 B.
-      auto tok_of = [&](int slot) -> int32_t {
-        if (slot < npool) {
-          const int32_t p = pl[slot >> 2];
-          return p >= 0 ? 4 * p + (slot & 3) : -1;
-        }
-        return slot < n ? lc[slot - npool] : -1;
-      };
+      // ---- per tile: K atoms [128 key x 64 d] (S^T), V atoms (dP^T), then
+      // K again in [2 x (64 key x 64 d)] stages, one per (128-d chunk, key
+      // half), for dQ^T.  A warp instruction copies 4 rows x 128 B.
       const int pw = ptid >> 5, plane = ptid & 31;
       const int rsub = plane >> 3, ch8 = plane & 7;
       bool ok = true;
       for (int j = 0; j < ntiles && ok; ++j) {
         int32_t* tt = tile_tok + (j & 1) * kTileK;
-        for (int r = ptid; r < kTileK; r += kProdThreads) tt[r] = tok_of(j * kTileK + r);
+        for (int r = ptid; r < kTileK; r += kProdThreads)
+          tt[r] = tok_of(pl, lc, npool, n, j * kTileK + r);
         if (!(ok = G.sync(W))) break;
         for (int pass = 0; pass < 3 && ok; ++pass) {
           const __nv_bfloat16* src = pass == 1 ? v : k;
@@ -277,13 +299,29 @@ __global__ void __maxnreg__(kMaxReg)
             const int s = (int)(u % kStages);
             if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
             const uint32_t st = sStage + s * kStageBytes;
+            if (pass < 2) {
 #pragma unroll 4
-            for (int i = 0; i < 16; ++i) {
-              const int r = pw * 64 + 4 * i + rsub;
-              const int32_t tok = tt[r];
-              const __nv_bfloat16* sp =
-                  src + (int64_t)(tok >= 0 ? tok : 0) * D + a * 64 + ch8 * 8;
-              cp_async16(st + r * 128 + ((ch8 ^ (r & 7)) << 4), sp, tok >= 0 ? 16u : 0u);
+              for (int i = 0; i < 16; ++i) {
+                const int r = pw * 64 + 4 * i + rsub;
+                const int32_t tok = tt[r];
+                const __nv_bfloat16* sp =
+                    src + (int64_t)(tok >= 0 ? tok : 0) * D + a * 64 + ch8 * 8;
+                cp_async16(st + r * 128 + ((ch8 ^ (r & 7)) << 4), sp,
+                           tok >= 0 ? 16u : 0u);
+              }
+            } else {
+              // stage a = (dc, kh): keys kh*64 .. +63, dims dc*128 .. +127
+              const int dc = a >> 1, kh = a & 1;
+#pragma unroll 4
+              for (int i = 0; i < 16; ++i) {
+                const int rr = pw * 64 + 4 * i + rsub;   // 0..127
+                const int blk = rr >> 6, r = rr & 63;    // d block, key row
+                const int32_t tok = tt[kh * 64 + r];
+                const __nv_bfloat16* sp = src + (int64_t)(tok >= 0 ? tok : 0) * D +
+                                          dc * 128 + blk * 64 + ch8 * 8;
+                cp_async16(st + blk * 8192 + r * 128 + ((ch8 ^ (r & 7)) << 4), sp,
+                           tok >= 0 ? 16u : 0u);
+              }
             }
             cp_async_mbar_arrive(full(s));
           }
@@ -292,20 +330,23 @@ __global__ void __maxnreg__(kMaxReg)
       if (!ok) break;
     }
     asm volatile("cp.async.wait_all;" ::: "memory");
-  } else if (warp == kMmaWarp) {
-    // ================================================== MMA issuer
+  } else if (warp == kMmaA) {
+    // ======================== MMA issuer A: S^T, dP^T, dQ^T (ring order)
     if (lane == 0) {
-      uint32_t u = 0, T = 0, nq = 0, chunk = 0;
+      uint32_t u = 0, T = 0, nq = 0;
       int qi = 0;
       bool ok = true, issued = false;
       for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
         const int buf = qi & 1;
         if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
         const int ntiles = (ntok[buf] + kTileK - 1) / kTileK;
+        mbar_arrive(toks_empty(buf));
         if (ntiles == 0) continue;
         if (!(ok = W.wait(qd_full, nq & 1u))) break;
         for (int j = 0; j < ntiles && ok; ++j, ++T) {
-          // ---- S^T = K Q^T, then dP^T = V dO^T (one 64-dim atom per stage)
+          // S^T / dP^T of the previous tile have been read
+          if (!(ok = W.wait(sdp_free, (T & 1u) ^ 1u))) break;
+          tc_fence_after();
           for (int pass = 0; pass < 2 && ok; ++pass) {
             const uint32_t dst = pass == 0 ? tS : tP;
             const uint32_t bsrc = pass == 0 ? sQ : sG;
@@ -326,39 +367,57 @@ __global__ void __maxnreg__(kMaxReg)
           }
           if (!ok) break;
           tc_commit(sdp_full);
-          // ---- dS in sB: dQ^T += K^T dS^T first (K re-gathered, two atoms
-          // per 128-dim chunk), so the stage ring is free for the next tile's
-          // gather while the chunks below are scattered
-          if (!(ok = W.wait(dsbuf_full, T & 1u))) break;
+          // ---- dQ^T += K^T dS^T, one [128 d x 64 key] stage at a time
+          if (!(ok = W.wait(ds_full, T & 1u))) break;
           tc_fence_after();
           if (j == 0 && !(ok = W.wait(tq_empty, (nq & 1u) ^ 1u))) break;
-          for (int dc = 0; dc < C::kDChunks && ok; ++dc, u += 2) {
-            const int s0 = (int)(u % kStages);  // u is even: s0, s0+1 adjacent
-            if (!(ok = W.wait(full(s0), (u / kStages) & 1u))) break;
-            if (!(ok = W.wait(full(s0 + 1), ((u + 1) / kStages) & 1u))) break;
+          for (int a = 0; a < C::kAtoms && ok; ++a, ++u) {
+            const int dc = a >> 1, kh = a & 1;
+            const int s = (int)(u % kStages);
+            if (!(ok = W.wait(full(s), (u / kStages) & 1u))) break;
             fence_proxy_async();
             tc_fence_after();
-            const uint32_t st = sStage + s0 * kStageBytes;
+            const uint32_t st = sStage + s * kStageBytes;
 #pragma unroll
-            for (int ks = 0; ks < kTileK / 16; ++ks)
+            for (int ks = 0; ks < 4; ++ks)
               tc_mma(tQ + dc * NH,
-                     // A = K^T [128 d x 16 key]: MN-major, atoms 16 KB apart
-                     sdesc_sw128(st + ks * 2048, kStageBytes, 1024),
-                     // B = dS^T [64 h x 16 key]: MN-major rows of 64 heads
-                     sdesc_sw128(sB + ks * 2048, 16, 1024), ID_MM,
-                     (j | ks) != 0 ? 1u : 0u);
-            tc_commit(empty(s0));
-            tc_commit(empty(s0 + 1));
+                     // A = K^T [128 d x 16 key]: MN-major, d blocks 8 KB apart
+                     sdesc_sw128(st + ks * 2048, 8192, 1024),
+                     // B = dS^T [16 key x 64 h]: MN-major rows of 64 heads
+                     sdesc_sw128(sDS + (kh * 64 + ks * 16) * 128, 16, 1024), ID_MM,
+                     (j | kh | ks) != 0 ? 1u : 0u);
+            tc_commit(empty(s));
           }
           if (!ok) break;
-          // ---- dK^T (dS in sB), then dV^T (P in sB): [128 d x 64 key] chunks
+          tc_commit(ds_free);
+          if (j == ntiles - 1) tc_commit(dq_done);
+        }
+        ++nq;
+      }
+      if (issued) {
+        tc_commit(done_a);
+        drain(done_a, 0, timeout_ns);
+      }
+    }
+  } else if (warp == kMmaB) {
+    // ============================ MMA issuer B: dK^T, dV^T chunks
+    if (lane == 0) {
+      uint32_t T = 0, nq = 0, chunk = 0;
+      int qi = 0;
+      bool ok = true, issued = false;
+      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
+        const int buf = qi & 1;
+        if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
+        const int ntiles = (ntok[buf] + kTileK - 1) / kTileK;
+        mbar_arrive(toks_empty(buf));
+        if (ntiles == 0) continue;
+        if (!(ok = W.wait(qd_full, nq & 1u))) break;
+        for (int j = 0; j < ntiles && ok; ++j, ++T) {
           for (int which = 0; which < 2 && ok; ++which) {
-            if (which == 1) {
-              tc_commit(dsbuf_free);  // dQ^T and dK^T have read dS
-              if (!(ok = W.wait(pbuf_full, T & 1u))) break;
-              tc_fence_after();
-            }
+            const uint32_t bsrc = which == 0 ? sDS : sP;
             const uint32_t asrc = which == 0 ? sQ : sG;
+            if (!(ok = W.wait(which == 0 ? ds_full : p_full, T & 1u))) break;
+            tc_fence_after();
             for (int q = 0; q < 2 * C::kDChunks; ++q, ++chunk) {
               const int dc = q >> 1, kh = q & 1;
               const int b = (int)(chunk & 1u);
@@ -370,45 +429,143 @@ __global__ void __maxnreg__(kMaxReg)
                        // A = X^T [128 d x 16 h]: MN-major, 64-dim atoms 8 KB apart
                        sdesc_sw128(asrc + (2 * dc) * (NH * 128) + ks * 2048, NH * 128, 1024),
                        // B = dS or P [64 key x 16 h]: K-major rows of 64 heads
-                       sdesc_sw128(sB + kh * 64 * 128 + ks * 32, 16, 1024), ID_MK,
+                       sdesc_sw128(bsrc + kh * 64 * 128 + ks * 32, 16, 1024), ID_MK,
                        ks > 0 ? 1u : 0u);
+              issued = true;
               tc_commit(chunk_full(b));
             }
+            if (!ok) break;
+            tc_commit(which == 0 ? ds_free : p_free);
           }
           if (!ok) break;
-          tc_commit(pbuf_free);  // dV^T has read P: the next tile's dS may go in
-          if (j == ntiles - 1) {
-            tc_commit(dq_done);
-            tc_commit(qd_empty);
-          }
+          if (j == ntiles - 1) tc_commit(qd_empty);  // last read of Q and dO
         }
         ++nq;
       }
       if (issued) {
-        tc_commit(done_bar);
-        drain(done_bar, 0, timeout_ns);
+        tc_commit(done_b);
+        drain(done_b, 0, timeout_ns);
       }
     }
-  } else {
-    // ============ softmax, dK/dV scatter and dQ epilogue (2 x 128 threads)
-    const int i = tid & 127;              // key lane / d lane
-    const int grp = tid >> 7;             // heads grp*32 .. +31, keys grp*32 ..
-    const int wq = warp & 3;
-    const uint32_t lane_base = (uint32_t)(wq * 32) << 16;
-    GroupBar G{sm_grp, 0u};
-    uint32_t T = 0, nq = 0, chunk = 0, passed = 0;
+  } else if (warp < kScWarp0) {
+    // ==================== softmax (128 threads, thread = key lane) + dQ
+    const int i = tid;                     // key lane / d lane
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    uint32_t T = 0, nq = 0;
     int qi = 0;
     bool ok = true;
-    // Grid-wide lock-step of the scatter (bar_every > 0): CTAs process
-    // generation g = their g-th query together (queries t of one generation
-    // lie within gridDim.x of each other, so tile j of each covers the same
-    // band of keys) and meet every bar_every tiles; the live band of the
-    // dK/dV accumulators then stays L2-resident.  bar_points barrier points
-    // per generation for every CTA, tiles or not (the grid is co-resident).
+    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
+      const int64_t t = S - 1 - item / n_hblk;
+      const int hb = (int)(item % n_hblk);
+      const int buf = qi & 1;
+      if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
+      const int n = ntok[buf];
+      const uint32_t* vm = vmask + buf * kMaskWords;
+      const float* l2 = lse2_s + buf * NH;
+      const float* dl = delta_s + buf * NH;
+      const int ntiles = (n + kTileK - 1) / kTileK;
+      const int hcount = H - hb * 64 < 64 ? H - hb * 64 : 64;
+      if (ntiles == 0) {  // empty key set: dQ = 0, no dK/dV contribution
+        for (int e = i; e < hcount * D; e += kSmThreads)
+          dq[(t * H + hb * 64) * (int64_t)D + e] = __float2bfloat16_rn(0.f);
+        mbar_arrive(toks_empty(buf));
+        continue;
+      }
+      const uint32_t rowa = (uint32_t)i * 128u;  // row i of a [key x 64 h] buffer
+      for (int j = 0; j < ntiles && ok; ++j, ++T) {
+        const int slot = j * kTileK + i;
+        const bool valid = (vm[slot >> 5] >> (slot & 31)) & 1u;
+        // dQ^T and dK^T of the previous tile have read dS
+        if (!(ok = W.wait(ds_free, (T & 1u) ^ 1u))) break;
+        if (!(ok = W.wait(sdp_full, T & 1u))) break;
+        tc_fence_after();
+        uint32_t pb[32];
+#pragma unroll
+        for (int qh = 0; qh < 4; ++qh) {  // 16 heads at a time
+          uint32_t sa[16], pa[16];
+          tmem_ld16(tS + lane_base + qh * 16, sa);
+          tmem_ld16(tP + lane_base + qh * 16, pa);
+          tmem_wait_ld();
+          uint32_t db[8];
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) {
+            const int h = qh * 16 + e;
+            const float p0 =
+                valid ? exp2f(__uint_as_float(sa[e]) * c2 - l2[h]) : 0.f;
+            const float p1 =
+                valid ? exp2f(__uint_as_float(sa[e + 1]) * c2 - l2[h + 1]) : 0.f;
+            pb[(h >> 1)] = pack_bf16(p0, p1);
+            db[e >> 1] = pack_bf16(p0 * (__uint_as_float(pa[e]) - dl[h]),
+                                   p1 * (__uint_as_float(pa[e + 1]) - dl[h + 1]));
+          }
+#pragma unroll
+          for (int c = 0; c < 2; ++c)
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
+                             sDS + rowa + (((uint32_t)(qh * 2 + c) ^ (uint32_t)(i & 7)) << 4)),
+                         "r"(db[4 * c]), "r"(db[4 * c + 1]), "r"(db[4 * c + 2]),
+                         "r"(db[4 * c + 3])
+                         : "memory");
+        }
+        tc_fence_before();
+        mbar_arrive(sdp_free);
+        fence_proxy_async();
+        mbar_arrive(ds_full);
+        // dV^T of the previous tile has read P
+        if (!(ok = W.wait(p_free, (T & 1u) ^ 1u))) break;
+#pragma unroll
+        for (int c = 0; c < 8; ++c)
+          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
+                           sP + rowa + (((uint32_t)c ^ (uint32_t)(i & 7)) << 4)),
+                       "r"(pb[4 * c]), "r"(pb[4 * c + 1]), "r"(pb[4 * c + 2]),
+                       "r"(pb[4 * c + 3])
+                       : "memory");
+        fence_proxy_async();
+        mbar_arrive(p_full);
+      }
+      if (!ok) break;
+      // ---- dQ = scale * dQ^T -> bf16 (thread = d within each 128-d chunk)
+      if (!(ok = W.wait(dq_done, nq & 1u))) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int dc = 0; dc < C::kDChunks; ++dc) {
+        const int d = dc * 128 + i;
+#pragma unroll 1
+        for (int hh = 0; hh < 2; ++hh) {
+          float qv[32];
+          tmem_ld32(tQ + dc * NH + lane_base + hh * 32, qv);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const int h = hh * 32 + e;
+            if (h < hcount)
+              dq[(t * H + hb * 64 + h) * (int64_t)D + d] = __float2bfloat16_rn(qv[e] * scale);
+          }
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(tq_empty);
+      mbar_arrive(toks_empty(buf));
+      ++nq;
+    }
+  } else {
+    // ========== scatter (256 threads): TMEM chunk -> fp32 reductions
+    const int sc = tid - kScWarp0 * 32;       // 0..255
+    const int quad = warp & 3, half = (warp - kScWarp0) >> 2;
+    const int di = quad * 32 + lane;          // d within a 128-d chunk
+    const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+    GroupBar G{sc_grp, 0u};
+    uint32_t chunk = 0, passed = 0;
+    int qi = 0;
+    bool ok = true;
+    // Grid-wide lock-step (bar_every > 0): CTAs process generation g = their
+    // g-th query together (queries of one generation lie within gridDim.x
+    // of each other, so tile j of each covers the same band of keys) and
+    // meet every bar_every tiles; the live band of the dK/dV accumulators
+    // then stays L2-resident.  bar_points barrier points per generation for
+    // every CTA, tiles or not (the grid is co-resident).
     auto grid_sync = [&]() -> bool {
       if (!G.sync(W)) return false;
       bool okg = true;
-      if (tid == 0) {
+      if (sc == 0) {
         asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(grid_ctr) : "memory");
         const uint32_t target = (passed + 1u) * gridDim.x;
         const uint64_t t0 = globaltimer_ns();
@@ -435,134 +592,53 @@ __global__ void __maxnreg__(kMaxReg)
         for (int k2 = 0; bar_every > 0 && k2 < bar_points && ok; ++k2) ok = grid_sync();
         continue;
       }
-      const int64_t t = S - 1 - item / n_hblk;
-      const int hb = (int)(item % n_hblk);
       const int buf = qi & 1;
       if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
       const int n = ntok[buf];
       const int npool = npool_s[buf];
       const int32_t* pl = pools + buf * (K_p + 8);
       const int32_t* lc = pl + K_p;
-      const uint32_t* vm = vmask + buf * kMaskWords;
-      const float* l2 = lse2_s + buf * NH + grp * 32;
-      const float* dl = delta_s + buf * NH + grp * 32;
       const int ntiles = (n + kTileK - 1) / kTileK;
-      auto tok_of = [&](int slot) -> int32_t {
-        if (slot < npool) {
-          const int32_t p = pl[slot >> 2];
-          return p >= 0 ? 4 * p + (slot & 3) : -1;
-        }
-        return slot < n ? lc[slot - npool] : -1;
-      };
-      const int hcount = H - hb * 64 < 64 ? H - hb * 64 : 64;
-      if (ntiles == 0) {  // empty key set: dQ = 0, no dK/dV contribution
-        for (int e = tid; e < hcount * D; e += kSmThreads)
-          dq[(t * H + hb * 64) * (int64_t)D + e] = __float2bfloat16_rn(0.f);
-      }
       const int jmax = bar_every > 0 ? bar_points * bar_every : ntiles;
       for (int j = 0; j < jmax && ok; ++j) {
         if (bar_every > 0 && j > 0 && j % bar_every == 0 && !(ok = grid_sync())) break;
         if (j >= ntiles) continue;
-        // ---- P and dS for key i, heads grp*32 .. +31
-        if (!(ok = W.wait(sdp_full, T & 1u))) break;
-        tc_fence_after();
-        float sv[32], pv[32];
-        tmem_ld32(tS + lane_base + grp * 32, sv);
-        tmem_ld32(tP + lane_base + grp * 32, pv);
-        const int slot = j * kTileK + i;
-        const bool valid = (vm[slot >> 5] >> (slot & 31)) & 1u;
-        int32_t* stt = sm_tok + (T & 1u) * kTileK;  // scatter targets of this tile
-        if (grp == 0) stt[i] = tok_of(slot);
-        uint32_t pb[16], db[16];
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          const float p0 = valid ? exp2f(sv[e] * c2 - l2[e]) : 0.f;
-          const float p1 = valid ? exp2f(sv[e + 1] * c2 - l2[e + 1]) : 0.f;
-          pb[e >> 1] = pack_bf16(p0, p1);
-          db[e >> 1] = pack_bf16(p0 * (pv[e] - dl[e]), p1 * (pv[e + 1] - dl[e + 1]));
-        }
-        // row i of the [key x 64 h] buffer: this group's 64 bytes = 4 chunks.
-        // dS goes in first (dQ^T, dK^T), then P (dV^T).
-        const uint32_t rowa = sB + (uint32_t)i * 128u;
-        if (!(ok = W.wait(pbuf_free, (T & 1u) ^ 1u))) break;  // previous P read
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                           rowa + (((uint32_t)(grp * 4 + c) ^ (uint32_t)(i & 7)) << 4)),
-                       "r"(db[4 * c]), "r"(db[4 * c + 1]), "r"(db[4 * c + 2]),
-                       "r"(db[4 * c + 3])
-                       : "memory");
-        fence_proxy_async();
-        tc_fence_before();
-        mbar_arrive(dsbuf_full);
-        if (!(ok = G.sync(W))) break;  // stt[] complete
-        // ---- scatter the dK^T chunks, then (after P is in place) dV^T
         for (int which = 0; which < 2 && ok; ++which) {
-          if (which == 1) {
-            // dQ^T and dK^T have read every dS: put P in the buffer for dV^T
-            if (!(ok = W.wait(dsbuf_free, T & 1u))) break;
-#pragma unroll
-            for (int c = 0; c < 4; ++c)
-              asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                               rowa + (((uint32_t)(grp * 4 + c) ^ (uint32_t)(i & 7)) << 4)),
-                           "r"(pb[4 * c]), "r"(pb[4 * c + 1]), "r"(pb[4 * c + 2]),
-                           "r"(pb[4 * c + 3])
-                           : "memory");
-            fence_proxy_async();
-            tc_fence_before();
-            mbar_arrive(pbuf_full);
-          }
-          float* acc = which == 0 ? dk_acc : dv_acc;
+          float* acc = (which == 0 ? dk_acc : dv_acc) + di;
           const float f = which == 0 ? scale : 1.f;
           for (int q = 0; q < 2 * C::kDChunks; ++q, ++chunk) {
             const int dc = q >> 1, kh = q & 1;
             const int b = (int)(chunk & 1u);
             if (!(ok = W.wait(chunk_full(b), (chunk >> 1) & 1u))) break;
             tc_fence_after();
-            float cv[32];  // d = dc*128 + i, keys kh*64 + grp*32 + e
-            tmem_ld32(tC + b * 64 + lane_base + grp * 32, cv);
+            float cv[32];  // d = dc*128 + di, keys kh*64 + half*32 + e
+            tmem_ld32(tC + b * 64 + lane_base + half * 32, cv);
             tc_fence_before();
             mbar_arrive(chunk_empty(b));
-            float* dst = acc + dc * 128 + i;
-            const int4* tk4 = reinterpret_cast<const int4*>(stt + kh * 64 + grp * 32);
+            float* dst = acc + dc * 128;
+            const int slot0 = j * kTileK + kh * 64 + half * 32;
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
-              const int4 tk = tk4[e4];  // warp-uniform tokens of 4 keys
-              const int32_t tks[4] = {tk.x, tk.y, tk.z, tk.w};
+              const int s4 = slot0 + 4 * e4;  // 4 keys of one pool (or locals)
+              int32_t tks[4];
+              if (s4 < npool) {
+                const int32_t p = pl[s4 >> 2];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) tks[e] = p >= 0 ? 4 * p + e : -1;
+              } else {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) tks[e] = s4 + e < n ? lc[s4 + e - npool] : -1;
+              }
 #pragma unroll
               for (int e = 0; e < 4; ++e)
                 if (tks[e] >= 0) red_add_f32(dst + (int64_t)tks[e] * D, f * cv[4 * e4 + e]);
             }
           }
         }
-        ++T;
       }
       if (!ok) break;
       if (bar_every > 0 && !(ok = grid_sync())) break;  // last point of the generation
-      if (ntiles == 0) {
-        mbar_arrive(toks_empty(buf));
-        ++qi;
-        continue;
-      }
-      // ---- dQ = scale * dQ^T -> bf16 (thread = d within each 128-d chunk)
-      if (!(ok = W.wait(dq_done, nq & 1u))) break;
-      tc_fence_after();
-#pragma unroll 1
-      for (int dc = 0; dc < C::kDChunks; ++dc) {
-        float qv[32];
-        tmem_ld32(tQ + dc * NH + lane_base + grp * 32, qv);
-        const int d = dc * 128 + i;
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const int h = grp * 32 + e;
-          if (h < hcount)
-            dq[(t * H + hb * 64 + h) * (int64_t)D + d] = __float2bfloat16_rn(qv[e] * scale);
-        }
-      }
-      tc_fence_before();
-      mbar_arrive(tq_empty);
       mbar_arrive(toks_empty(buf));
-      ++nq;
       ++qi;
     }
   }
@@ -571,7 +647,7 @@ __global__ void __maxnreg__(kMaxReg)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == kMmaWarp) tmem_dealloc(tmem, 512);
+  if (warp == kMmaA) tmem_dealloc(tmem, 512);
 }
 
 template <int D>
