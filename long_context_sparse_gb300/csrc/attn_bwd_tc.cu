@@ -12,9 +12,10 @@
 //   dQ^T [d, h]  += K_tile^T dS          (TMEM-resident over the tiles)
 //   dK^T [d, key] = Q^T dS^T            dV^T [d, key] = dO^T P^T
 //
-// dK^T / dV^T are produced in [128 d x 64 key] chunks with d on the TMEM
+// dK^T / dV^T are produced in [128 d x 32 key] chunks with d on the TMEM
 // lanes, so a warp's fp32 reduction into the dK/dV accumulators covers one
-// contiguous 128-byte segment of a key row (fully coalesced).  That scatter
+// contiguous 128-byte segment of a key row (fully coalesced).  The softmax
+// scale is folded into dS, so dQ and dK need no rescaling.  That scatter
 // carries 4 KB per (query, key) pair at d = 512 and is the bound of the
 // whole backward, so the kernel is organised to keep it running without a
 // break: eight warps do nothing but drain chunks from TMEM into
@@ -25,7 +26,8 @@
 //   0-3   softmax: P and dS of a tile (thread = key lane), written to two
 //         separate shared buffers; the dQ epilogue of each query.
 //   4-11  scatter: TMEM chunk -> fp32 reductions (warp w reads lane quadrant
-//         w % 4, half the chunk's 64 key columns).
+//         w % 4); warps 4-7 drain the even chunks, 8-11 the odd ones, each
+//         half double-buffered in TMEM.
 //   12-13 producers: key lists, Q/dO by TMA, K/V rows gathered with cp.async
 //         into 128-byte-swizzled 16 KB stages.
 //   14    MMA issuer A (TMEM owner): S^T, dP^T and dQ^T, in ring order.
@@ -64,12 +66,25 @@ struct BwdTcCfg {
     return 1024 + 2 * kQBytes + 2 * kBufBytes + kStages * kStageBytes +
            carved(2 * (K_p + 8) * 4) + carved(2 * kTileK * 4) +
            carved(2 * kMaskWords * 4) + 2 * carved(2 * NH * 4) + carved(32) +
-           carved(32 * 8);
+           carved(40 * 8);
   }
 };
 
 __device__ __forceinline__ void red_add_f32(float* p, float v) {
   asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+// The four keys of pool p are consecutive rows: one address, the other three
+// rows at immediate offsets of D floats.
+template <int D>
+__device__ __forceinline__ void red_add_pool(float* r, float a, float b, float c,
+                                             float d) {
+  asm volatile(
+      "red.global.add.f32 [%0], %1;\n\t"
+      "red.global.add.f32 [%0+%5], %2;\n\t"
+      "red.global.add.f32 [%0+%6], %3;\n\t"
+      "red.global.add.f32 [%0+%7], %4;" ::"l"(r),
+      "f"(a), "f"(b), "f"(c), "f"(d), "n"(D * 4), "n"(D * 8), "n"(D * 12)
+      : "memory");
 }
 // 32 consecutive fp32 TMEM columns of this thread's lane.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
@@ -100,7 +115,7 @@ __global__ void __maxnreg__(kMaxReg)
                        int bar_points) {
   using C = BwdTcCfg<D>;
   constexpr uint32_t ID_KK = idesc_bf16(128, NH, 0, 0);  // S^T, dP^T
-  constexpr uint32_t ID_MK = idesc_bf16(128, 64, 1, 0);  // dV^T, dK^T
+  constexpr uint32_t ID_MK = idesc_bf16(128, 32, 1, 0);  // dV^T, dK^T chunks
   constexpr uint32_t ID_MM = idesc_bf16(128, NH, 1, 1);  // dQ^T
 
   extern __shared__ uint8_t smem_raw[];
@@ -120,7 +135,7 @@ __global__ void __maxnreg__(kMaxReg)
   float* lse2_s = carve<float>(tail, 2 * NH);                // [2][NH]
   float* delta_s = carve<float>(tail, 2 * NH);               // [2][NH]
   int* misc = carve<int>(tail, 8);                 // ntok[2], npool[2], last, nadd
-  uint64_t* bars = carve<uint64_t>(tail, 32);
+  uint64_t* bars = carve<uint64_t>(tail, 40);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
@@ -130,13 +145,13 @@ __global__ void __maxnreg__(kMaxReg)
                  p_full = b1 + 48, p_free = b1 + 56, dq_done = b1 + 64,
                  tq_empty = b1 + 72, done_a = b1 + 80, done_b = b1 + 88,
                  sm_grp = b1 + 96, sc_grp = b1 + 104, prod_grp = b1 + 112;
-  auto chunk_full = [&](int b) { return b1 + 120u + 8u * b; };
-  auto chunk_empty = [&](int b) { return b1 + 136u + 8u * b; };
-  auto toks_full = [&](int b) { return b1 + 152u + 8u * b; };
-  auto toks_empty = [&](int b) { return b1 + 168u + 8u * b; };
-  // 6 ring barriers + 23 above = 29 of the 32 slots; slot 30 abort, 31 TMEM
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 30);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 31);
+  auto chunk_full = [&](int b) { return b1 + 120u + 8u * b; };   // [4]
+  auto chunk_empty = [&](int b) { return b1 + 152u + 8u * b; };  // [4]
+  auto toks_full = [&](int b) { return b1 + 184u + 8u * b; };
+  auto toks_empty = [&](int b) { return b1 + 200u + 8u * b; };
+  // 6 ring barriers + 27 above = 33 of the 40 slots; slot 38 abort, 39 TMEM
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 38);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 39);
   int* ntok = misc;        // [2]
   int* npool_s = misc + 2; // [2]
   int* s_last = misc + 4;
@@ -169,9 +184,11 @@ __global__ void __maxnreg__(kMaxReg)
     mbar_init(sm_grp, kSmThreads);
     mbar_init(sc_grp, kScThreads);
     mbar_init(prod_grp, kProdThreads);
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < 4; ++b) {
       mbar_init(chunk_full(b), 1);
-      mbar_init(chunk_empty(b), kScThreads);
+      mbar_init(chunk_empty(b), kScThreads / 2);  // one half of the scatter warps
+    }
+    for (int b = 0; b < 2; ++b) {
       mbar_init(toks_full(b), kProdThreads);
       mbar_init(toks_empty(b), kToksUsers);
     }
@@ -188,7 +205,7 @@ __global__ void __maxnreg__(kMaxReg)
   const uint32_t tS = tmem;            // S^T   [128 key x 64 h]
   const uint32_t tP = tmem + 64;       // dP^T  [128 key x 64 h]
   const uint32_t tQ = tmem + 128;      // dQ^T  [128 d x 64 h] x D/128
-  const uint32_t tC = tmem + 384;      // 2 x [128 d x 64 key] chunk accumulators
+  const uint32_t tC = tmem + 384;      // 4 x [128 d x 32 key] chunk accumulators
 
   // token of key slot `slot` of a query's list (-1: empty or invalid)
   auto tok_of = [&](const int32_t* pl, const int32_t* lc, int npool, int n,
@@ -418,18 +435,18 @@ __global__ void __maxnreg__(kMaxReg)
             const uint32_t asrc = which == 0 ? sQ : sG;
             if (!(ok = W.wait(which == 0 ? ds_full : p_full, T & 1u))) break;
             tc_fence_after();
-            for (int q = 0; q < 2 * C::kDChunks; ++q, ++chunk) {
-              const int dc = q >> 1, kh = q & 1;
-              const int b = (int)(chunk & 1u);
-              if (!(ok = W.wait(chunk_empty(b), ((chunk >> 1) & 1u) ^ 1u))) break;
+            for (int q = 0; q < 4 * C::kDChunks; ++q, ++chunk) {
+              const int dc = q >> 2, kq = q & 3;
+              const int b = (int)(chunk & 3u);
+              if (!(ok = W.wait(chunk_empty(b), ((chunk >> 2) & 1u) ^ 1u))) break;
               tc_fence_after();
 #pragma unroll
               for (int ks = 0; ks < NH / 16; ++ks)
-                tc_mma(tC + b * 64,
+                tc_mma(tC + b * 32,
                        // A = X^T [128 d x 16 h]: MN-major, 64-dim atoms 8 KB apart
                        sdesc_sw128(asrc + (2 * dc) * (NH * 128) + ks * 2048, NH * 128, 1024),
-                       // B = dS or P [64 key x 16 h]: K-major rows of 64 heads
-                       sdesc_sw128(bsrc + kh * 64 * 128 + ks * 32, 16, 1024), ID_MK,
+                       // B = dS or P [32 key x 16 h]: K-major rows of 64 heads
+                       sdesc_sw128(bsrc + kq * 32 * 128 + ks * 32, 16, 1024), ID_MK,
                        ks > 0 ? 1u : 0u);
               issued = true;
               tc_commit(chunk_full(b));
@@ -495,8 +512,8 @@ __global__ void __maxnreg__(kMaxReg)
             const float p1 =
                 valid ? exp2f(__uint_as_float(sa[e + 1]) * c2 - l2[h + 1]) : 0.f;
             pb[(h >> 1)] = pack_bf16(p0, p1);
-            db[e >> 1] = pack_bf16(p0 * (__uint_as_float(pa[e]) - dl[h]),
-                                   p1 * (__uint_as_float(pa[e + 1]) - dl[h + 1]));
+            db[e >> 1] = pack_bf16(scale * p0 * (__uint_as_float(pa[e]) - dl[h]),
+                                   scale * p1 * (__uint_as_float(pa[e + 1]) - dl[h + 1]));
           }
 #pragma unroll
           for (int c = 0; c < 2; ++c)
@@ -523,7 +540,7 @@ __global__ void __maxnreg__(kMaxReg)
         mbar_arrive(p_full);
       }
       if (!ok) break;
-      // ---- dQ = scale * dQ^T -> bf16 (thread = d within each 128-d chunk)
+      // ---- dQ = dQ^T -> bf16 (thread = d within each 128-d chunk)
       if (!(ok = W.wait(dq_done, nq & 1u))) break;
       tc_fence_after();
 #pragma unroll 1
@@ -537,7 +554,7 @@ __global__ void __maxnreg__(kMaxReg)
           for (int e = 0; e < 32; ++e) {
             const int h = hh * 32 + e;
             if (h < hcount)
-              dq[(t * H + hb * 64 + h) * (int64_t)D + d] = __float2bfloat16_rn(qv[e] * scale);
+              dq[(t * H + hb * 64 + h) * (int64_t)D + d] = __float2bfloat16_rn(qv[e]);
           }
         }
       }
@@ -549,7 +566,7 @@ __global__ void __maxnreg__(kMaxReg)
   } else {
     // ========== scatter (256 threads): TMEM chunk -> fp32 reductions
     const int sc = tid - kScWarp0 * 32;       // 0..255
-    const int quad = warp & 3, half = (warp - kScWarp0) >> 2;
+    const int quad = warp & 3, half = (warp - kScWarp0) >> 2;  // chunk parity
     const int di = quad * 32 + lane;          // d within a 128-d chunk
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
     GroupBar G{sc_grp, 0u};
@@ -605,35 +622,36 @@ __global__ void __maxnreg__(kMaxReg)
         if (j >= ntiles) continue;
         for (int which = 0; which < 2 && ok; ++which) {
           float* acc = (which == 0 ? dk_acc : dv_acc) + di;
-          const float f = which == 0 ? scale : 1.f;
-          for (int q = 0; q < 2 * C::kDChunks; ++q, ++chunk) {
-            const int dc = q >> 1, kh = q & 1;
-            const int b = (int)(chunk & 1u);
-            if (!(ok = W.wait(chunk_full(b), (chunk >> 1) & 1u))) break;
+          // this half's chunks: q = half, half + 2, ... (chunk parity = half)
+          for (int q = half; q < 4 * C::kDChunks; q += 2) {
+            const uint32_t c = chunk + (uint32_t)q;
+            const int dc = q >> 2, kq = q & 3;
+            const int b = (int)(c & 3u);
+            if (!(ok = W.wait(chunk_full(b), (c >> 2) & 1u))) break;
             tc_fence_after();
-            float cv[32];  // d = dc*128 + di, keys kh*64 + half*32 + e
-            tmem_ld32(tC + b * 64 + lane_base + half * 32, cv);
+            float cv[32];  // d = dc*128 + di, keys kq*32 + e
+            tmem_ld32(tC + b * 32 + lane_base, cv);
             tc_fence_before();
             mbar_arrive(chunk_empty(b));
             float* dst = acc + dc * 128;
-            const int slot0 = j * kTileK + kh * 64 + half * 32;
+            const int slot0 = j * kTileK + kq * 32;
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const int s4 = slot0 + 4 * e4;  // 4 keys of one pool (or locals)
-              int32_t tks[4];
               if (s4 < npool) {
                 const int32_t p = pl[s4 >> 2];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) tks[e] = p >= 0 ? 4 * p + e : -1;
+                if (p >= 0)
+                  red_add_pool<D>(dst + (int64_t)(4 * p) * D, cv[4 * e4], cv[4 * e4 + 1],
+                                  cv[4 * e4 + 2], cv[4 * e4 + 3]);
               } else {
 #pragma unroll
-                for (int e = 0; e < 4; ++e) tks[e] = s4 + e < n ? lc[s4 + e - npool] : -1;
+                for (int e = 0; e < 4; ++e)
+                  if (s4 + e < n)
+                    red_add_f32(dst + (int64_t)lc[s4 + e - npool] * D, cv[4 * e4 + e]);
               }
-#pragma unroll
-              for (int e = 0; e < 4; ++e)
-                if (tks[e] >= 0) red_add_f32(dst + (int64_t)tks[e] * D, f * cv[4 * e4 + e]);
             }
           }
+          chunk += 4 * C::kDChunks;
         }
       }
       if (!ok) break;
