@@ -14,9 +14,9 @@ namespace {
 // delta[t,h] = sum_d dO[t,h,d] O[t,h,d] (fp32), one warp per (t,h) row.
 __global__ void __launch_bounds__(256) bwd_delta_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
-    float* __restrict__ delta, int64_t n_rows, int D, uint32_t* grid_ctr) {
-  // the backward's grid-barrier counter restarts at zero for every call
-  if (blockIdx.x == 0 && threadIdx.x == 0 && grid_ctr) *grid_ctr = 0u;
+    float* __restrict__ delta, int64_t n_rows, int D, uint32_t* sched) {
+  // the backward's work counter and tile clock restart at zero every call
+  if (blockIdx.x == 0 && threadIdx.x < 2 && sched) sched[threadIdx.x] = 0u;
   const int lane = threadIdx.x & 31;
   const int64_t w0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
   const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;

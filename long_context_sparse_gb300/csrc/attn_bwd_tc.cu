@@ -22,19 +22,31 @@
 // red.global.add, while the products of the next chunks and tiles proceed
 // behind them.
 //
-// Roles (16 warps):
+// Roles (18 warps):
 //   0-3   softmax: P and dS of a tile (thread = key lane), written to two
 //         separate shared buffers; the dQ epilogue of each query.
 //   4-11  scatter: TMEM chunk -> fp32 reductions (warp w reads lane quadrant
 //         w % 4); warps 4-7 drain the even chunks, 8-11 the odd ones, each
 //         half double-buffered in TMEM.
-//   12-13 producers: key lists, Q/dO by TMA, K/V rows gathered with cp.async
-//         into 128-byte-swizzled 16 KB stages.
-//   14    MMA issuer A (TMEM owner): S^T, dP^T and dQ^T, in ring order.
-//   15    MMA issuer B: the dK^T and dV^T chunks.
+//   12-15 producers: key lists, Q/dO by TMA, K/V rows gathered with cp.async
+//         into 128-byte-swizzled 16 KB stages.  The gather rate grows with
+//         the number of issuing warps, not with the bytes in flight, hence
+//         four.  (TMA tile::gather4 moves the same rows, but at 128 bytes
+//         per row segment one issuing thread reaches only a fraction of it.)
+//   16    MMA issuer A (TMEM owner): S^T, dP^T and dQ^T, in ring order.
+//   17    MMA issuer B: the dK^T and dV^T chunks.
 // Two issuers keep the chunk stream independent of the gather ring: A runs
 // up to a tile ahead of B.  Heads are padded to N = 64 (padding heads get
 // P = 0 through LSE = +inf).  Every wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
+//
+// Scheduling.  CTAs take queries from a global counter in descending t, so
+// SMs that run slower take fewer.  For L2 locality every CTA should touch
+// the same band of keys at the same time: a query's key list is sorted, so
+// tile j of every recent query covers about the same key range.  A global
+// tile clock (tiles gathered so far / number of CTAs) names the current
+// band, and each query starts at that tile index and wraps around.  The
+// live part of the fp32 dK/dV accumulators and of K/V then stays small
+// without any grid-wide barrier.
 #include "attn_common.cuh"
 #include "dsa_internal.h"
 
@@ -47,14 +59,13 @@ constexpr int kStages = 3;             // 16 KB gather stages
 constexpr uint32_t kStageBytes = 16384;
 constexpr int kSmThreads = 128;        // softmax warps 0-3
 constexpr int kScThreads = 256;        // scatter warps 4-11
-constexpr int kProdThreads = 64;       // producer warps 12-13
-constexpr int kScWarp0 = 4, kProdWarp0 = 12, kMmaA = 14, kMmaB = 15;
-constexpr int kThreads = 512;
-constexpr int kBarEvery = 2;           // key tiles between grid-wide meetings
+constexpr int kProdThreads = 128;      // producer warps 12-15
+constexpr int kScWarp0 = 4, kProdWarp0 = 12, kMmaA = 16, kMmaB = 17;
+constexpr int kThreads = 576;
 constexpr int kMaskWords = (2048 * 4 + 3 + kTileK + 31) / 32;
-// four warps on every SM sub-partition
+// the fullest SM sub-partition holds five of the 18 warps
 constexpr int kMaxReg = (16384 / (((kThreads / 32) + 3) / 4 * 32)) & ~7;
-static_assert(kMaxReg == 128, "register budget");
+static_assert(kMaxReg == 96, "register budget");
 
 template <int D>
 struct BwdTcCfg {
@@ -65,7 +76,7 @@ struct BwdTcCfg {
   static uint32_t smem(int K_p) {
     return 1024 + 2 * kQBytes + 2 * kBufBytes + kStages * kStageBytes +
            carved(2 * (K_p + 8) * 4) + carved(2 * kTileK * 4) +
-           carved(2 * kMaskWords * 4) + 2 * carved(2 * NH * 4) + carved(32) +
+           carved(2 * kMaskWords * 4) + 2 * carved(2 * NH * 4) + carved(48) +
            carved(40 * 8);
   }
 };
@@ -111,8 +122,7 @@ __global__ void __maxnreg__(kMaxReg)
                        __nv_bfloat16* __restrict__ dq, float* __restrict__ dk_acc,
                        float* __restrict__ dv_acc, int64_t S, int H, int K_p,
                        int n_loc, float scale, int n_hblk, uint32_t* status,
-                       uint64_t timeout_ns, uint32_t* grid_ctr, int bar_every,
-                       int bar_points) {
+                       uint64_t timeout_ns, uint32_t* sched) {
   using C = BwdTcCfg<D>;
   constexpr uint32_t ID_KK = idesc_bf16(128, NH, 0, 0);  // S^T, dP^T
   constexpr uint32_t ID_MK = idesc_bf16(128, 32, 1, 0);  // dV^T, dK^T chunks
@@ -134,7 +144,7 @@ __global__ void __maxnreg__(kMaxReg)
   uint32_t* vmask = carve<uint32_t>(tail, 2 * kMaskWords);   // [2][words]
   float* lse2_s = carve<float>(tail, 2 * NH);                // [2][NH]
   float* delta_s = carve<float>(tail, 2 * NH);               // [2][NH]
-  int* misc = carve<int>(tail, 8);                 // ntok[2], npool[2], last, nadd
+  int* misc = carve<int>(tail, 12);  // ntok[2] npool[2] last nadd item[2] rot[2]
   uint64_t* bars = carve<uint64_t>(tail, 40);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
@@ -144,18 +154,22 @@ __global__ void __maxnreg__(kMaxReg)
                  sdp_free = b1 + 24, ds_full = b1 + 32, ds_free = b1 + 40,
                  p_full = b1 + 48, p_free = b1 + 56, dq_done = b1 + 64,
                  tq_empty = b1 + 72, done_a = b1 + 80, done_b = b1 + 88,
-                 sm_grp = b1 + 96, sc_grp = b1 + 104, prod_grp = b1 + 112;
-  auto chunk_full = [&](int b) { return b1 + 120u + 8u * b; };   // [4]
-  auto chunk_empty = [&](int b) { return b1 + 152u + 8u * b; };  // [4]
-  auto toks_full = [&](int b) { return b1 + 184u + 8u * b; };
-  auto toks_empty = [&](int b) { return b1 + 200u + 8u * b; };
-  // 6 ring barriers + 27 above = 33 of the 40 slots; slot 38 abort, 39 TMEM
+                 prod_grp = b1 + 96;
+  auto chunk_full = [&](int b) { return b1 + 104u + 8u * b; };   // [4]
+  auto chunk_empty = [&](int b) { return b1 + 136u + 8u * b; };  // [4]
+  auto toks_full = [&](int b) { return b1 + 168u + 8u * b; };
+  auto toks_empty = [&](int b) { return b1 + 184u + 8u * b; };
+  // 6 ring barriers + 25 above = 31 of the 40 slots; slot 38 abort, 39 TMEM
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 38);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 39);
   int* ntok = misc;        // [2]
   int* npool_s = misc + 2; // [2]
   int* s_last = misc + 4;
   int* s_nadd = misc + 5;
+  int* item_s = misc + 6;  // [2] query of the buffer (>= n_items: no more)
+  int* rot_s = misc + 8;   // [2] first tile of the query (rotation)
+  uint32_t* work_ctr = sched;     // next query to take
+  uint32_t* tile_clock = sched + 1;  // tiles gathered by all CTAs so far
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Waiter W{abort_flag, status, timeout_ns};
@@ -181,8 +195,6 @@ __global__ void __maxnreg__(kMaxReg)
     mbar_init(tq_empty, kSmThreads);
     mbar_init(done_a, 1);
     mbar_init(done_b, 1);
-    mbar_init(sm_grp, kSmThreads);
-    mbar_init(sc_grp, kScThreads);
     mbar_init(prod_grp, kProdThreads);
     for (int b = 0; b < 4; ++b) {
       mbar_init(chunk_full(b), 1);
@@ -218,17 +230,24 @@ __global__ void __maxnreg__(kMaxReg)
   };
 
   if (warp >= kProdWarp0 && warp < kMmaA) {
-    // ============================================ gather producers (64)
+    // =========================================== gather producers (128)
     const int ptid = tid - kProdWarp0 * 32;
     GroupBar G{prod_grp, 0u};
     uint32_t u = 0, nq = 0;
     int qi = 0;
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++qi) {
+    for (;; ++qi) {
       if (W.aborted()) break;
-      const int64_t t = S - 1 - item / n_hblk;
-      const int hb = (int)(item % n_hblk);
       const int buf = qi & 1;
       if (!W.wait(toks_empty(buf), ((qi >> 1) & 1) ^ 1)) break;
+      if (ptid == 0) item_s[buf] = (int)atomicAdd(work_ctr, 1u);
+      if (!G.sync(W)) break;
+      const int64_t item = item_s[buf];
+      if (item >= n_items) {  // no query left: tell the other roles
+        mbar_arrive(toks_full(buf));
+        break;
+      }
+      const int64_t t = S - 1 - item / n_hblk;
+      const int hb = (int)(item % n_hblk);
       // ---- key list of query t as pool ids + local tokens; LSE/delta rows
       const int32_t* row = idx + t * K_p;
       const int64_t nf = n_full(t);
@@ -283,6 +302,10 @@ __global__ void __maxnreg__(kMaxReg)
       if (ptid == 0) {
         ntok[buf] = n;
         npool_s[buf] = npool;
+        uint32_t clk;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(clk) : "l"(tile_clock)
+                     : "memory");
+        rot_s[buf] = ntiles > 0 ? (int)((clk / gridDim.x) % (uint32_t)ntiles) : 0;
       }
       if (!G.sync(W)) break;
       mbar_arrive(toks_full(buf));  // releases list, mask, LSE, delta, counts
@@ -301,14 +324,17 @@ __global__ void __maxnreg__(kMaxReg)
       ++nq;
       // ---- per tile: K atoms [128 key x 64 d] (S^T), V atoms (dP^T), then
       // K again in [2 x (64 key x 64 d)] stages, one per (128-d chunk, key
-      // half), for dQ^T.  A warp instruction copies 4 rows x 128 B.
+      // half), for dQ^T.  A warp instruction copies 4 rows x 128 B; empty
+      // slots are zero-filled.
       const int pw = ptid >> 5, plane = ptid & 31;
       const int rsub = plane >> 3, ch8 = plane & 7;
+      const int rot = rot_s[buf];
       bool ok = true;
       for (int j = 0; j < ntiles && ok; ++j) {
+        const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
         int32_t* tt = tile_tok + (j & 1) * kTileK;
         for (int r = ptid; r < kTileK; r += kProdThreads)
-          tt[r] = tok_of(pl, lc, npool, n, j * kTileK + r);
+          tt[r] = tok_of(pl, lc, npool, n, jr * kTileK + r);
         if (!(ok = G.sync(W))) break;
         for (int pass = 0; pass < 3 && ok; ++pass) {
           const __nv_bfloat16* src = pass == 1 ? v : k;
@@ -318,8 +344,8 @@ __global__ void __maxnreg__(kMaxReg)
             const uint32_t st = sStage + s * kStageBytes;
             if (pass < 2) {
 #pragma unroll 4
-              for (int i = 0; i < 16; ++i) {
-                const int r = pw * 64 + 4 * i + rsub;
+              for (int i = 0; i < 8; ++i) {
+                const int r = pw * 32 + 4 * i + rsub;
                 const int32_t tok = tt[r];
                 const __nv_bfloat16* sp =
                     src + (int64_t)(tok >= 0 ? tok : 0) * D + a * 64 + ch8 * 8;
@@ -330,8 +356,8 @@ __global__ void __maxnreg__(kMaxReg)
               // stage a = (dc, kh): keys kh*64 .. +63, dims dc*128 .. +127
               const int dc = a >> 1, kh = a & 1;
 #pragma unroll 4
-              for (int i = 0; i < 16; ++i) {
-                const int rr = pw * 64 + 4 * i + rsub;   // 0..127
+              for (int i = 0; i < 8; ++i) {
+                const int rr = pw * 32 + 4 * i + rsub;   // 0..127
                 const int blk = rr >> 6, r = rr & 63;    // d block, key row
                 const int32_t tok = tt[kh * 64 + r];
                 const __nv_bfloat16* sp = src + (int64_t)(tok >= 0 ? tok : 0) * D +
@@ -343,6 +369,8 @@ __global__ void __maxnreg__(kMaxReg)
             cp_async_mbar_arrive(full(s));
           }
         }
+        if (ptid == 0)
+          asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(tile_clock) : "memory");
       }
       if (!ok) break;
     }
@@ -353,9 +381,10 @@ __global__ void __maxnreg__(kMaxReg)
       uint32_t u = 0, T = 0, nq = 0;
       int qi = 0;
       bool ok = true, issued = false;
-      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
+      for (;; ++qi) {
         const int buf = qi & 1;
         if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
+        if (item_s[buf] >= n_items) break;
         const int ntiles = (ntok[buf] + kTileK - 1) / kTileK;
         mbar_arrive(toks_empty(buf));
         if (ntiles == 0) continue;
@@ -422,9 +451,10 @@ __global__ void __maxnreg__(kMaxReg)
       uint32_t T = 0, nq = 0, chunk = 0;
       int qi = 0;
       bool ok = true, issued = false;
-      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
+      for (;; ++qi) {
         const int buf = qi & 1;
         if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
+        if (item_s[buf] >= n_items) break;
         const int ntiles = (ntok[buf] + kTileK - 1) / kTileK;
         mbar_arrive(toks_empty(buf));
         if (ntiles == 0) continue;
@@ -471,12 +501,15 @@ __global__ void __maxnreg__(kMaxReg)
     uint32_t T = 0, nq = 0;
     int qi = 0;
     bool ok = true;
-    for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
-      const int64_t t = S - 1 - item / n_hblk;
-      const int hb = (int)(item % n_hblk);
+    for (;; ++qi) {
       const int buf = qi & 1;
       if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
+      const int64_t item = item_s[buf];
+      if (item >= n_items) break;
+      const int64_t t = S - 1 - item / n_hblk;
+      const int hb = (int)(item % n_hblk);
       const int n = ntok[buf];
+      const int rot = rot_s[buf];
       const uint32_t* vm = vmask + buf * kMaskWords;
       const float* l2 = lse2_s + buf * NH;
       const float* dl = delta_s + buf * NH;
@@ -490,20 +523,22 @@ __global__ void __maxnreg__(kMaxReg)
       }
       const uint32_t rowa = (uint32_t)i * 128u;  // row i of a [key x 64 h] buffer
       for (int j = 0; j < ntiles && ok; ++j, ++T) {
-        const int slot = j * kTileK + i;
+        const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
+        const int slot = jr * kTileK + i;
         const bool valid = (vm[slot >> 5] >> (slot & 31)) & 1u;
-        // dQ^T and dK^T of the previous tile have read dS
+        // dQ^T, dK^T and dV^T of the previous tile have read dS and P (by
+        // the time the softmax gets here they almost always have)
         if (!(ok = W.wait(ds_free, (T & 1u) ^ 1u))) break;
+        if (!(ok = W.wait(p_free, (T & 1u) ^ 1u))) break;
         if (!(ok = W.wait(sdp_full, T & 1u))) break;
         tc_fence_after();
-        uint32_t pb[32];
 #pragma unroll
         for (int qh = 0; qh < 4; ++qh) {  // 16 heads at a time
           uint32_t sa[16], pa[16];
           tmem_ld16(tS + lane_base + qh * 16, sa);
           tmem_ld16(tP + lane_base + qh * 16, pa);
           tmem_wait_ld();
-          uint32_t db[8];
+          uint32_t pb[8], db[8];
 #pragma unroll
           for (int e = 0; e < 16; e += 2) {
             const int h = qh * 16 + e;
@@ -511,32 +546,27 @@ __global__ void __maxnreg__(kMaxReg)
                 valid ? exp2f(__uint_as_float(sa[e]) * c2 - l2[h]) : 0.f;
             const float p1 =
                 valid ? exp2f(__uint_as_float(sa[e + 1]) * c2 - l2[h + 1]) : 0.f;
-            pb[(h >> 1)] = pack_bf16(p0, p1);
+            pb[e >> 1] = pack_bf16(p0, p1);
             db[e >> 1] = pack_bf16(scale * p0 * (__uint_as_float(pa[e]) - dl[h]),
                                    scale * p1 * (__uint_as_float(pa[e + 1]) - dl[h + 1]));
           }
 #pragma unroll
-          for (int c = 0; c < 2; ++c)
-            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                             sDS + rowa + (((uint32_t)(qh * 2 + c) ^ (uint32_t)(i & 7)) << 4)),
+          for (int c = 0; c < 2; ++c) {
+            const uint32_t off = rowa + (((uint32_t)(qh * 2 + c) ^ (uint32_t)(i & 7)) << 4);
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sDS + off),
                          "r"(db[4 * c]), "r"(db[4 * c + 1]), "r"(db[4 * c + 2]),
                          "r"(db[4 * c + 3])
                          : "memory");
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(sP + off),
+                         "r"(pb[4 * c]), "r"(pb[4 * c + 1]), "r"(pb[4 * c + 2]),
+                         "r"(pb[4 * c + 3])
+                         : "memory");
+          }
         }
         tc_fence_before();
         mbar_arrive(sdp_free);
         fence_proxy_async();
         mbar_arrive(ds_full);
-        // dV^T of the previous tile has read P
-        if (!(ok = W.wait(p_free, (T & 1u) ^ 1u))) break;
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
-                           sP + rowa + (((uint32_t)c ^ (uint32_t)(i & 7)) << 4)),
-                       "r"(pb[4 * c]), "r"(pb[4 * c + 1]), "r"(pb[4 * c + 2]),
-                       "r"(pb[4 * c + 3])
-                       : "memory");
-        fence_proxy_async();
         mbar_arrive(p_full);
       }
       if (!ok) break;
@@ -565,61 +595,24 @@ __global__ void __maxnreg__(kMaxReg)
     }
   } else {
     // ========== scatter (256 threads): TMEM chunk -> fp32 reductions
-    const int sc = tid - kScWarp0 * 32;       // 0..255
     const int quad = warp & 3, half = (warp - kScWarp0) >> 2;  // chunk parity
     const int di = quad * 32 + lane;          // d within a 128-d chunk
     const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
-    GroupBar G{sc_grp, 0u};
-    uint32_t chunk = 0, passed = 0;
+    uint32_t chunk = 0;
     int qi = 0;
     bool ok = true;
-    // Grid-wide lock-step (bar_every > 0): CTAs process generation g = their
-    // g-th query together (queries of one generation lie within gridDim.x
-    // of each other, so tile j of each covers the same band of keys) and
-    // meet every bar_every tiles; the live band of the dK/dV accumulators
-    // then stays L2-resident.  bar_points barrier points per generation for
-    // every CTA, tiles or not (the grid is co-resident).
-    auto grid_sync = [&]() -> bool {
-      if (!G.sync(W)) return false;
-      bool okg = true;
-      if (sc == 0) {
-        asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(grid_ctr) : "memory");
-        const uint32_t target = (passed + 1u) * gridDim.x;
-        const uint64_t t0 = globaltimer_ns();
-        for (;;) {
-          uint32_t cur;
-          asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(cur) : "l"(grid_ctr) : "memory");
-          if ((int32_t)(cur - target) >= 0) break;
-          if (*abort_flag) { okg = false; break; }
-          if (globaltimer_ns() - t0 > timeout_ns) {
-            W.fail(DSA_ERR_DEVICE_TIMEOUT);
-            okg = false;
-            break;
-          }
-          __nanosleep(256);
-        }
-      }
-      ++passed;
-      return G.sync(W) && okg && !W.aborted();
-    };
-    const int64_t n_gens = (n_items + gridDim.x - 1) / gridDim.x;
-    for (int64_t gen = 0; gen < n_gens && ok; ++gen) {
-      const int64_t item = blockIdx.x + gen * gridDim.x;
-      if (item >= n_items) {  // no query left here: keep the others moving
-        for (int k2 = 0; bar_every > 0 && k2 < bar_points && ok; ++k2) ok = grid_sync();
-        continue;
-      }
+    for (;; ++qi) {
       const int buf = qi & 1;
       if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
+      if (item_s[buf] >= n_items) break;
       const int n = ntok[buf];
       const int npool = npool_s[buf];
+      const int rot = rot_s[buf];
       const int32_t* pl = pools + buf * (K_p + 8);
       const int32_t* lc = pl + K_p;
       const int ntiles = (n + kTileK - 1) / kTileK;
-      const int jmax = bar_every > 0 ? bar_points * bar_every : ntiles;
-      for (int j = 0; j < jmax && ok; ++j) {
-        if (bar_every > 0 && j > 0 && j % bar_every == 0 && !(ok = grid_sync())) break;
-        if (j >= ntiles) continue;
+      for (int j = 0; j < ntiles && ok; ++j) {
+        const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
         for (int which = 0; which < 2 && ok; ++which) {
           float* acc = (which == 0 ? dk_acc : dv_acc) + di;
           // this half's chunks: q = half, half + 2, ... (chunk parity = half)
@@ -634,7 +627,7 @@ __global__ void __maxnreg__(kMaxReg)
             tc_fence_before();
             mbar_arrive(chunk_empty(b));
             float* dst = acc + dc * 128;
-            const int slot0 = j * kTileK + kq * 32;
+            const int slot0 = jr * kTileK + kq * 32;
 #pragma unroll
             for (int e4 = 0; e4 < 8; ++e4) {
               const int s4 = slot0 + 4 * e4;  // 4 keys of one pool (or locals)
@@ -655,9 +648,7 @@ __global__ void __maxnreg__(kMaxReg)
         }
       }
       if (!ok) break;
-      if (bar_every > 0 && !(ok = grid_sync())) break;  // last point of the generation
       mbar_arrive(toks_empty(buf));
-      ++qi;
     }
   }
 
@@ -697,35 +688,12 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
   const int64_t items = s.S * n_hblk;
   int64_t grid = c.num_sms;
   if (grid > items) grid = items;
-  // lock-step scatter only when the fp32 dK/dV accumulators outgrow L2
-  const int max_tiles = (4 * s.K_p + s.n_loc + kTileK - 1) / kTileK;
-  int bar_every = (double)s.S * s.D * 8.0 > 96.0 * (1 << 20) ? kBarEvery : 0;
-  if (grid < 2) bar_every = 0;
-  int bar_points = bar_every > 0 ? (max_tiles + bar_every - 1) / bar_every : 0;
-  uint32_t* grid_ctr = c.status + 32;  // zeroed by the delta kernel
-  if (bar_every == 0) {
-    attn_bwd_tc_kernel<D><<<(unsigned)grid, kThreads, smem, c.stream>>>(
-        qm, gm, k, v, lse, delta, idx, dq, dk_acc, dv_acc, s.S, s.H, s.K_p, s.n_loc,
-        s.scale, n_hblk, c.status, c.timeout_ns, grid_ctr, bar_every, bar_points);
-    return cudaGetLastError();
-  }
-  // the CTAs wait on one another: a cooperative launch guarantees that
-  // every CTA of the grid is resident at once (or refuses the launch)
-  const CUtensorMap q_arg = qm, g_arg = gm;
-  int64_t S_arg = s.S;
-  int H_arg = s.H, K_arg = s.K_p, nl_arg = s.n_loc, nh_arg = n_hblk;
-  float sc_arg = s.scale;
-  uint32_t* st_arg = c.status;
-  uint64_t to_arg = c.timeout_ns;
-  void* args[] = {(void*)&q_arg, (void*)&g_arg, (void*)&k, (void*)&v, (void*)&lse,
-                  (void*)&delta, (void*)&idx, (void*)&dq, (void*)&dk_acc,
-                  (void*)&dv_acc, (void*)&S_arg, (void*)&H_arg, (void*)&K_arg,
-                  (void*)&nl_arg, (void*)&sc_arg, (void*)&nh_arg, (void*)&st_arg,
-                  (void*)&to_arg, (void*)&grid_ctr, (void*)&bar_every,
-                  (void*)&bar_points};
-  return cudaLaunchCooperativeKernel((const void*)attn_bwd_tc_kernel<D>,
-                                     dim3((unsigned)grid), dim3(kThreads), args, smem,
-                                     c.stream);
+  // sched[0]: work counter, sched[1]: tile clock; zeroed by the delta kernel
+  uint32_t* sched = c.status + 32;
+  attn_bwd_tc_kernel<D><<<(unsigned)grid, kThreads, smem, c.stream>>>(
+      qm, gm, k, v, lse, delta, idx, dq, dk_acc, dv_acc, s.S, s.H, s.K_p, s.n_loc,
+      s.scale, n_hblk, c.status, c.timeout_ns, sched);
+  return cudaGetLastError();
 }
 
 }  // namespace
