@@ -20,10 +20,17 @@
 // (the final normalisation uses the same maximum, so the result is exact).
 //
 // Warps: 4 or 8 softmax / epilogue warps (one warpgroup per 32 heads; warp
-// w reads TMEM lane quadrant w % 4), 2 gather producers (cp.async of the
+// w reads TMEM lane quadrant w % 4), 4 gather producers (cp.async of the
 // selected K/V rows into 128-byte-swizzled stages, completion signalled on
-// an mbarrier), 1 MMA issuer and TMEM owner.  Q comes in by TMA.  Every
-// wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
+// an mbarrier; the gather rate grows with the number of issuing warps), 1
+// MMA issuer and TMEM owner.  Q comes in by TMA.  Every wait is bounded
+// (DSA_ERR_DEVICE_TIMEOUT).
+//
+// Scheduling: CTAs take queries from a global counter in descending t, and
+// each query starts at the tile index named by a global tile clock (tiles
+// gathered so far / CTAs), wrapping around.  A query's key list is sorted,
+// so tile j of every recent query covers about the same band of keys: the
+// CTAs then gather from the same L2-resident band of K/V at any time.
 #include "attn_common.cuh"
 #include "dsa_internal.h"
 
@@ -33,7 +40,7 @@ namespace {
 constexpr int kTileK = 128;            // keys per tile (MMA M)
 constexpr int kStages = 4;             // gather ring depth
 constexpr uint32_t kStageBytes = 32768;  // 128 keys x 128 dims (2 atoms)
-constexpr int kProdThreads = 64;     // 2 gather warps, 2 key rows each
+constexpr int kProdThreads = 128;    // 4 gather warps, 2 key rows each
 constexpr float kMaxSlack = 8.0f;      // log2 headroom before raising a max
 constexpr int kMaskWords = (2048 * 4 + 3 + kTileK + 31) / 32;
 
@@ -59,7 +66,7 @@ struct TcFwdCfg {
   static uint32_t smem(int K_p) {
     return 1024 + kQBytes + kPBytes + kStages * kStageBytes + carved((K_p + 4) * 4) +
            carved(2 * kTileK * 4) + carved(2 * kMaskWords * 4) + carved(4 * NH * 4) +
-           3 * carved(NH * 4) + carved(32) + carved(32 * 8);
+           3 * carved(NH * 4) + carved(48) + carved(32 * 8);
   }
 };
 
@@ -93,7 +100,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
                        int64_t S, int H, int K_p, int n_loc, float scale_log2,
                        int n_hblk, uint32_t* status,
-                       uint64_t timeout_ns) {
+                       uint64_t timeout_ns, uint32_t* sched) {
   using C = TcFwdCfg<D, NH>;
   constexpr int HPG = C::HPG;
   constexpr int kSoftmaxThreads = C::kSoftmaxThreads;
@@ -119,7 +126,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   float* m_s = carve<float>(tail, NH);                        // [NH]
   float* alpha_s = carve<float>(tail, NH);                    // [NH]
   float* inv_s = carve<float>(tail, NH);                      // [NH]
-  int* misc = carve<int>(tail, 8);  // ntok[2], last, nadd, flag[2]
+  int* misc = carve<int>(tail, 12);  // ntok[2] last nadd flag[2] item[2] rot[2]
   uint64_t* bars = carve<uint64_t>(tail, 32);
   const uint32_t bar0 = smem_u32(bars);
   auto full = [&](int s) { return bar0 + 8u * s; };
@@ -142,6 +149,10 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   int* s_last = misc + 2;
   int* s_nadd = misc + 3;
   volatile int* flags = misc + 4;
+  int* item_s = misc + 6;  // [2] query of the buffer (>= n_items: no more)
+  int* rot_s = misc + 8;   // [2] first tile of the query (rotation)
+  uint32_t* work_ctr = sched;        // next query to take
+  uint32_t* tile_clock = sched + 1;  // tiles gathered by all CTAs so far
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Waiter W{abort_flag, status, timeout_ns};
@@ -184,12 +195,19 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
     GroupBar G{prod_grp, 0u};
     uint32_t u = 0, nq = 0;
     int qi = 0;
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++qi) {
+    for (;; ++qi) {
       if (W.aborted()) break;
-      const int64_t t = S - 1 - item / n_hblk;
-      const int hb = (int)(item % n_hblk);
       const int buf = qi & 1;
       if (!W.wait(toks_empty(buf), ((qi >> 1) & 1) ^ 1)) break;
+      if (ptid == 0) item_s[buf] = (int)atomicAdd(work_ctr, 1u);
+      if (!G.sync(W)) break;
+      const int64_t item = item_s[buf];
+      if (item >= n_items) {  // no query left: tell the other roles
+        mbar_arrive(toks_full(buf));
+        break;
+      }
+      const int64_t t = S - 1 - item / n_hblk;
+      const int hb = (int)(item % n_hblk);
       // ---- key list of query t: tokens of the selected pools, then the
       // local tokens no selected pool covers; validity bits for softmax
       const int32_t* row = idx + t * K_p;
@@ -236,8 +254,15 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       const int n = npool + *s_nadd;
       const int ntiles = (n + kTileK - 1) / kTileK;
       if (!G.sync(W)) break;
-      if (ptid == 0) ntok[buf] = n;
-      mbar_arrive(toks_full(buf));  // release: list, mask and count
+      if (ptid == 0) {
+        ntok[buf] = n;
+        uint32_t clk;
+        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(clk) : "l"(tile_clock)
+                     : "memory");
+        rot_s[buf] = ntiles > 0 ? (int)((clk / gridDim.x) % (uint32_t)ntiles) : 0;
+      }
+      if (!G.sync(W)) break;
+      mbar_arrive(toks_full(buf));  // release: list, mask, count, rotation
       if (ntiles == 0) continue;
       // ---- Q rows of this head block by TMA (box {64, NH} per 64-wide d)
       if (ptid == 0 && W.wait(q_empty, (nq & 1u) ^ 1u)) {
@@ -259,14 +284,16 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       };
       // Coalesced gather: one warp instruction copies 2 key rows x 256
       // contiguous bytes (lanes 0-15 row r, lanes 16-31 row r+1; lane&15 =
-      // the 16-byte chunk).  Producer warp pw owns rows pw*64 .. pw*64+63.
+      // the 16-byte chunk).  Producer warp pw owns rows pw*32 .. pw*32+31.
       const int pw = ptid >> 5, pl = ptid & 31;
       const int sub = pl >> 4, c16 = pl & 15;     // row of the pair, chunk
       const int a16 = c16 >> 3, ch8 = c16 & 7;    // 64-dim atom, 16B chunk
+      const int rot = rot_s[buf];
       bool ok = true;
       for (int j = 0; j < ntiles && ok; ++j) {
+        const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
         int32_t* tt = tile_tok + (j & 1) * kTileK;
-        for (int r = ptid; r < kTileK; r += kProdThreads) tt[r] = tok_of(j * kTileK + r);
+        for (int r = ptid; r < kTileK; r += kProdThreads) tt[r] = tok_of(jr * kTileK + r);
         if (!(ok = G.sync(W))) break;
         for (int kv = 0; kv < 2 && ok; ++kv) {
           const __nv_bfloat16* src = kv == 0 ? k : v;
@@ -275,8 +302,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
             const uint32_t st = sStage + s * kStageBytes + a16 * 16384;
 #pragma unroll 4
-            for (int i = 0; i < 32; ++i) {
-              const int r = pw * 64 + 2 * i + sub;
+            for (int i = 0; i < 16; ++i) {
+              const int r = pw * 32 + 2 * i + sub;
               const int32_t tok = tt[r];
               const __nv_bfloat16* sp =
                   src + (int64_t)(tok >= 0 ? tok : 0) * D + c * 128 + c16 * 8;
@@ -285,6 +312,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             cp_async_mbar_arrive(full(s));
           }
         }
+        if (ptid == 0)
+          asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(tile_clock) : "memory");
       }
       if (!ok) break;
     }
@@ -295,9 +324,10 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       uint32_t u = 0, ntile_all = 0, nq = 0;
       int qi = 0;
       bool issued = false, ok = true;
-      for (int64_t item = blockIdx.x; item < n_items && ok; item += gridDim.x, ++qi) {
+      for (;; ++qi) {
         const int buf = qi & 1;
         if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
+        if (item_s[buf] >= n_items) break;
         const int n = ntok[buf];
         const int ntiles = (n + kTileK - 1) / kTileK;
         if (ntiles == 0) continue;
@@ -369,13 +399,16 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
     // address pieces of P^T element (h, key i), K-major 128-byte rows
     const uint32_t p_off = (uint32_t)(i >> 6) * (NH * 128) + (uint32_t)(i & 7) * 2;
     const uint32_t p_chunk = (uint32_t)((i & 63) >> 3);
-    for (int64_t item = blockIdx.x; item < n_items; item += gridDim.x, ++qi) {
+    for (;; ++qi) {
+      const int buf = qi & 1;
+      if (!W.wait(toks_full(buf), (qi >> 1) & 1)) break;
+      const int64_t item = item_s[buf];
+      if (item >= n_items) break;
       const int64_t t = S - 1 - item / n_hblk;
       const int hb = (int)(item % n_hblk);
       const int hcount = min(NH, H - hb * 64);
-      const int buf = qi & 1;
-      if (!W.wait(toks_full(buf), (qi >> 1) & 1)) break;
       const int n = ntok[buf];
+      const int rot = rot_s[buf];
       const uint32_t* vm = vmask + buf * kMaskWords;
       const int ntiles = (n + kTileK - 1) / kTileK;
       __nv_bfloat16* orow = o + (t * H + hb * 64) * (int64_t)D;
@@ -387,31 +420,35 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         continue;
       }
       if (tid < NH) m_s[tid] = -INFINITY;
-      float l[HPG], mr[HPG];  // row-sum partials and the running maxima
+      // row-sum partials; the running maxima are m_s[] (shared, the same
+      // for every thread of a head)
+      float l[HPG];
 #pragma unroll
-      for (int h = 0; h < HPG; ++h) {
-        l[h] = 0.f;
-        mr[h] = -INFINITY;
-      }
+      for (int h = 0; h < HPG; ++h) l[h] = 0.f;
       bool ok = true;
       for (int j = 0; j < ntiles; ++j, ++ntile_all) {
         if (!(ok = W.wait(s_full, ntile_all & 1u))) break;
         tc_fence_after();
-        const int slot = j * kTileK + i;
+        const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
+        const int slot = jr * kTileK + i;
         const bool valid = (vm[slot >> 5] >> (slot & 31)) & 1u;
         // does any score beat its running max by more than 2^8?  (always
-        // true on the first tile; rare afterwards).  S^T is read from TMEM
-        // in groups of 16 columns to keep few scores live.
-        bool need = false;
+        // true on the first tile, which also avoids reading m_s before its
+        // reset is visible; rare afterwards).  S^T is read from TMEM in
+        // groups of 16 columns to keep few scores live.
+        bool need = j == 0;
+        if (j > 0) {
 #pragma unroll
-        for (int h0 = 0; h0 < HPG; h0 += 16) {
-          uint32_t r[16];
-          tmem_ld16(tS + lane_base + h0g + h0, r);
-          tmem_wait_ld();
+          for (int h0 = 0; h0 < HPG; h0 += 16) {
+            uint32_t r[16];
+            tmem_ld16(tS + lane_base + h0g + h0, r);
+            tmem_wait_ld();
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float x = valid ? __uint_as_float(r[e]) * scale_log2 : -INFINITY;
-            need |= x > mr[h0 + e] + kMaxSlack || (mr[h0 + e] == -INFINITY && x > mr[h0 + e]);
+            for (int e = 0; e < 16; ++e) {
+              const float x = valid ? __uint_as_float(r[e]) * scale_log2 : -INFINITY;
+              const float m = m_s[h0g + h0 + e];
+              need |= x > m + kMaxSlack || (m == -INFINITY && x > m);
+            }
           }
         }
         if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr((int*)&flags[j & 1], 1);
@@ -447,7 +484,6 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
 #pragma unroll
           for (int h = 0; h < HPG; ++h) {
             const float a = alpha_s[h0g + h];
-            mr[h] = m_s[h0g + h];
             l[h] *= a;
             rescale |= a != 1.f;
           }
@@ -481,7 +517,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
           for (int e = 0; e < 16; ++e) {
             const int h = h0 + e, hh = h0g + h;
             const float x = valid ? __uint_as_float(r[e]) * scale_log2 : -INFINITY;
-            const float p = exp2f(x - (mr[h] == -INFINITY ? 0.f : mr[h]));
+            const float m = m_s[hh];
+            const float p = exp2f(x - (m == -INFINITY ? 0.f : m));
             l[h] += p;
             const uint32_t addr = sP + p_off + (uint32_t)hh * 128u +
                                   ((p_chunk ^ (uint32_t)(hh & 7)) << 4);
@@ -572,9 +609,13 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
   const int64_t items = s.S * n_hblk;
   int64_t grid = c.num_sms;
   if (grid > items) grid = items;
+  // sched[0]: work counter, sched[1]: tile clock (workspace header words)
+  uint32_t* sched = c.status + 32;
+  e = cudaMemsetAsync(sched, 0, 2 * sizeof(uint32_t), c.stream);
+  if (e != cudaSuccess) return e;
   attn_fwd_tc_kernel<D, NH><<<(unsigned)grid, C::kThreads, smem, c.stream>>>(
       qm, k, v, idx, o, lse, s.S, s.H, s.K_p, s.n_loc, s.scale * kLog2e, n_hblk,
-      c.status, c.timeout_ns);
+      c.status, c.timeout_ns, sched);
   return cudaGetLastError();
 }
 
