@@ -13,12 +13,16 @@
 //   N = 256 columns    -> (query, head) pairs, 256/H_I queries x H_I heads;
 //                         B = q_idx rows [256 x D_I], K-major
 //   K = D_I            -> D_I/16 tcgen05.mma (kind::f16, bf16 -> fp32)
-// Each epilogue thread owns one pool (one TMEM lane) and reads the H_I
-// columns of each query: ReLU, times w[t,h], summed over heads in fp32, then
-// one coalesced store per query.  No cross-lane traffic.
+// Each epilogue thread owns one pool (one TMEM lane) and half of the tile's
+// columns: ReLU, times w[t,h], summed over heads in fp32 (four independent
+// partial sums, so the adds do not wait on one another), then one coalesced
+// store per query.  No cross-lane traffic.
 //
-// Warp roles (192 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warps 2-5 epilogue.  A tiles stream through a 4-stage TMA ring;
+// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocator and
+// MMA issuer, warps 2-9 epilogue (two per TMEM lane quadrant, one per
+// column half).  The epilogue's ALU work per tile is about half the MMA
+// time only when two warps per SM sub-partition hide each other's
+// latencies.  A tiles stream through a 4-stage TMA ring;
 // the B tile stays resident while consecutive tiles share it; accumulators
 // are double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
 // overlaps the MMAs of the next.
@@ -30,7 +34,8 @@ namespace {
 
 constexpr int kBM = 128;  // pools per tile
 constexpr int kBN = 256;  // (query, head) columns per tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kEpiWarps = 8;
 
 template <int DI>
 struct IdxCfg {
@@ -102,7 +107,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(b_empty, 1);
     for (int a = 0; a < 2; ++a) {
       mbar_init(acc_full(a), 1);
-      mbar_init(acc_empty(a), 4);
+      mbar_init(acc_empty(a), kEpiWarps);
     }
     mbar_init(done_bar, 1);
     *abort_flag = 0u;
@@ -196,18 +201,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else {
     // --------------------------------------------------------- epilogue
-    const int quad = warp & 3;
-    const int etid = threadIdx.x - 64;  // 0..127
+    const int quad = warp & 3;                // TMEM lane quadrant
+    const int half = (warp - 2) >> 2;         // columns half*128 .. +127
+    const int etid = threadIdx.x - 64;        // 0..255
     int64_t cur_nt = -1, local = 0;
     for (int64_t item = beg; item < end; ++item) {
       const int64_t nt = item / n_ptiles, pt = item - nt * n_ptiles;
       if (nt != cur_nt) {
-        named_bar_sync(1, 128);
-        for (int j = etid; j < kBN; j += 128) {
+        named_bar_sync(1, 32 * kEpiWarps);
+        for (int j = etid; j < kBN; j += 32 * kEpiWarps) {
           const int64_t qrow = nt * QT + j / HI;
           w_s[j] = qrow < rows ? __ldg(w + (t0 + qrow) * HI + (j % HI)) : 0.f;
         }
-        named_bar_sync(1, 128);
+        named_bar_sync(1, 32 * kEpiWarps);
         cur_nt = nt;
       }
       const int a = (int)(local & 1);
@@ -216,23 +222,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_after();
       const int64_t p = pt * kBM + quad * 32 + lane;
       const bool p_ok = p < p_lim;
-      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(a * kBN);
-      float acc = 0.f;
+      const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) +
+                             (uint32_t)(a * kBN + half * (kBN / 2));
+      float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int c = 0; c < kBN / 32; ++c) {
+      for (int c = 0; c < kBN / 64; ++c) {
         uint32_t r0[16], r1[16];
         tmem_ld16(taddr + c * 32, r0);
         tmem_ld16(taddr + c * 32 + 16, r1);
         tmem_wait_ld();
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          const int col = c * 32 + j;
+          const int col = half * (kBN / 2) + c * 32 + j;
           const float x = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
-          acc = fmaf(w_s[col], fmaxf(x, 0.f), acc);
+          acc[j & 3] = fmaf(w_s[col], fmaxf(x, 0.f), acc[j & 3]);
           if (col % HI == HI - 1) {
             const int64_t qrow = nt * QT + col / HI;
-            if (p_ok && qrow < rows) scores[qrow * ld + p] = acc;
-            acc = 0.f;
+            if (p_ok && qrow < rows)
+              scores[qrow * ld + p] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
           }
         }
       }
