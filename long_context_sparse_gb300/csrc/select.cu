@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     topk_rows_kernel(const float* __restrict__ scores, int64_t ld, int64_t row0,
                      int64_t rows, int K_p, int32_t* __restrict__ out,
                      int cache_cap) {
-  extern __shared__ uint32_t cache[];
+  extern __shared__ __align__(16) uint32_t cache[];
   __shared__ __align__(16) uint32_t hist[kBins];
   __shared__ uint32_t wcnt[2][kTopkWarps];
   __shared__ uint32_t sel_digit, sel_above;
@@ -126,6 +126,11 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
       continue;
     }
     const bool cached = n <= cache_cap;
+    // 16-byte rows (the library's own score chunks always are) are read as
+    // float4, four loads in flight per thread, so the first pass does not
+    // wait on one L2 round trip per element
+    const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
+    const int64_t n4 = vec ? n / 4 : 0;
 
     // ---- radix select of the K_p-th largest key: digits of 11, 11, 10 bits
     uint32_t prefix = 0u, pmask = 0u, kk = (uint32_t)K_p;
@@ -137,14 +142,58 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
       __syncthreads();
       if (pass == 0) {
         // first touch of the row: load, map, cache, count
-        for (int64_t i = tid; i < n; i += kTopkThreads) {
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        for (int64_t b = tid; b < n4; b += 4 * kTopkThreads) {
+          float4 x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int64_t j = b + u * kTopkThreads;
+            x[u] = j < n4 ? __ldg(row4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int64_t j = b + u * kTopkThreads;
+            if (j < n4) {
+              const uint32_t k4[4] = {order_key(x[u].x), order_key(x[u].y),
+                                      order_key(x[u].z), order_key(x[u].w)};
+              if (cached)
+                *reinterpret_cast<uint4*>(cache + 4 * j) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) atomicAdd(&hist[k4[e] >> 21], 1u);
+            }
+          }
+        }
+        for (int64_t i = 4 * n4 + tid; i < n; i += kTopkThreads) {
           const uint32_t key = order_key(__ldg(row + i));
           if (cached) cache[i] = key;
           atomicAdd(&hist[key >> 21], 1u);
         }
-      } else {
+      } else if (cached) {
         for (int64_t i = tid; i < n; i += kTopkThreads) {
-          const uint32_t key = cached ? cache[i] : order_key(__ldg(row + i));
+          const uint32_t key = cache[i];
+          if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
+        }
+      } else {
+        const float4* row4 = reinterpret_cast<const float4*>(row);
+        for (int64_t b = tid; b < n4; b += 4 * kTopkThreads) {
+          float4 x[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int64_t j = b + u * kTopkThreads;
+            x[u] = j < n4 ? __ldg(row4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            if (b + u * kTopkThreads >= n4) continue;
+            const uint32_t k4[4] = {order_key(x[u].x), order_key(x[u].y),
+                                    order_key(x[u].z), order_key(x[u].w)};
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              if ((k4[e] & pmask) == prefix) atomicAdd(&hist[(k4[e] >> shift) & dmask], 1u);
+          }
+        }
+        for (int64_t i = 4 * n4 + tid; i < n; i += kTopkThreads) {
+          const uint32_t key = order_key(__ldg(row + i));
           if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
         }
       }
