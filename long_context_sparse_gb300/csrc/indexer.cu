@@ -15,8 +15,10 @@
 //   K = D_I            -> D_I/16 tcgen05.mma (kind::f16, bf16 -> fp32)
 // Each epilogue thread owns one pool (one TMEM lane) and half of the tile's
 // columns: ReLU, times w[t,h], summed over heads in fp32 (four independent
-// partial sums, so the adds do not wait on one another), then one coalesced
-// store per query.  No cross-lane traffic.
+// partial sums, packed fp32x2 FMAs), then one coalesced store per query.
+// No cross-lane traffic; the 128 weights of a thread's columns stay in
+// registers for all tiles of an N tile (read from shared memory per tile
+// they took as much shared-memory bandwidth as the MMA operands).
 //
 // Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocator and
 // MMA issuer, warps 2-9 epilogue (two per TMEM lane quadrant, one per
@@ -43,8 +45,7 @@ struct IdxCfg {
   static constexpr int kStages = DI == 64 ? 8 : 4;
   static constexpr uint32_t kABytes = kBM * DI * 2;  // one pool tile
   static constexpr uint32_t kBBytes = kBN * DI * 2;  // one query tile
-  static constexpr uint32_t kSmem =
-      kBBytes + kStages * kABytes + kBN * 4 + 256 + 1024;
+  static constexpr uint32_t kSmem = kBBytes + kStages * kABytes + 256 + 1024;
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
@@ -54,6 +55,19 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
     if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
   return true;
+}
+
+// (a0, a1) += (w0, w1) * (x0, x1) with one packed fp32 FMA (each lane of
+// the pair rounds exactly like fmaf).
+__device__ __forceinline__ void fma2(float& a0, float& a1, float w0, float w1,
+                                     float x0, float x1) {
+  asm("{\n\t.reg .b64 ww, xx, aa;\n\t"
+      "mov.b64 ww, {%2, %3};\n\tmov.b64 xx, {%4, %5};\n\t"
+      "mov.b64 aa, {%0, %1};\n\t"
+      "fma.rn.f32x2 aa, ww, xx, aa;\n\t"
+      "mov.b64 {%0, %1}, aa;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
@@ -78,8 +92,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* gbase = smem_raw + (base - raw);
   const uint32_t sB = base;
   const uint32_t sA = base + C::kBBytes;
-  float* w_s = reinterpret_cast<float*>(gbase + C::kBBytes + C::kStages * C::kABytes);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(w_s + kBN);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBBytes + C::kStages * C::kABytes);
   // barrier slots
   const uint32_t bar0 = smem_u32(bars);
   auto a_full = [&](int s) { return bar0 + 8u * s; };
@@ -203,17 +216,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     // --------------------------------------------------------- epilogue
     const int quad = warp & 3;                // TMEM lane quadrant
     const int half = (warp - 2) >> 2;         // columns half*128 .. +127
-    const int etid = threadIdx.x - 64;        // 0..255
     int64_t cur_nt = -1, local = 0;
+    float wr[kBN / 2];  // weights of this half's columns (all lanes alike)
     for (int64_t item = beg; item < end; ++item) {
       const int64_t nt = item / n_ptiles, pt = item - nt * n_ptiles;
       if (nt != cur_nt) {
-        named_bar_sync(1, 32 * kEpiWarps);
-        for (int j = etid; j < kBN; j += 32 * kEpiWarps) {
-          const int64_t qrow = nt * QT + j / HI;
-          w_s[j] = qrow < rows ? __ldg(w + (t0 + qrow) * HI + (j % HI)) : 0.f;
+#pragma unroll
+        for (int j = 0; j < kBN / 2; ++j) {
+          const int col = half * (kBN / 2) + j;
+          const int64_t qrow = nt * QT + col / HI;
+          wr[j] = qrow < rows ? __ldg(w + (t0 + qrow) * HI + (col % HI)) : 0.f;
         }
-        named_bar_sync(1, 32 * kEpiWarps);
         cur_nt = nt;
       }
       const int a = (int)(local & 1);
@@ -224,6 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool p_ok = p < p_lim;
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) +
                              (uint32_t)(a * kBN + half * (kBN / 2));
+      // four partial sums (two packed pairs) per query
       float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int c = 0; c < kBN / 64; ++c) {
@@ -232,11 +246,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld16(taddr + c * 32 + 16, r1);
         tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
+        for (int j = 0; j < 32; j += 2) {
           const int col = half * (kBN / 2) + c * 32 + j;
-          const float x = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
-          acc[j & 3] = fmaf(w_s[col], fmaxf(x, 0.f), acc[j & 3]);
-          if (col % HI == HI - 1) {
+          const float x0 = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
+          const float x1 = __uint_as_float(j < 16 ? r0[j + 1] : r1[j - 15]);
+          const int pr = (j >> 1) & 1;
+          fma2(acc[2 * pr], acc[2 * pr + 1], wr[c * 32 + j], wr[c * 32 + j + 1],
+               fmaxf(x0, 0.f), fmaxf(x1, 0.f));
+          if (HI == 1) {  // two queries in the pair
+            const int64_t q0 = nt * QT + col;
+            if (p_ok && q0 < rows) scores[q0 * ld + p] = acc[2 * pr];
+            if (p_ok && q0 + 1 < rows) scores[(q0 + 1) * ld + p] = acc[2 * pr + 1];
+            acc[2 * pr] = acc[2 * pr + 1] = 0.f;
+          } else if ((col + 1) % HI == HI - 1) {
             const int64_t qrow = nt * QT + col / HI;
             if (p_ok && qrow < rows)
               scores[qrow * ld + p] = (acc[0] + acc[1]) + (acc[2] + acc[3]);

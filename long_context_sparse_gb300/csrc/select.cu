@@ -70,11 +70,14 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // Digit d of the highest bins that holds the kk-th largest key; *above =
-// number of keys in higher bins.  Warp 0 only; lane l owns 64 bins.
+// number of keys in higher bins.  Warp 0 only: lane l first sums the 64
+// bins kBins-64(l+1) .. kBins-64l-1 (lane 0: the top 64), a warp scan finds
+// the lane whose range holds the kk-th key, then the whole warp scans that
+// range two bins per lane, highest first.
 __device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t kk,
                                            uint32_t* sel_digit, uint32_t* sel_above) {
   const int lane = threadIdx.x & 31;
-  const int base = kBins - 64 * (lane + 1);  // lane 0: the top 64 bins
+  const int base = kBins - 64 * (lane + 1);
   uint32_t s = 0u;
 #pragma unroll
   for (int j = 0; j < 64; j += 4) {
@@ -87,17 +90,28 @@ __device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t kk,
     const uint32_t x = __shfl_up_sync(0xffffffffu, incl, d);
     if (lane >= d) incl += x;
   }
-  const uint32_t excl = incl - s;
-  if (excl < kk && kk <= incl) {
-    uint32_t acc = excl;
-    for (int j = 63; j >= 0; --j) {
-      const uint32_t c = hist[base + j];
-      if (acc + c >= kk) {
-        *sel_digit = (uint32_t)(base + j);
-        *sel_above = acc;
-        break;
-      }
-      acc += c;
+  const uint32_t hit = __ballot_sync(0xffffffffu, incl - s < kk && kk <= incl);
+  const int tl = __ffs(hit) - 1;  // exactly one lane (kk <= total count)
+  const uint32_t excl_tl = __shfl_sync(0xffffffffu, incl - s, tl);
+  // lane l takes bins top - 2l and top - 2l - 1 of lane tl's range
+  const int top = kBins - 64 * tl - 1;
+  const uint32_t c0 = hist[top - 2 * lane], c1 = hist[top - 2 * lane - 1];
+  const uint32_t pair = c0 + c1;
+  uint32_t pin = pair;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const uint32_t x = __shfl_up_sync(0xffffffffu, pin, d);
+    if (lane >= d) pin += x;
+  }
+  const uint32_t before = excl_tl + pin - pair;  // keys in bins above this pair
+  const uint32_t hit2 = __ballot_sync(0xffffffffu, before < kk && kk <= before + pair);
+  if (lane == __ffs(hit2) - 1) {
+    if (before + c0 >= kk) {
+      *sel_digit = (uint32_t)(top - 2 * lane);
+      *sel_above = before;
+    } else {
+      *sel_digit = (uint32_t)(top - 2 * lane - 1);
+      *sel_above = before + c0;
     }
   }
 }
@@ -143,7 +157,9 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
       if (pass == 0) {
         // first touch of the row: load, map, cache, count
         const float4* row4 = reinterpret_cast<const float4*>(row);
-        for (int64_t b = tid; b < n4; b += 4 * kTopkThreads) {
+        const int64_t nb = (n4 + 4 * kTopkThreads - 1) / (4 * kTopkThreads);
+        for (int64_t bi = 0; bi < nb; ++bi) {
+          const int64_t b = bi * 4 * kTopkThreads + tid;
           float4 x[4];
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
@@ -153,11 +169,12 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
             const int64_t j = b + u * kTopkThreads;
-            if (j < n4) {
-              const uint32_t k4[4] = {order_key(x[u].x), order_key(x[u].y),
-                                      order_key(x[u].z), order_key(x[u].w)};
-              if (cached)
-                *reinterpret_cast<uint4*>(cache + 4 * j) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+            const bool in = j < n4;
+            const uint32_t k4[4] = {order_key(x[u].x), order_key(x[u].y),
+                                    order_key(x[u].z), order_key(x[u].w)};
+            if (cached && in)
+              *reinterpret_cast<uint4*>(cache + 4 * j) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
+            if (in) {
 #pragma unroll
               for (int e = 0; e < 4; ++e) atomicAdd(&hist[k4[e] >> 21], 1u);
             }
@@ -206,19 +223,45 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     }
     // prefix = key of the K_p-th best; take every key above it and the kk
     // lowest-index keys equal to it, in index order.  Each warp owns one
-    // contiguous segment: count, one block-wide exclusive scan, write.
+    // contiguous segment of whole 128-key blocks (lane l: keys 4l .. 4l+3
+    // of a block): count, one block-wide exclusive scan, then write with a
+    // warp scan per block.
     const uint32_t T = prefix;
-    const int64_t seg = ((n + kTopkWarps - 1) / kTopkWarps + 31) & ~int64_t(31);
-    const int64_t b0 = warp * seg;
-    const int64_t b1 = b0 + seg < n ? b0 + seg : n;
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    auto keys4 = [&](int64_t i, int64_t lim, uint32_t (&kq)[4]) {
+      if (i + 3 < lim && (cached || vec)) {
+        if (cached) {
+          const uint4 c4 = *reinterpret_cast<const uint4*>(cache + i);
+          kq[0] = c4.x; kq[1] = c4.y; kq[2] = c4.z; kq[3] = c4.w;
+        } else {
+          const float4 f4 = __ldg(row4 + (i >> 2));
+          kq[0] = order_key(f4.x); kq[1] = order_key(f4.y);
+          kq[2] = order_key(f4.z); kq[3] = order_key(f4.w);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          kq[e] = i + e < lim ? (cached ? cache[i + e] : order_key(__ldg(row + i + e))) : 0u;
+      }
+    };
+    const int64_t nblk = (n + 127) / 128;
+    const int64_t bpw = (nblk + kTopkWarps - 1) / kTopkWarps;
+    const int64_t b0 = warp * bpw * 128;
+    const int64_t b1 = b0 + bpw * 128 < n ? b0 + bpw * 128 : n;
     uint32_t cg = 0u, ct = 0u;
-    for (int64_t i0 = b0; i0 < b1; i0 += 32) {
-      const int64_t i = i0 + lane;
-      uint32_t key = 0u;
-      if (i < b1) key = cached ? cache[i] : order_key(__ldg(row + i));
-      cg += __popc(__ballot_sync(0xffffffffu, i < b1 && key > T));
-      ct += __popc(__ballot_sync(0xffffffffu, i < b1 && key == T));
+    for (int64_t i0 = b0; i0 < b1; i0 += 128) {
+      const int64_t i = i0 + 4 * lane;
+      uint32_t kq[4];
+      keys4(i, b1, kq);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool in = i + e < b1;
+        cg += in && kq[e] > T;
+        ct += in && kq[e] == T;
+      }
     }
+    cg = __reduce_add_sync(0xffffffffu, cg);
+    ct = __reduce_add_sync(0xffffffffu, ct);
     if (lane == 0) {
       wcnt[0][warp] = cg;
       wcnt[1][warp] = ct;
@@ -232,23 +275,46 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
         t_base += wcnt[1][w];
       }
     }
-    for (int64_t i0 = b0; i0 < b1; i0 += 32) {
+    for (int64_t i0 = b0; i0 < b1; i0 += 128) {
       if (t_base >= kk && g_base + kk >= (uint32_t)K_p) break;  // warp-uniform
-      const int64_t i = i0 + lane;
-      uint32_t key = 0u;
-      if (i < b1) key = cached ? cache[i] : order_key(__ldg(row + i));
-      const bool gt = i < b1 && key > T;
-      const bool tie = i < b1 && key == T;
-      const uint32_t bg = __ballot_sync(0xffffffffu, gt);
-      const uint32_t bt = __ballot_sync(0xffffffffu, tie);
-      const uint32_t g_before = g_base + __popc(bg & lane_lt);
-      const uint32_t t_before = t_base + __popc(bt & lane_lt);
-      // (positions are < K_p by construction; the guard keeps a corrupted
-      // row from writing into its neighbour)
-      const uint32_t pos = gt ? g_before + min(t_before, kk) : g_before + t_before;
-      if ((gt || (tie && t_before < kk)) && pos < (uint32_t)K_p) o[pos] = (int32_t)i;
-      g_base += __popc(bg);
-      t_base += __popc(bt);
+      const int64_t i = i0 + 4 * lane;
+      uint32_t kq[4];
+      keys4(i, b1, kq);
+      uint32_t gl = 0u, tl = 0u;
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool in = i + e < b1;
+        gl += in && kq[e] > T;
+        tl += in && kq[e] == T;
+      }
+      // (above, ties) counts packed as hi/lo 16 bits: at most 128 each
+      const uint32_t v = (gl << 16) | tl;
+      uint32_t incl = v;
+#pragma unroll
+      for (int d = 1; d < 32; d <<= 1) {
+        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, d);
+        if (lane >= d) incl += x;
+      }
+      const uint32_t excl = incl - v;
+      uint32_t g_before = g_base + (excl >> 16), t_before = t_base + (excl & 0xFFFFu);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        if (i + e >= b1) break;
+        // (positions are < K_p by construction; the guard keeps a corrupted
+        // row from writing into its neighbour)
+        if (kq[e] > T) {
+          const uint32_t pos = g_before + min(t_before, kk);
+          if (pos < (uint32_t)K_p) o[pos] = (int32_t)(i + e);
+          ++g_before;
+        } else if (kq[e] == T) {
+          if (t_before < kk && g_before + t_before < (uint32_t)K_p)
+            o[g_before + t_before] = (int32_t)(i + e);
+          ++t_before;
+        }
+      }
+      const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
+      g_base += tot >> 16;
+      t_base += tot & 0xFFFFu;
     }
     __syncthreads();
   }
