@@ -12,10 +12,14 @@
 //   S^T[key, h]   = K_tile[key, :] . Q[h, :]        M=128 keys, N=heads, K=D
 //   O^T[dv, h]   += V_tile[:, dv]^T . P^T[key, h]    M=128 dv,   N=heads,
 //                                                    K=128 keys (per 128 dv)
-// S^T and O^T live in TMEM (fp32).  Each softmax thread owns one key (one
+// S^T (double-buffered) and O^T live in TMEM (fp32).  The gather runs one
+// tile ahead for K: K(j+1) is fetched before V(j), so S^T of the next tile
+// is computed while the softmax of this one runs, and the tensor core does
+// not wait for it.  Each softmax thread owns one key (one
 // TMEM lane): it reads its row of S^T, column maxima are taken across the
-// 128 lanes, and it writes its column of P (bf16) into shared memory as the
-// K-major B operand of the second product.  A running maximum is only
+// 128 lanes, and it writes P (bf16) into shared memory as the B operand of
+// the second product: with 64 heads as a row of 64 heads per key (16-byte
+// stores, MN-major operand), with fewer as a row of 128 keys per head.  A running maximum is only
 // raised when a tile beats it by more than 2^8, so O^T is rarely rescaled
 // (the final normalisation uses the same maximum, so the result is exact).
 //
@@ -60,12 +64,13 @@ struct TcFwdCfg {
   static constexpr int kChunks = D / 128;  // 128-wide d slices
   static constexpr uint32_t kQBytes = NH * D * 2;
   static constexpr uint32_t kPBytes = NH * kTileK * 2;
-  static constexpr uint32_t kTmemCols = NH + kChunks * NH <= 256 ? 256 : 512;
+  static constexpr uint32_t kTmemCols = 2 * NH + kChunks * NH <= 256 ? 256 : 512;
+  static constexpr bool kPRows = NH == 64;  // P as [key][64 heads] rows
   // dynamic shared memory for a key list of `cap` entries
   // dynamic shared memory: the selected pool ids (K_p) + 4 local tokens
   static uint32_t smem(int K_p) {
     return 1024 + kQBytes + kPBytes + kStages * kStageBytes + carved((K_p + 4) * 4) +
-           carved(2 * kTileK * 4) + carved(2 * kMaskWords * 4) + carved(4 * NH * 4) +
+           carved(3 * kTileK * 4) + carved(2 * kMaskWords * 4) + carved(4 * NH * 4) +
            3 * carved(NH * 4) + carved(48) + carved(32 * 8);
   }
 };
@@ -105,7 +110,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   constexpr int HPG = C::HPG;
   constexpr int kSoftmaxThreads = C::kSoftmaxThreads;
   constexpr uint32_t IDESC_S = idesc_bf16(128, NH, 0, 0);  // K-major A and B
-  constexpr uint32_t IDESC_O = idesc_bf16(128, NH, 1, 0);  // MN-major A
+  constexpr uint32_t IDESC_O = idesc_bf16(128, NH, 1, C::kPRows ? 1 : 0);  // MN-major A
 
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -120,7 +125,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   uint8_t* tail = gb + C::kQBytes + C::kPBytes + kStages * kStageBytes;
   int32_t* pools = carve<int32_t>(tail, K_p + 4);
   int32_t* locs = pools + K_p;
-  int32_t* tile_tok = carve<int32_t>(tail, 2 * kTileK);       // [2][128]
+  int32_t* tile_tok = carve<int32_t>(tail, 3 * kTileK);       // [3][128]
   uint32_t* vmask = carve<uint32_t>(tail, 2 * kMaskWords);    // [2][words]
   float* red = carve<float>(tail, 4 * NH);                    // [4][NH]
   float* m_s = carve<float>(tail, NH);                        // [NH]
@@ -133,18 +138,20 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   auto empty = [&](int s) { return bar0 + 8u * (kStages + s); };
   const uint32_t q_full = bar0 + 8u * (2 * kStages);
   const uint32_t q_empty = q_full + 8u;
-  const uint32_t s_full = q_full + 16u;
-  const uint32_t p_full = q_full + 24u;
-  const uint32_t pv_done = q_full + 32u;
-  const uint32_t o_empty = q_full + 40u;
-  const uint32_t done_bar = q_full + 48u;
-  auto toks_full = [&](int b) { return q_full + 56u + 8u * b; };
-  auto toks_empty = [&](int b) { return q_full + 72u + 8u * b; };
-  const uint32_t sm_grp = q_full + 88u;    // softmax group barrier
-  const uint32_t prod_grp = q_full + 96u;  // producer group barrier
+  const uint32_t p_full = q_full + 16u;
+  const uint32_t pv_done = q_full + 24u;
+  const uint32_t o_empty = q_full + 32u;
+  const uint32_t done_bar = q_full + 40u;
+  auto toks_full = [&](int b) { return q_full + 48u + 8u * b; };
+  auto toks_empty = [&](int b) { return q_full + 64u + 8u * b; };
+  const uint32_t sm_grp = q_full + 80u;    // softmax group barrier
+  const uint32_t prod_grp = q_full + 88u;  // producer group barrier
+  auto s_full = [&](int b) { return q_full + 96u + 8u * b; };   // S^T buffer b ready
+  auto s_free = [&](int b) { return q_full + 112u + 8u * b; };  // S^T buffer b read
+  const uint32_t p_done = q_full + 128u;  // a PV product completed (P, O^T free)
   volatile uint32_t* abort_flag =
-      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 13);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 14);
+      reinterpret_cast<volatile uint32_t*>(bars + 2 * kStages + 17);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 18);
   int* ntok = misc;
   int* s_last = misc + 2;
   int* s_nadd = misc + 3;
@@ -165,7 +172,11 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
     }
     mbar_init(q_full, 1);
     mbar_init(q_empty, 1);
-    mbar_init(s_full, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(s_full(b), 1);
+      mbar_init(s_free(b), kSoftmaxThreads);
+    }
+    mbar_init(p_done, 1);
     mbar_init(p_full, kSoftmaxThreads);
     mbar_init(pv_done, 1);
     mbar_init(o_empty, kSoftmaxThreads);
@@ -186,8 +197,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS = tmem;       // S^T: NH columns
-  const uint32_t tO = tmem + NH;  // O^T: kChunks x NH columns
+  const uint32_t tS = tmem;           // S^T: 2 buffers x NH columns
+  const uint32_t tO = tmem + 2 * NH;  // O^T: kChunks x NH columns
 
   if (warp >= C::kProdWarp0 && warp < C::kMmaWarp) {
     // ============================================ gather producers (128)
@@ -290,13 +301,20 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       const int a16 = c16 >> 3, ch8 = c16 & 7;    // 64-dim atom, 16B chunk
       const int rot = rot_s[buf];
       bool ok = true;
-      for (int j = 0; j < ntiles && ok; ++j) {
-        const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
-        int32_t* tt = tile_tok + (j & 1) * kTileK;
-        for (int r = ptid; r < kTileK; r += kProdThreads) tt[r] = tok_of(jr * kTileK + r);
+      // order: K(0), then K(j), V(j-1) for j = 1 .. ntiles-1, then V(last);
+      // token tables rotate over three buffers (tile j is read at steps j
+      // and j+1 and rewritten at j+3, after two more group barriers)
+      for (int j = 0; j <= ntiles && ok; ++j) {
+        if (j < ntiles) {
+          const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
+          int32_t* tt = tile_tok + (j % 3) * kTileK;
+          for (int r = ptid; r < kTileK; r += kProdThreads) tt[r] = tok_of(jr * kTileK + r);
+        }
         if (!(ok = G.sync(W))) break;
         for (int kv = 0; kv < 2 && ok; ++kv) {
+          if (kv == 0 ? j == ntiles : j == 0) continue;
           const __nv_bfloat16* src = kv == 0 ? k : v;
+          const int32_t* tt = tile_tok + ((kv == 0 ? j : j - 1) % 3) * kTileK;
           for (int c = 0; c < C::kChunks; ++c, ++u) {
             const int s = (int)(u % kStages);
             if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
@@ -312,7 +330,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             cp_async_mbar_arrive(full(s));
           }
         }
-        if (ptid == 0)
+        if (ptid == 0 && j < ntiles)
           asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(tile_clock) : "memory");
       }
       if (!ok) break;
@@ -332,53 +350,71 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         const int ntiles = (n + kTileK - 1) / kTileK;
         if (ntiles == 0) continue;
         if (!(ok = W.wait(q_full, nq & 1u))) break;
-        for (int j = 0; j < ntiles && ok; ++j, ++ntile_all) {
-          // ---- S^T = K_tile Q^T (accumulated over the D/128 slices)
-          for (int c = 0; c < C::kChunks; ++c, ++u) {
-            const int s = (int)(u % kStages);
-            if (!(ok = W.wait(full(s), (u / kStages) & 1u))) break;
-            fence_proxy_async();  // cp.async (generic) -> tensor core (async)
+        // step j: S^T of tile j (if any), then O^T += V^T P^T of tile j-1
+        for (int j = 0; j <= ntiles && ok; ++j) {
+          if (j < ntiles) {
+            const uint32_t T = ntile_all + (uint32_t)j;
+            const int b = (int)(T & 1u);
+            // the softmax has read this buffer's S^T of tile T-2
+            if (!(ok = W.wait(s_free(b), ((T >> 1) & 1u) ^ 1u))) break;
             tc_fence_after();
-            const uint32_t st = sStage + s * kStageBytes;
+            // ---- S^T = K_tile Q^T (accumulated over the D/128 slices)
+            for (int c = 0; c < C::kChunks; ++c, ++u) {
+              const int s = (int)(u % kStages);
+              if (!(ok = W.wait(full(s), (u / kStages) & 1u))) break;
+              fence_proxy_async();  // cp.async (generic) -> tensor core (async)
+              tc_fence_after();
+              const uint32_t st = sStage + s * kStageBytes;
 #pragma unroll
-            for (int a = 0; a < 2; ++a)
+              for (int a = 0; a < 2; ++a)
 #pragma unroll
-              for (int kin = 0; kin < 4; ++kin) {
-                const uint64_t ad = sdesc_sw128(st + a * 16384 + kin * 32, 16, 1024);
-                const uint64_t bd =
-                    sdesc_sw128(sQ + (2 * c + a) * (NH * 128) + kin * 32, 16, 1024);
-                tc_mma(tS, ad, bd, IDESC_S, (c | a | kin) != 0 ? 1u : 0u);
-              }
-            issued = true;
-            tc_commit(empty(s));
-          }
-          if (!ok) break;
-          if (j == ntiles - 1) tc_commit(q_empty);
-          tc_commit(s_full);
-          // ---- O^T += V_tile^T P^T
-          if (!(ok = W.wait(p_full, ntile_all & 1u))) break;
-          if (j == 0 && !(ok = W.wait(o_empty, (nq & 1u) ^ 1u))) break;
-          tc_fence_after();
-          for (int c = 0; c < C::kChunks; ++c, ++u) {
-            const int s = (int)(u % kStages);
-            if (!(ok = W.wait(full(s), (u / kStages) & 1u))) break;
-            fence_proxy_async();
-            tc_fence_after();
-            const uint32_t st = sStage + s * kStageBytes;
-#pragma unroll
-            for (int ks = 0; ks < kTileK / 16; ++ks) {
-              // A = V^T [128 dv x 16 keys], MN-major: two 64-dv atoms 16 KB
-              // apart (LBO), 8-key groups 1024 B apart (SBO)
-              const uint64_t ad = sdesc_sw128(st + ks * 2048, 16384, 1024);
-              // B = P^T [NH heads x 16 keys], K-major rows of 128 keys
-              const uint64_t bd =
-                  sdesc_sw128(sP + (ks >> 2) * (NH * 128) + (ks & 3) * 32, 16, 1024);
-              tc_mma(tO + c * NH, ad, bd, IDESC_O, (j | ks) != 0 ? 1u : 0u);
+                for (int kin = 0; kin < 4; ++kin) {
+                  const uint64_t ad = sdesc_sw128(st + a * 16384 + kin * 32, 16, 1024);
+                  const uint64_t bd =
+                      sdesc_sw128(sQ + (2 * c + a) * (NH * 128) + kin * 32, 16, 1024);
+                  tc_mma(tS + b * NH, ad, bd, IDESC_S, (c | a | kin) != 0 ? 1u : 0u);
+                }
+              issued = true;
+              tc_commit(empty(s));
             }
-            tc_commit(empty(s));
+            if (!ok) break;
+            if (j == ntiles - 1) tc_commit(q_empty);
+            tc_commit(s_full(b));
           }
-          if (ok && j == ntiles - 1) tc_commit(pv_done);
+          if (j >= 1) {
+            const int jp = j - 1;
+            const uint32_t T = ntile_all + (uint32_t)jp;
+            // ---- O^T += V_tile^T P^T
+            if (!(ok = W.wait(p_full, T & 1u))) break;
+            if (jp == 0 && !(ok = W.wait(o_empty, (nq & 1u) ^ 1u))) break;
+            tc_fence_after();
+            for (int c = 0; c < C::kChunks; ++c, ++u) {
+              const int s = (int)(u % kStages);
+              if (!(ok = W.wait(full(s), (u / kStages) & 1u))) break;
+              fence_proxy_async();
+              tc_fence_after();
+              const uint32_t st = sStage + s * kStageBytes;
+#pragma unroll
+              for (int ks = 0; ks < kTileK / 16; ++ks) {
+                // A = V^T [128 dv x 16 keys], MN-major: two 64-dv atoms 16 KB
+                // apart (LBO), 8-key groups 1024 B apart (SBO)
+                const uint64_t ad = sdesc_sw128(st + ks * 2048, 16384, 1024);
+                // B = P^T [NH heads x 16 keys]: rows of 64 heads per key
+                // (MN-major) or rows of 128 keys per head (K-major)
+                const uint64_t bd =
+                    C::kPRows
+                        ? sdesc_sw128(sP + ks * 2048, 16, 1024)
+                        : sdesc_sw128(sP + (ks >> 2) * (NH * 128) + (ks & 3) * 32, 16, 1024);
+                tc_mma(tO + c * NH, ad, bd, IDESC_O, (jp | ks) != 0 ? 1u : 0u);
+              }
+              tc_commit(empty(s));
+            }
+            if (!ok) break;
+            tc_commit(p_done);
+            if (jp == ntiles - 1) tc_commit(pv_done);
+          }
         }
+        ntile_all += (uint32_t)ntiles;
         ++nq;
       }
       if (issued) {
@@ -427,7 +463,9 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       for (int h = 0; h < HPG; ++h) l[h] = 0.f;
       bool ok = true;
       for (int j = 0; j < ntiles; ++j, ++ntile_all) {
-        if (!(ok = W.wait(s_full, ntile_all & 1u))) break;
+        const int sb = (int)(ntile_all & 1u);
+        const uint32_t tSb = tS + sb * NH;
+        if (!(ok = W.wait(s_full(sb), (ntile_all >> 1) & 1u))) break;
         tc_fence_after();
         const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
         const int slot = jr * kTileK + i;
@@ -441,7 +479,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
 #pragma unroll
           for (int h0 = 0; h0 < HPG; h0 += 16) {
             uint32_t r[16];
-            tmem_ld16(tS + lane_base + h0g + h0, r);
+            tmem_ld16(tSb + lane_base + h0g + h0, r);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -454,12 +492,16 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         if (__any_sync(0xffffffffu, need) && lane == 0) atomicOr((int*)&flags[j & 1], 1);
         if (!(ok = G.sync(W))) break;
         if (tid == 0) flags[(j + 1) & 1] = 0;  // next tile's flag (read two syncs ago)
+        // the previous PV product has completed: O^T is current and P's
+        // buffer is free
+        if (ntile_all > 0 && !(ok = W.wait(p_done, (ntile_all - 1u) & 1u))) break;
+        tc_fence_after();
         if (flags[j & 1] != 0) {
           // ---- slow path: exact column maxima, raise the beaten maxima
 #pragma unroll
           for (int h0 = 0; h0 < HPG; h0 += 16) {
             uint32_t r[16];
-            tmem_ld16(tS + lane_base + h0g + h0, r);
+            tmem_ld16(tSb + lane_base + h0g + h0, r);
             tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 16; ++e) {
@@ -488,8 +530,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             rescale |= a != 1.f;
           }
           if (j > 0 && __any_sync(0xffffffffu, rescale)) {
-            // O^T columns of raised maxima (the previous PV has completed:
-            // it precedes this S^T)
+            // O^T columns of raised maxima (the previous PV has completed)
 #pragma unroll 1
             for (int c = 0; c < C::kChunks; ++c) {
 #pragma unroll
@@ -507,25 +548,46 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             tmem_wait_st();
           }
         }
-        // P = exp2(s - m) -> row sums and P^T (bf16) in shared memory
+        // P = exp2(s - m) -> row sums and P (bf16) in shared memory
+        uint32_t pk[HPG / 2];  // P of this thread's heads, bf16 pairs
 #pragma unroll
         for (int h0 = 0; h0 < HPG; h0 += 16) {
           uint32_t r[16];
-          tmem_ld16(tS + lane_base + h0g + h0, r);
+          tmem_ld16(tSb + lane_base + h0g + h0, r);
           tmem_wait_ld();
+          float pv[16];
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             const int h = h0 + e, hh = h0g + h;
             const float x = valid ? __uint_as_float(r[e]) * scale_log2 : -INFINITY;
             const float m = m_s[hh];
-            const float p = exp2f(x - (m == -INFINITY ? 0.f : m));
-            l[h] += p;
+            pv[e] = exp2f(x - (m == -INFINITY ? 0.f : m));
+            l[h] += pv[e];
+          }
+#pragma unroll
+          for (int e = 0; e < 16; e += 2) pk[(h0 + e) >> 1] = pack_bf16(pv[e], pv[e + 1]);
+        }
+        tc_fence_before();
+        mbar_arrive(s_free(sb));  // S^T of this tile fully read
+        if constexpr (C::kPRows) {
+          // row i: 64 heads = 8 chunks of 16 B, this group's 4 chunks
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint32_t ch = (uint32_t)(grp * 4 + c);
+            asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(
+                             sP + (uint32_t)i * 128u + ((ch ^ (uint32_t)(i & 7)) << 4)),
+                         "r"(pk[4 * c]), "r"(pk[4 * c + 1]), "r"(pk[4 * c + 2]),
+                         "r"(pk[4 * c + 3])
+                         : "memory");
+          }
+        } else {
+#pragma unroll
+          for (int h = 0; h < HPG; ++h) {
+            const int hh = h0g + h;
             const uint32_t addr = sP + p_off + (uint32_t)hh * 128u +
                                   ((p_chunk ^ (uint32_t)(hh & 7)) << 4);
-            const __nv_bfloat16 pb = __float2bfloat16_rn(p);
-            asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr),
-                         "h"(*reinterpret_cast<const uint16_t*>(&pb))
-                         : "memory");
+            const uint16_t b16 = (uint16_t)((h & 1) ? (pk[h >> 1] >> 16) : (pk[h >> 1] & 0xFFFFu));
+            asm volatile("st.shared.b16 [%0], %1;" ::"r"(addr), "h"(b16) : "memory");
           }
         }
         fence_proxy_async();  // P^T writes -> tensor core reads
