@@ -22,19 +22,20 @@
 // red.global.add, while the products of the next chunks and tiles proceed
 // behind them.
 //
-// Roles (18 warps):
+// Roles (20 warps):
 //   0-3   softmax: P and dS of a tile (thread = key lane), written to two
 //         separate shared buffers; the dQ epilogue of each query.
 //   4-11  scatter: TMEM chunk -> fp32 reductions (warp w reads lane quadrant
 //         w % 4); warps 4-7 drain the even chunks, 8-11 the odd ones, each
 //         half double-buffered in TMEM.
-//   12-15 producers: key lists, Q/dO by TMA, K/V rows gathered with cp.async
+//   12-17 producers: key lists, Q/dO by TMA, K/V rows gathered with cp.async
 //         into 128-byte-swizzled 16 KB stages.  The gather rate grows with
 //         the number of issuing warps, not with the bytes in flight, hence
-//         four.  (TMA tile::gather4 moves the same rows, but at 128 bytes
-//         per row segment one issuing thread reaches only a fraction of it.)
-//   16    MMA issuer A (TMEM owner): S^T, dP^T and dQ^T, in ring order.
-//   17    MMA issuer B: the dK^T and dV^T chunks.
+//         six (the register budget is the same for 18 and 20 warps).  (TMA
+//         tile::gather4 moves the same rows, but at 128 bytes per row
+//         segment one issuing thread reaches only a fraction of it.)
+//   18    MMA issuer A (TMEM owner): S^T, dP^T and dQ^T, in ring order.
+//   19    MMA issuer B: the dK^T and dV^T chunks.
 // Two issuers keep the chunk stream independent of the gather ring: A runs
 // up to a tile ahead of B.  Heads are padded to N = 64 (padding heads get
 // P = 0 through LSE = +inf).  Every wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
@@ -59,11 +60,12 @@ constexpr int kStages = 3;             // 16 KB gather stages
 constexpr uint32_t kStageBytes = 16384;
 constexpr int kSmThreads = 128;        // softmax warps 0-3
 constexpr int kScThreads = 256;        // scatter warps 4-11
-constexpr int kProdThreads = 128;      // producer warps 12-15
-constexpr int kScWarp0 = 4, kProdWarp0 = 12, kMmaA = 16, kMmaB = 17;
-constexpr int kThreads = 576;
+constexpr int kProdThreads = 192;      // producer warps 12-17
+constexpr int kProdWarps = kProdThreads / 32;
+constexpr int kScWarp0 = 4, kProdWarp0 = 12, kMmaA = 18, kMmaB = 19;
+constexpr int kThreads = 640;
 constexpr int kMaskWords = (2048 * 4 + 3 + kTileK + 31) / 32;
-// the fullest SM sub-partition holds five of the 18 warps
+// the fullest SM sub-partition holds five of the 20 warps
 constexpr int kMaxReg = (16384 / (((kThreads / 32) + 3) / 4 * 32)) & ~7;
 static_assert(kMaxReg == 96, "register budget");
 
@@ -230,7 +232,7 @@ __global__ void __maxnreg__(kMaxReg)
   };
 
   if (warp >= kProdWarp0 && warp < kMmaA) {
-    // =========================================== gather producers (128)
+    // =========================================== gather producers (192)
     const int ptid = tid - kProdWarp0 * 32;
     GroupBar G{prod_grp, 0u};
     uint32_t u = 0, nq = 0;
@@ -343,9 +345,9 @@ __global__ void __maxnreg__(kMaxReg)
             if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
             const uint32_t st = sStage + s * kStageBytes;
             if (pass < 2) {
-#pragma unroll 4
-              for (int i = 0; i < 8; ++i) {
-                const int r = pw * 32 + 4 * i + rsub;
+              // 32 four-row groups per stage, dealt round-robin to the warps
+              for (int g = pw; g < kTileK / 4; g += kProdWarps) {
+                const int r = 4 * g + rsub;
                 const int32_t tok = tt[r];
                 const __nv_bfloat16* sp =
                     src + (int64_t)(tok >= 0 ? tok : 0) * D + a * 64 + ch8 * 8;
@@ -355,9 +357,8 @@ __global__ void __maxnreg__(kMaxReg)
             } else {
               // stage a = (dc, kh): keys kh*64 .. +63, dims dc*128 .. +127
               const int dc = a >> 1, kh = a & 1;
-#pragma unroll 4
-              for (int i = 0; i < 8; ++i) {
-                const int rr = pw * 32 + 4 * i + rsub;   // 0..127
+              for (int g = pw; g < kTileK / 4; g += kProdWarps) {
+                const int rr = 4 * g + rsub;             // 0..127
                 const int blk = rr >> 6, r = rr & 63;    // d block, key row
                 const int32_t tok = tt[kh * 64 + r];
                 const __nv_bfloat16* sp = src + (int64_t)(tok >= 0 ? tok : 0) * D +

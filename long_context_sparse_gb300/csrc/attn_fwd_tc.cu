@@ -24,10 +24,11 @@
 // (the final normalisation uses the same maximum, so the result is exact).
 //
 // Warps: 4 or 8 softmax / epilogue warps (one warpgroup per 32 heads; warp
-// w reads TMEM lane quadrant w % 4), 4 gather producers (cp.async of the
+// w reads TMEM lane quadrant w % 4), 7 gather producers (cp.async of the
 // selected K/V rows into 128-byte-swizzled stages, completion signalled on
-// an mbarrier; the gather rate grows with the number of issuing warps), 1
-// MMA issuer and TMEM owner.  Q comes in by TMA.  Every wait is bounded
+// an mbarrier; the gather rate grows with the number of issuing warps, and
+// 16 warps have the same register budget as 13), 1 MMA issuer and TMEM
+// owner.  Q comes in by TMA.  Every wait is bounded
 // (DSA_ERR_DEVICE_TIMEOUT).
 //
 // Scheduling: CTAs take queries from a global counter in descending t, and
@@ -44,7 +45,8 @@ namespace {
 constexpr int kTileK = 128;            // keys per tile (MMA M)
 constexpr int kStages = 4;             // gather ring depth
 constexpr uint32_t kStageBytes = 32768;  // 128 keys x 128 dims (2 atoms)
-constexpr int kProdThreads = 128;    // 4 gather warps, 2 key rows each
+constexpr int kProdThreads = 224;    // 7 gather warps
+constexpr int kProdWarps = kProdThreads / 32;
 constexpr float kMaxSlack = 8.0f;      // log2 headroom before raising a max
 constexpr int kMaskWords = (2048 * 4 + 3 + kTileK + 31) / 32;
 
@@ -295,7 +297,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       };
       // Coalesced gather: one warp instruction copies 2 key rows x 256
       // contiguous bytes (lanes 0-15 row r, lanes 16-31 row r+1; lane&15 =
-      // the 16-byte chunk).  Producer warp pw owns rows pw*32 .. pw*32+31.
+      // the 16-byte chunk); the 64 row pairs of a stage are dealt
+      // round-robin to the producer warps.
       const int pw = ptid >> 5, pl = ptid & 31;
       const int sub = pl >> 4, c16 = pl & 15;     // row of the pair, chunk
       const int a16 = c16 >> 3, ch8 = c16 & 7;    // 64-dim atom, 16B chunk
@@ -319,9 +322,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             const int s = (int)(u % kStages);
             if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
             const uint32_t st = sStage + s * kStageBytes + a16 * 16384;
-#pragma unroll 4
-            for (int i = 0; i < 16; ++i) {
-              const int r = pw * 32 + 2 * i + sub;
+            for (int g = pw; g < kTileK / 2; g += kProdWarps) {
+              const int r = 2 * g + sub;
               const int32_t tok = tt[r];
               const __nv_bfloat16* sp =
                   src + (int64_t)(tok >= 0 ? tok : 0) * D + c * 128 + c16 * 8;
