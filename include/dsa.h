@@ -105,6 +105,20 @@ DSA_API dsa_status_t dsa_workspace_init(void* ws, size_t ws_bytes, void* stream)
 DSA_API dsa_status_t dsa_pool_keys(const dsa_config_t* cfg, const void* k_idx,
                            void* k_pool, void* stream);
 
+/* Step 1 with gated pools ("Scaling Training to 1M Token Context on
+ * GLM-5.3-Flash", section "DSA: Gather by Token Position": k-pool gate
+ * scores weight each key within its pool), read as a softmax over the
+ * pool's four gate scores, in fp32:
+ *   w_j = exp(g_j - m) / ((e_0 + e_1) + (e_2 + e_3)),  m = max_j g_j,
+ *   k_pool[p,d] = bf16_rne((w_0 k[4p,d] + w_1 k[4p+1,d])
+ *                          + (w_2 k[4p+2,d] + w_3 k[4p+3,d])).
+ * k_gate [S] fp32 (finite), 16-byte aligned.  Equal gates give the mean
+ * pooling of dsa_pool_keys.  Forward only: the pages do not say how the
+ * gates are trained. */
+DSA_API dsa_status_t dsa_pool_keys_gated(const dsa_config_t* cfg, const void* k_idx,
+                                 const float* k_gate, void* k_pool,
+                                 void* stream);
+
 /* Step 2 for one block of queries t0 .. t0+rows-1 (rows <= 4096):
  *   scores[r*ld + p] = I[t0 + r, p]  (fp32, tensor-core bf16 products,
  *   fp32 accumulation) for p < n_full(t0 + r).  Entries with p >= n_full(t)
@@ -138,6 +152,24 @@ DSA_API dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg,
                                    const void* q_idx, const void* k_idx,
                                    const float* w, int32_t* topk_idx,
                                    void* ws, size_t ws_bytes, void* stream);
+
+/* Steps 1-4 for the query rows t_begin .. t_end-1 only, with mean pooling
+ * (k_gate NULL) or gated pooling (k_gate [S] fp32, as dsa_pool_keys_gated):
+ * the share of one
+ * rank when the indexer is split by query, each rank scoring its queries
+ * against all earlier pools and the int32 selections being gathered
+ * afterwards ("Scaling Training to 1M Token Context on GLM-5.3-Flash",
+ * section "Across GPUs: Sharding").  The selection of every row is exactly
+ * the one dsa_index_scores_topk gives that row.
+ * q_idx [t_end-t_begin, H_I, D_I] bf16 and w [t_end-t_begin, H_I] fp32 hold
+ * the range's rows (row r <-> query t_begin + r); k_idx [S, D_I] bf16 holds
+ * every key -> topk_idx [t_end-t_begin, K_p] int32.  0 <= t_begin <= t_end
+ * <= S, else DSA_ERR_INVALID_ARG; an empty range does nothing.
+ * ws: DSA_WS_INDEX (pooled keys of all S tokens plus one score chunk). */
+DSA_API dsa_status_t dsa_index_scores_topk_range(
+    const dsa_config_t* cfg, const void* q_idx, const void* k_idx, const float* k_gate,
+    const float* w, int64_t t_begin, int64_t t_end, int32_t* topk_idx, void* ws,
+    size_t ws_bytes, void* stream);
 
 /* Step 5, forward.  For every query t and head h, over the key set K(t):
  *   O[t,h]   = sum_j softmax_j(scale * q[t,h] . k_j) v_j

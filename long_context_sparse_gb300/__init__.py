@@ -50,7 +50,8 @@ EXPORTS = [
     "dsa_index_scores", "dsa_topk_from_scores", "dsa_index_scores_topk",
     "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_get_device_status",
     "dsa_status_string", "dsa_abi_version", "dsa_last_cuda_error",
-    "dsa_index_scores_topk_static",
+    "dsa_index_scores_topk_static", "dsa_index_scores_topk_range",
+    "dsa_pool_keys_gated",
 ]
 
 
@@ -140,6 +141,8 @@ def _load():
                                     P],
             "dsa_get_device_status": [P, P, ctypes.POINTER(ctypes.c_uint32)],
             "dsa_index_scores_topk_static": [CP, P, P, P, P, P],
+            "dsa_index_scores_topk_range": [CP, P, P, P, P, I64, I64, P, P, SZ, P],
+            "dsa_pool_keys_gated": [CP, P, P, P, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -288,6 +291,66 @@ def index_scores_topk(cfg: Config, q_idx, k_idx, w, out=None,
                                          _ptr(ws), ws.numel(), _stream(dev)),
            "dsa_index_scores_topk")
     return out
+
+
+def index_scores_topk_range(cfg: Config, q_idx, k_idx, w, t_begin: int,
+                            t_end: int, k_gate=None, out=None,
+                            ws=None) -> torch.Tensor:
+    """Pool (mean, or gated by k_gate [S] fp32), score and select for
+    queries t_begin .. t_end-1 only (one rank's share of a query-sharded
+    indexer): q_idx [n, H_I, D_I] and w [n, H_I] hold the range's rows,
+    k_idx [S, D_I] every key; returns topk_idx [n, K_p] int32,
+    n = t_end - t_begin."""
+    S = cfg.seq_len
+    n = t_end - t_begin
+    _need(q_idx, "q_idx", torch.bfloat16, (n, cfg.idx_heads, cfg.idx_dim))
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, (S, cfg.idx_dim), dev)
+    _need(w, "w", torch.float32, (n, cfg.idx_heads), dev)
+    if k_gate is not None:
+        _need(k_gate, "k_gate", torch.float32, (S,), dev)
+    if out is None:
+        out = torch.empty((n, cfg.topk_pools), dtype=torch.int32, device=dev)
+    _need(out, "topk_idx", torch.int32, (n, cfg.topk_pools), dev)
+    ws = _ws(cfg, WS_INDEX, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_index_scores_topk_range(
+        ctypes.byref(cc), _ptr(q_idx), _ptr(k_idx),
+        _ptr(k_gate) if k_gate is not None else None, _ptr(w), t_begin, t_end,
+        _ptr(out), _ptr(ws), ws.numel(), _stream(dev)),
+        "dsa_index_scores_topk_range")
+    return out
+
+
+def pool_keys_gated(cfg: Config, k_idx: torch.Tensor, k_gate: torch.Tensor,
+                    k_pool=None) -> torch.Tensor:
+    """Gated pool keys [S//4, D_I] bf16: softmax of each pool's 4 gate
+    scores (k_gate [S] fp32) weights its keys."""
+    S = cfg.seq_len
+    _need(k_idx, "k_idx", torch.bfloat16, (S, cfg.idx_dim))
+    dev = k_idx.device
+    _need(k_gate, "k_gate", torch.float32, (S,), dev)
+    if k_pool is None:
+        k_pool = torch.empty((S // 4, cfg.idx_dim), dtype=torch.bfloat16, device=dev)
+    _need(k_pool, "k_pool", torch.bfloat16, (S // 4, cfg.idx_dim), dev)
+    cc = cfg.c()
+    _check(_load().dsa_pool_keys_gated(ctypes.byref(cc), _ptr(k_idx), _ptr(k_gate),
+                                       _ptr(k_pool), _stream(dev)),
+           "dsa_pool_keys_gated")
+    return k_pool
+
+
+def query_shard(S: int, world: int, rank: int, align: int = 4):
+    """Query rows [t_begin, t_end) of `rank` when S queries are split over
+    `world` ranks in contiguous blocks of whole `align`-row groups (pool
+    boundaries by default), the earlier ranks taking the remainder."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad world/rank")
+    groups = (S + align - 1) // align
+    base, extra = divmod(groups, world)
+    g0 = rank * base + min(rank, extra)
+    g1 = g0 + base + (1 if rank < extra else 0)
+    return min(S, g0 * align), min(S, g1 * align)
 
 
 def index_scores_topk_static(cfg: Config, q_idx, k_idx, w,

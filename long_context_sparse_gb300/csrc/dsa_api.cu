@@ -275,6 +275,21 @@ dsa_status_t dsa_pool_keys(const dsa_config_t* cfg, const void* k_idx, void* k_p
                                  cfg->idx_dim));
 }
 
+dsa_status_t dsa_pool_keys_gated(const dsa_config_t* cfg, const void* k_idx,
+                                 const float* k_gate, void* k_pool, void* stream) {
+  dsa_status_t st = check_cfg(cfg, true, false);
+  if (st != DSA_OK) return st;
+  if (!k_idx || !k_gate || (!k_pool && cfg->seq_len >= 4)) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(k_idx) || !aligned16(k_gate) || !aligned16(k_pool))
+    return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  st = make_ctx(nullptr, stream, &ctx);
+  if (st != DSA_OK) return st;
+  return cuda_status(launch_pool_gated(ctx, static_cast<const __nv_bfloat16*>(k_idx),
+                                       k_gate, static_cast<__nv_bfloat16*>(k_pool),
+                                       cfg->seq_len, cfg->idx_dim));
+}
+
 dsa_status_t dsa_index_scores(const dsa_config_t* cfg, const void* q_idx,
                               const void* k_pool, const float* w, int64_t t0,
                               int64_t rows, float* scores, int64_t ld, void* ws,
@@ -303,7 +318,7 @@ dsa_status_t dsa_index_scores(const dsa_config_t* cfg, const void* q_idx,
   if ((st = encode_2d(&km, k_pool, (uint64_t)(S / 4), cfg->idx_dim, 128)) != DSA_OK)
     return st;
   return cuda_status(launch_indexer(ctx, qm, km, w, cfg->idx_heads, cfg->idx_dim, t0,
-                                    rows, p_lim, scores, ld));
+                                    0, rows, p_lim, scores, ld));
 }
 
 dsa_status_t dsa_topk_from_scores(const dsa_config_t* cfg, const float* scores,
@@ -324,15 +339,23 @@ dsa_status_t dsa_topk_from_scores(const dsa_config_t* cfg, const float* scores,
       launch_topk(ctx, scores, ld, row0, rows, cfg->topk_pools, topk_idx));
 }
 
-dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg, const void* q_idx,
-                                   const void* k_idx, const float* w,
-                                   int32_t* topk_idx, void* ws, size_t ws_bytes,
-                                   void* stream) {
+namespace {
+
+// Steps 1-4 for the query rows [t_begin, t_end): pool every key, then one
+// indexer + one top-k launch per chunk of C queries.  q_idx / w / topk_idx
+// hold the range's rows only (row r <-> query t_begin + r).
+dsa_status_t index_topk_rows(const dsa_config_t* cfg, const void* q_idx,
+                             const void* k_idx, const float* k_gate, const float* w,
+                             int64_t t_begin, int64_t t_end, int32_t* topk_idx,
+                             void* ws, size_t ws_bytes, void* stream) {
   dsa_status_t st = check_cfg(cfg, true, false);
   if (st != DSA_OK) return st;
+  if (t_begin < 0 || t_end < t_begin || t_end > cfg->seq_len) return DSA_ERR_INVALID_ARG;
+  if (t_end == t_begin) return DSA_OK;  // nothing is read or written
   if (!q_idx || !k_idx || !w || !topk_idx) return DSA_ERR_INVALID_ARG;
   if ((st = check_ws(cfg, DSA_WS_INDEX, ws, ws_bytes)) != DSA_OK) return st;
-  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx))
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx) ||
+      (k_gate && !aligned16(k_gate)))
     return DSA_ERR_MISALIGNED;
   const int64_t S = cfg->seq_len, P = S / 4, C = chunk_rows(cfg), ld = score_ld(cfg);
   if ((uint64_t)C * (uint64_t)ld * 4u > cfg->scratch_cap) return DSA_ERR_SCRATCH_CAP;
@@ -342,30 +365,51 @@ dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg, const void* q_idx,
   __nv_bfloat16* k_pool = reinterpret_cast<__nv_bfloat16*>(base + kHeader);
   float* scores = reinterpret_cast<float*>(
       base + kHeader + round_up((size_t)P * cfg->idx_dim * 2, 256));
+  const int64_t n_q = t_end - t_begin;
   CUtensorMap qm, km;
   if (P > 0) {
-    cudaError_t e = launch_pool(ctx, static_cast<const __nv_bfloat16*>(k_idx), k_pool,
-                                S, cfg->idx_dim);
+    const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(k_idx);
+    cudaError_t e = k_gate ? launch_pool_gated(ctx, kb, k_gate, k_pool, S, cfg->idx_dim)
+                           : launch_pool(ctx, kb, k_pool, S, cfg->idx_dim);
     if (e != cudaSuccess) return cuda_status(e);
-    if ((st = encode_2d(&qm, q_idx, (uint64_t)(S * cfg->idx_heads), cfg->idx_dim,
+    if ((st = encode_2d(&qm, q_idx, (uint64_t)(n_q * cfg->idx_heads), cfg->idx_dim,
                         256)) != DSA_OK)
       return st;
     if ((st = encode_2d(&km, k_pool, (uint64_t)P, cfg->idx_dim, 128)) != DSA_OK)
       return st;
   }
-  for (int64_t t0 = 0; t0 < S; t0 += C) {
-    const int64_t rows = (S - t0) < C ? (S - t0) : C;
+  for (int64_t t0 = t_begin; t0 < t_end; t0 += C) {
+    const int64_t rows = (t_end - t0) < C ? (t_end - t0) : C;
     const int64_t p_lim = n_full(t0 + rows - 1);
     if (p_lim > cfg->topk_pools) {  // some row has more pools than K_p: score
       cudaError_t e = launch_indexer(ctx, qm, km, w, cfg->idx_heads, cfg->idx_dim, t0,
-                                     rows, p_lim, scores, ld);
+                                     t_begin, rows, p_lim, scores, ld);
       if (e != cudaSuccess) return cuda_status(e);
     }
     cudaError_t e = launch_topk(ctx, scores, ld, t0, rows, cfg->topk_pools,
-                                topk_idx + t0 * cfg->topk_pools);
+                                topk_idx + (t0 - t_begin) * cfg->topk_pools);
     if (e != cudaSuccess) return cuda_status(e);
   }
   return DSA_OK;
+}
+
+}  // namespace
+
+dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg, const void* q_idx,
+                                   const void* k_idx, const float* w, int32_t* topk_idx,
+                                   void* ws, size_t ws_bytes, void* stream) {
+  if (!cfg) return DSA_ERR_INVALID_ARG;
+  return index_topk_rows(cfg, q_idx, k_idx, nullptr, w, 0, cfg->seq_len, topk_idx, ws,
+                         ws_bytes, stream);
+}
+
+dsa_status_t dsa_index_scores_topk_range(const dsa_config_t* cfg, const void* q_idx,
+                                         const void* k_idx, const float* k_gate,
+                                         const float* w, int64_t t_begin, int64_t t_end,
+                                         int32_t* topk_idx, void* ws, size_t ws_bytes,
+                                         void* stream) {
+  return index_topk_rows(cfg, q_idx, k_idx, k_gate, w, t_begin, t_end, topk_idx, ws,
+                         ws_bytes, stream);
 }
 
 dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q, const void* k,

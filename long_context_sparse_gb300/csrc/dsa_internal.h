@@ -24,17 +24,24 @@ struct LaunchCtx {
 cudaError_t launch_pool(const LaunchCtx& c, const __nv_bfloat16* k_idx,
                         __nv_bfloat16* k_pool, int64_t S, int D_I);
 
+// a1 with gates: softmax of gate[4p..4p+3] weights the pool's keys (fp32),
+// then bf16 RNE.  gate [S] fp32, 16-byte aligned.
+cudaError_t launch_pool_gated(const LaunchCtx& c, const __nv_bfloat16* k_idx,
+                              const float* gate, __nv_bfloat16* k_pool, int64_t S,
+                              int D_I);
+
 // a4: per-row top-k over fp32 scores (row r <-> query row0 + r).
 cudaError_t launch_topk(const LaunchCtx& c, const float* scores, int64_t ld,
                         int64_t row0, int64_t rows, int K_p, int32_t* out);
 
 // a2: indexer scores for queries t0 .. t0+rows-1 against pools < p_lim.
-// q_map: q_idx viewed as [S*H_I, D_I] bf16, box {64, 256};
-// k_map: k_pool [P, D_I] bf16, box {64, 128}.
+// q_map: q_idx viewed as [rows_q*H_I, D_I] bf16, box {64, 256}, and w
+// [rows_q, H_I], whose row 0 is query q0 (q0 = 0 for whole-sequence
+// tensors); k_map: k_pool [P, D_I] bf16, box {64, 128}.
 cudaError_t launch_indexer(const LaunchCtx& c, const CUtensorMap& q_map,
                            const CUtensorMap& k_map, const float* w, int H_I,
-                           int D_I, int64_t t0, int64_t rows, int64_t p_lim,
-                           float* scores, int64_t ld);
+                           int D_I, int64_t t0, int64_t q0, int64_t rows,
+                           int64_t p_lim, float* scores, int64_t ld);
 
 struct AttnShape {
   int64_t S;

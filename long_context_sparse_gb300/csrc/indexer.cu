@@ -78,8 +78,8 @@ template <int HI, int DI>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
-                   const float* __restrict__ w, int64_t t0, int64_t rows,
-                   int64_t p_lim, float* __restrict__ scores, int64_t ld,
+                   const float* __restrict__ w, int64_t t0, int64_t q0,
+                   int64_t rows, int64_t p_lim, float* __restrict__ scores, int64_t ld,
                    int n_ptiles, int64_t n_items, uint32_t* status,
                    uint64_t timeout_ns) {
   using C = IdxCfg<DI>;
@@ -145,7 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (nt != cur_nt) {
           if (!W.wait(b_empty, (bcount & 1) ^ 1)) break;
           mbar_expect_tx(b_full, C::kBBytes);
-          const int32_t row = (int32_t)(t0 * HI + nt * kBN);
+          const int32_t row = (int32_t)((t0 - q0) * HI + nt * kBN);
 #pragma unroll
           for (int kb = 0; kb < C::KB; ++kb)
             tma_load_2d(sB + kb * (kBN * 128), &q_map, kb * 64, row, b_full);
@@ -225,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < kBN / 2; ++j) {
           const int col = half * (kBN / 2) + j;
           const int64_t qrow = nt * QT + col / HI;
-          wr[j] = qrow < rows ? __ldg(w + (t0 + qrow) * HI + (col % HI)) : 0.f;
+          wr[j] = qrow < rows ? __ldg(w + (t0 - q0 + qrow) * HI + (col % HI)) : 0.f;
         }
         cur_nt = nt;
       }
@@ -282,7 +282,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int HI, int DI>
 cudaError_t launch_indexer_t(const LaunchCtx& c, const CUtensorMap& q_map,
                              const CUtensorMap& k_map, const float* w,
-                             int64_t t0, int64_t rows, int64_t p_lim,
+                             int64_t t0, int64_t q0, int64_t rows, int64_t p_lim,
                              float* scores, int64_t ld) {
   using C = IdxCfg<DI>;
   constexpr int QT = kBN / HI;
@@ -302,7 +302,7 @@ cudaError_t launch_indexer_t(const LaunchCtx& c, const CUtensorMap& q_map,
   }
   int64_t grid = n_items < c.num_sms ? n_items : c.num_sms;
   indexer_kernel<HI, DI><<<(unsigned)grid, kThreads, C::kSmem, c.stream>>>(
-      q_map, k_map, w, t0, rows, p_lim, scores, ld, n_ptiles, n_items, c.status,
+      q_map, k_map, w, t0, q0, rows, p_lim, scores, ld, n_ptiles, n_items, c.status,
       c.timeout_ns);
   return cudaGetLastError();
 }
@@ -311,12 +311,12 @@ cudaError_t launch_indexer_t(const LaunchCtx& c, const CUtensorMap& q_map,
 
 cudaError_t launch_indexer(const LaunchCtx& c, const CUtensorMap& q_map,
                            const CUtensorMap& k_map, const float* w, int H_I,
-                           int D_I, int64_t t0, int64_t rows, int64_t p_lim,
-                           float* scores, int64_t ld) {
+                           int D_I, int64_t t0, int64_t q0, int64_t rows,
+                           int64_t p_lim, float* scores, int64_t ld) {
 #define DSA_IDX_CASE(HI, DI)                                                   \
   if (H_I == HI && D_I == DI)                                                  \
-    return launch_indexer_t<HI, DI>(c, q_map, k_map, w, t0, rows, p_lim, scores, \
-                                    ld);
+    return launch_indexer_t<HI, DI>(c, q_map, k_map, w, t0, q0, rows, p_lim,    \
+                                    scores, ld);
   DSA_IDX_CASE(1, 64) DSA_IDX_CASE(2, 64) DSA_IDX_CASE(4, 64)
   DSA_IDX_CASE(8, 64) DSA_IDX_CASE(16, 64) DSA_IDX_CASE(32, 64)
   DSA_IDX_CASE(64, 64)

@@ -54,6 +54,54 @@ cudaError_t launch_pool(const LaunchCtx& c, const __nv_bfloat16* k_idx,
   return cudaGetLastError();
 }
 
+// --------------------------------------------------------- gated pooling
+// "k-pool gate scores that weight each key within a pool" ("Scaling
+// Training to 1M Token Context on GLM-5.3-Flash", section "DSA: Gather by
+// Token Position"), read as a softmax over the pool's 4 gate scores:
+//   w_j = exp(g_j - m) / ((e0 + e1) + (e2 + e3)),  m = max_j g_j
+//   k_pool = bf16_rne(((w0 k0 + w1 k1) + (w2 k2 + w3 k3)))      (fp32)
+// Equal gates give weights of exactly 1/4, i.e. the mean pooling above.
+__global__ void __launch_bounds__(256) pool4_gated_kernel(
+    const uint32_t* __restrict__ k, const float* __restrict__ gate,
+    uint32_t* __restrict__ kp, int64_t P, int half_d) {
+  const int64_t n = P * half_d;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t p = i / half_d;
+    const int64_t c = i - p * half_d;
+    const float4 g = __ldg(reinterpret_cast<const float4*>(gate) + p);
+    const float m = fmaxf(fmaxf(g.x, g.y), fmaxf(g.z, g.w));
+    const float e0 = expf(g.x - m), e1 = expf(g.y - m), e2 = expf(g.z - m),
+                e3 = expf(g.w - m);
+    const float den = __fadd_rn(__fadd_rn(e0, e1), __fadd_rn(e2, e3));
+    const float w0 = __fdiv_rn(e0, den), w1 = __fdiv_rn(e1, den),
+                w2 = __fdiv_rn(e2, den), w3 = __fdiv_rn(e3, den);
+    const uint32_t* base = k + (4 * p) * half_d + c;
+    const uint32_t x0 = __ldg(base), x1 = __ldg(base + half_d),
+                   x2 = __ldg(base + 2 * half_d), x3 = __ldg(base + 3 * half_d);
+    const float lo = __fadd_rn(__fadd_rn(__fmul_rn(w0, bf16_lo(x0)), __fmul_rn(w1, bf16_lo(x1))),
+                               __fadd_rn(__fmul_rn(w2, bf16_lo(x2)), __fmul_rn(w3, bf16_lo(x3))));
+    const float hi = __fadd_rn(__fadd_rn(__fmul_rn(w0, bf16_hi(x0)), __fmul_rn(w1, bf16_hi(x1))),
+                               __fadd_rn(__fmul_rn(w2, bf16_hi(x2)), __fmul_rn(w3, bf16_hi(x3))));
+    kp[i] = pack_bf16(lo, hi);
+  }
+}
+
+cudaError_t launch_pool_gated(const LaunchCtx& c, const __nv_bfloat16* k_idx,
+                              const float* gate, __nv_bfloat16* k_pool, int64_t S,
+                              int D_I) {
+  const int64_t P = S / 4;
+  if (P == 0) return cudaSuccess;
+  const int64_t n = P * (D_I / 2);
+  int64_t blocks = (n + 255) / 256;
+  const int64_t cap = (int64_t)c.num_sms * 16;
+  if (blocks > cap) blocks = cap;
+  pool4_gated_kernel<<<(unsigned)blocks, 256, 0, c.stream>>>(
+      reinterpret_cast<const uint32_t*>(k_idx), gate, reinterpret_cast<uint32_t*>(k_pool),
+      P, D_I / 2);
+  return cudaGetLastError();
+}
+
 // ----------------------------------------------------------------- top-k
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;

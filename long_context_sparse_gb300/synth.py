@@ -100,6 +100,12 @@ def indexer_inputs(wl: Workload, seed: int, device="cpu"):
     return q_idx, k_idx, w
 
 
+def gate_inputs(wl: Workload, seed: int, device="cpu"):
+    """Per-token pool gate scores [S] fp32 ~ N(0,1) (gated pooling)."""
+    g = _gen(seed + 4242, device)
+    return torch.randn(wl.S, generator=g, device=device, dtype=torch.float32)
+
+
 def attention_inputs(wl: Workload, seed: int, device="cpu"):
     """q [S,H,d_qk], k [S,d_qk], v [S,d_v], dO [S,H,d_v], all bf16."""
     g = _gen(seed + 7919, device)

@@ -61,6 +61,8 @@ def _load():
             lib.oracle_n_full.argtypes = [_i64]
             lib.oracle_pool.restype = None
             lib.oracle_pool.argtypes = [_i64, _i32, _p, _p]
+            lib.oracle_pool_gated.restype = None
+            lib.oracle_pool_gated.argtypes = [_i64, _i32, _p, _p, _p]
             lib.oracle_pool_f64.restype = None
             lib.oracle_pool_f64.argtypes = [_i64, _i32, _p, _p]
             lib.oracle_index_scores.restype = None
@@ -134,6 +136,18 @@ def pool(k_idx: np.ndarray) -> np.ndarray:
     return out
 
 
+def pool_gated(k_idx: np.ndarray, gate: np.ndarray) -> np.ndarray:
+    """Gated pool keys [S//4, D_I] bf16 bits: softmax over each pool's 4 gate
+    scores (fp32 [S]) weighting its keys, fp64, rounded via fp32 to bf16."""
+    k = _c(k_idx, np.uint16)
+    g = _c(gate, np.float32)
+    S, D = k.shape
+    assert g.shape == (S,)
+    out = np.empty((S // 4, D), np.uint16)
+    _load().oracle_pool_gated(S, D, _ptr(k), _ptr(g), _ptr(out))
+    return out
+
+
 def pool_f64(k_idx: np.ndarray) -> np.ndarray:
     k = _c(k_idx, np.uint16)
     S, D = k.shape
@@ -193,11 +207,12 @@ def topk(scores: np.ndarray, rows, K_p: int) -> np.ndarray:
     return out
 
 
-def index_topk(q_idx, k_idx, w, K_p: int, rows=None):
-    """Pool + fp64 indexer + top-k for the given rows.
-    Returns (topk [nrows, K_p] int32, scores [nrows, P] fp64)."""
+def index_topk(q_idx, k_idx, w, K_p: int, rows=None, gate=None):
+    """Pool (mean, or gated when `gate` [S] is given) + fp64 indexer + top-k
+    for the given rows.  Returns (topk [nrows, K_p] int32, scores [nrows, P]
+    fp64)."""
     S = k_idx.shape[0]
-    kp = pool(k_idx)
+    kp = pool(k_idx) if gate is None else pool_gated(k_idx, gate)
     if rows is None:
         r = np.arange(S, dtype=np.int64)
         sc = index_scores(q_idx, kp, w)

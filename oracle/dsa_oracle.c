@@ -94,6 +94,33 @@ void oracle_pool(int64_t S, int32_t D_I, const uint16_t* k_idx,
   }
 }
 
+/* Gated pooling ("Scaling Training to 1M Token Context on GLM-5.3-Flash",
+ * section "DSA: Gather by Token Position": k-pool gate scores weight each
+ * key within its pool), read as a softmax of the 4 gate scores:
+ *   k_pool[p] = sum_j w_j k[4p+j],  w_j = exp(g_j) / sum_i exp(g_i)
+ * computed in fp64 (exp of g_j - max g for range), then rounded to fp32
+ * and to bf16 nearest-even.  Equal gates give the mean. */
+void oracle_pool_gated(int64_t S, int32_t D_I, const uint16_t* k_idx,
+                       const float* gate, uint16_t* k_pool) {
+  int64_t P = S / 4;
+  for (int64_t p = 0; p < P; ++p) {
+    double g[4], m = -HUGE_VAL, e[4], den = 0.0;
+    for (int j = 0; j < 4; ++j) {
+      g[j] = (double)gate[4 * p + j];
+      if (g[j] > m) m = g[j];
+    }
+    for (int j = 0; j < 4; ++j) {
+      e[j] = exp(g[j] - m);
+      den += e[j];
+    }
+    for (int32_t d = 0; d < D_I; ++d) {
+      double acc = 0.0;
+      for (int j = 0; j < 4; ++j) acc += (e[j] / den) * bf(k_idx[(4 * p + j) * D_I + d]);
+      k_pool[p * D_I + d] = oracle_f32_to_bf16((float)acc);
+    }
+  }
+}
+
 /* fp64 pooling, for information (not bit-matched by anything). */
 void oracle_pool_f64(int64_t S, int32_t D_I, const uint16_t* k_idx,
                      double* k_pool) {

@@ -36,6 +36,32 @@ def test_pool_bit_exact(S, D):
     np.testing.assert_array_equal(bits(got), oracle.pool(bits(k_idx)))
 
 
+@pytest.mark.parametrize("S,D", [(4, 64), (1024, 128), (16387, 128)])
+def test_pool_gated_matches_oracle(S, D):
+    """fp32 softmax weights on the GPU vs the fp64 definition: equal up to
+    one bf16 ulp (different exp implementations), and bit-exactly the mean
+    pool when the gates of a pool are equal."""
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], S, D_I=D)
+    cfg = _cfg(wl)
+    _, k_idx, _ = synth.indexer_inputs(wl, 1, "cpu")
+    gate = synth.gate_inputs(wl, 1, "cpu")
+    got = dsa.pool_keys_gated(cfg, k_idx.to(DEV), gate.to(DEV))
+    torch.cuda.synchronize()
+    g = oracle.bf16_to_f32(bits(got)).astype(np.float64)
+    r = oracle.bf16_to_f32(oracle.pool_gated(bits(k_idx), gate.numpy())).astype(np.float64)
+    # one bf16 ulp of the result, plus the fp32 weights' and sums' error,
+    # which scales with sum_j w_j |k_j| (a cancelling sum can be tiny)
+    mag = oracle.bf16_to_f32(oracle.pool_gated(abs_bits(bits(k_idx)),
+                                                gate.numpy())).astype(np.float64)
+    assert np.all(np.abs(g - r) <= 2.0 ** -7 * np.abs(r) + 2.0 ** -18 * mag + 1e-30)
+    assert np.mean(g == r) > 0.99
+    flat = torch.repeat_interleave(gate[::4].contiguous(), 4)[:S].contiguous()
+    same = dsa.pool_keys_gated(cfg, k_idx.to(DEV), flat.to(DEV))
+    mean = dsa.pool_keys(cfg, k_idx.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(same, mean)
+
+
 # ----------------------------------------------------------------- top-k
 
 
@@ -141,6 +167,55 @@ def test_index_topk_chunked_equals_unchunked_bit_exact():
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+
+
+@pytest.mark.parametrize("ranges", [
+    [(0, 6000)], [(1000, 3333), (3333, 3334), (5, 5), (4000, 6000)],
+    [(0, 1), (17, 2100), (5999, 6000)]])
+def test_index_topk_range_equals_whole_sequence_rows(ranges):
+    """Each range's rows equal the whole-sequence call's rows (bit-exact:
+    a row's scores do not depend on which rows share its chunk) and the
+    oracle's selection of those rows (tie band)."""
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], 6000)
+    cfg = _cfg(wl, chunk_q=256)
+    q_idx, k_idx, w = synth.indexer_inputs(wl, 9, "cpu")
+    qd, kd, wd = q_idx.to(DEV), k_idx.to(DEV), w.to(DEV)
+    whole = dsa.index_scores_topk(cfg, qd, kd, wd)
+    ws = dsa.workspace(cfg, dsa.WS_INDEX, DEV)
+    for t0, t1 in ranges:
+        got = dsa.index_scores_topk_range(cfg, qd[t0:t1].contiguous(), kd,
+                                          wd[t0:t1].contiguous(), t0, t1, ws=ws)
+        _status_ok(ws)
+        assert got.shape == (t1 - t0, wl.K_p)
+        assert torch.equal(got, whole[t0:t1])
+        if t1 > t0:
+            rows = np.unique(np.linspace(t0, t1 - 1, 24).astype(np.int64))
+            ref, sc = oracle.index_topk(bits(q_idx), bits(k_idx), w.numpy(),
+                                        wl.K_p, rows)
+            eq, ex = check_index_rows(got.cpu().numpy()[rows - t0], ref, sc,
+                                      rows, wl.K_p)
+            assert eq + ex == rows.size
+
+
+@pytest.mark.parametrize("name,S,t0,t1", [("glm_s16k", 6000, 0, 6000),
+                                          ("padded2051_s64k", 9000, 3000, 7777)])
+def test_index_topk_gated_matches_oracle(name, S, t0, t1):
+    wl = synth.scaled(synth.WORKLOADS[name], S)
+    cfg = _cfg(wl)
+    q_idx, k_idx, w = synth.indexer_inputs(wl, 3, "cpu")
+    gate = synth.gate_inputs(wl, 3, "cpu")
+    ws = dsa.workspace(cfg, dsa.WS_INDEX, DEV)
+    got = dsa.index_scores_topk_range(cfg, q_idx[t0:t1].contiguous().to(DEV),
+                                      k_idx.to(DEV), w[t0:t1].contiguous().to(DEV),
+                                      t0, t1, k_gate=gate.to(DEV), ws=ws)
+    _status_ok(ws)
+    got = got.cpu().numpy()
+    rows = np.unique(np.concatenate([
+        np.linspace(t0, t1 - 1, 48).astype(np.int64), [t0, t1 - 1]]))
+    ref, sc = oracle.index_topk(bits(q_idx), bits(k_idx), w.numpy(), wl.K_p,
+                                rows, gate=gate.numpy())
+    eq, ex = check_index_rows(got[rows - t0], ref, sc, rows, wl.K_p)
+    assert eq + ex == rows.size and eq >= 0.9 * rows.size
 
 
 def test_index_topk_full_budget_selects_every_pool():

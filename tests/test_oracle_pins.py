@@ -95,6 +95,56 @@ def test_pool_rounding_rule_golden():
         assert got == want, (r, got)
 
 
+# --------------------------------------------------------- gated pool
+
+
+def test_gated_pool_with_equal_gates_is_the_mean_pool():
+    # a softmax of equal scores weighs every key 1/4: the mean pooling
+    S, D = 64, 48
+    m = RNG.integers(-120, 120, size=(S, D)).astype(np.float64) / 64.0
+    k = bf16_bits(m)
+    for g in (np.zeros(S), np.full(S, -7.25), np.repeat(RNG.standard_normal(S // 4), 4)):
+        np.testing.assert_array_equal(oracle.pool_gated(k, g.astype(np.float32)),
+                                      oracle.pool(k))
+
+
+def test_gated_pool_with_one_dominant_gate_is_that_key():
+    # exp(-80) relative weight: the other three keys vanish below bf16's
+    # resolution, so the pool is the dominant token's key exactly
+    S, D = 32, 16
+    k = rand_bf16((S, D))
+    win = RNG.integers(0, 4, size=S // 4)
+    g = np.zeros(S, np.float32)
+    g[4 * np.arange(S // 4) + win] = 80.0
+    got = oracle.pool_gated(k, g)
+    np.testing.assert_array_equal(got, k[4 * np.arange(S // 4) + win])
+
+
+def test_gated_pool_softmax_weights_closed_form():
+    # gates (0, ln 3, 0, 0) on one-hot keys: weights 1/6, 1/2, 1/6, 1/6
+    k = bf16_bits(np.eye(4))
+    g = np.array([0.0, math.log(3.0), 0.0, 0.0], np.float32)
+    got = bits_to_f64(oracle.pool_gated(k, g))[0]
+    want = bits_to_f64(bf16_bits(np.array([1 / 6, 1 / 2, 1 / 6, 1 / 6])))
+    np.testing.assert_array_equal(got, want)
+
+
+def test_gated_pool_invariances():
+    # adding a constant to a pool's gates, or permuting its four tokens
+    # (keys with their gates), leaves the pool unchanged
+    S, D = 128, 32
+    k = rand_bf16((S, D), std=0.3)
+    g = RNG.standard_normal(S).astype(np.float32)
+    base = oracle.pool_gated(k, g)
+    shift = np.repeat(RNG.integers(-5, 5, size=S // 4).astype(np.float32), 4)
+    np.testing.assert_array_equal(oracle.pool_gated(k, g + shift), base)
+    perm = np.concatenate([4 * p + RNG.permutation(4) for p in range(S // 4)])
+    diff = bits_to_f64(oracle.pool_gated(k[perm], g[perm])) - bits_to_f64(base)
+    # the fp64 sum order changes; after bf16 rounding at most a rare ulp
+    assert np.mean(diff == 0) > 0.99
+    assert np.all(np.abs(diff) <= 2.0 ** -7 * np.abs(bits_to_f64(base)) + 1e-30)
+
+
 # ------------------------------------------------------------- indexer
 
 
