@@ -172,8 +172,9 @@ def _oracle_init(wl_dict, paths, scale):
     import oracle
     wl = synth.Workload(**wl_dict)
     d = {k: np.load(v, mmap_mode="r") for k, v in paths.items()}
-    _W.update(oracle=oracle, wl=wl, d=d, scale=scale,
-              kp=oracle.pool(np.asarray(d["k_idx"])),
+    kp = (oracle.pool_gated(np.asarray(d["k_idx"]), np.asarray(d["k_gate"]))
+          if "k_gate" in d else oracle.pool(np.asarray(d["k_idx"])))
+    _W.update(oracle=oracle, wl=wl, d=d, scale=scale, kp=kp,
               idx=np.empty((wl.S, wl.K_p), np.int32))
 
 
@@ -213,6 +214,8 @@ def oracle_rows_data(wl, inputs, n_rows=256, seed=99):
     rt = torch.from_numpy(rows).to(inputs["q"].device)
     out = {"rows": rows, "k_idx": _np(inputs["k_idx"]), "k": _np(inputs["k"]),
            "v": _np(inputs["v"])}
+    if "k_gate" in inputs:
+        out["k_gate"] = _np(inputs["k_gate"])
     for k in ("q_idx", "w", "q", "dO"):
         out[k] = _np(inputs[k][rt])
     return out
@@ -292,14 +295,16 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def make_inputs(wl, seed, device):
+def make_inputs(wl, seed, device, gated=False):
     q_idx, k_idx, w = synth.indexer_inputs(wl, seed, device)
     q, k, v, dO = synth.attention_inputs(wl, seed, device)
-    return {"q_idx": q_idx, "k_idx": k_idx, "w": w, "q": q, "k": k, "v": v,
-            "dO": dO}
+    x = {"q_idx": q_idx, "k_idx": k_idx, "w": w, "q": q, "k": k, "v": v, "dO": dO}
+    if gated:
+        x["k_gate"] = synth.gate_inputs(wl, seed, device)
+    return x
 
 
-def reference_rows_data(wl, seed, n_rows=256):
+def reference_rows_data(wl, seed, n_rows=256, gated=False):
     """Seeded synthetic data for the oracle-only arm, generated on the host
     for the sampled rows only (same shapes and distributions)."""
     import math as _m
@@ -311,7 +316,7 @@ def reference_rows_data(wl, seed, n_rows=256):
     def nb(shape, std):
         return _np((torch.randn(shape, generator=g) * std).to(torch.bfloat16))
 
-    return {"rows": rows,
+    out = {"rows": rows,
             "k_idx": nb((wl.S, wl.D_I), 1 / _m.sqrt(wl.D_I)),
             "k": nb((wl.S, wl.d_qk), 1 / _m.sqrt(wl.d_qk)),
             "v": nb((wl.S, wl.d_v), 1 / _m.sqrt(wl.d_v)),
@@ -320,6 +325,9 @@ def reference_rows_data(wl, seed, n_rows=256):
                                -1).numpy(),
             "q": nb((n_rows, wl.H, wl.d_qk), 1 / _m.sqrt(wl.d_qk)),
             "dO": nb((n_rows, wl.H, wl.d_v), 1.0)}
+    if gated:
+        out["k_gate"] = torch.randn(wl.S, generator=g).numpy()
+    return out
 
 
 class Step:
@@ -344,8 +352,13 @@ class Step:
         x, c = self.x, self.cfg
         if ev is not None:
             ev[0].record()
-        dsa.index_scores_topk(c, x["q_idx"], x["k_idx"], x["w"], out=self.idx,
-                              ws=self.ws_i)
+        if "k_gate" in x:  # gated pools: the range entry over every query
+            dsa.index_scores_topk_range(c, x["q_idx"], x["k_idx"], x["w"], 0,
+                                        self.wl.S, k_gate=x["k_gate"],
+                                        out=self.idx, ws=self.ws_i)
+        else:
+            dsa.index_scores_topk(c, x["q_idx"], x["k_idx"], x["w"], out=self.idx,
+                                  ws=self.ws_i)
         if ev is not None:
             ev[1].record()
         dsa.sparse_attn_fwd(c, x["q"], x["k"], x["v"], self.idx, o=self.o,
@@ -388,6 +401,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu", action="store_true")
+    ap.add_argument("--pool", default="mean", choices=["mean", "gated"],
+                    help="pool keys by their mean (default) or by gate scores")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -402,6 +417,7 @@ def main():
                 "topk_pools": wl.K_p, "keys": wl.keys_per_query,
                 "heads": wl.H, "d_qk": wl.d_qk, "d_v": wl.d_v,
                 "chunk_q": wl.chunk_q, "passes": "fwd+bwd" if wl.backward else "fwd",
+                "pool": args.pool,
                 "replica_per_gpu": True,
                 "l2": "inputs larger than L2 (q 8 GiB, k/v 256 MiB at S=131072)"
                       if wl.S >= 65536 else "working set may fit L2"}
@@ -412,7 +428,7 @@ def main():
         if args.warmup < 0 or args.steps < 1:
             raise SystemExit("bad steps")
         cores = max(1, min(16, os.cpu_count() or 1))
-        data = reference_rows_data(wl, 20262)
+        data = reference_rows_data(wl, 20262, gated=args.pool == "gated")
         per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
         vals = []
         for i in range(args.warmup + args.steps):
@@ -443,7 +459,7 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     seed = 20262 + rank
-    inputs = make_inputs(wl, seed, dev)
+    inputs = make_inputs(wl, seed, dev, gated=args.pool == "gated")
     step = Step(wl, dev, inputs)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
            for _ in range(args.steps)]
