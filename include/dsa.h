@@ -200,6 +200,23 @@ DSA_API dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q,
                                  void* dv, void* ws, size_t ws_bytes,
                                  void* stream);
 
+/* Steps 5 and 6 with K = V: one tensor kv [S, d] (d = d_qk = d_v) serves as
+ * both keys and values, as the shared latent of multi-head latent attention
+ * does ("shared NoPE K/V" read as one tensor; the backward gathers each key
+ * row once for both products and sums dK and dV per row before a single
+ * scatter).  Results are those of dsa_sparse_attn_fwd / _bwd with k = v = kv,
+ * except that dkv [S, d] bf16 = dK + dV (one fp32 accumulator).
+ * ws: DSA_WS_FWD / DSA_WS_BWD. */
+DSA_API dsa_status_t dsa_sparse_attn_fwd_kv(const dsa_config_t* cfg, const void* q,
+                                    const void* kv, const int32_t* topk_idx, void* o,
+                                    float* lse, void* ws, size_t ws_bytes,
+                                    void* stream);
+DSA_API dsa_status_t dsa_sparse_attn_bwd_kv(const dsa_config_t* cfg, const void* q,
+                                    const void* kv, const void* o, const float* lse,
+                                    const void* dO, const int32_t* topk_idx, void* dq,
+                                    void* dkv, void* ws, size_t ws_bytes,
+                                    void* stream);
+
 /* Allocation-free variant of dsa_index_scores_topk (the pages have no
  * counterpart: it exists for callers that cannot allocate device memory,
  * such as a plugin whose host application has reserved all device memory

@@ -51,7 +51,7 @@ EXPORTS = [
     "dsa_sparse_attn_fwd", "dsa_sparse_attn_bwd", "dsa_get_device_status",
     "dsa_status_string", "dsa_abi_version", "dsa_last_cuda_error",
     "dsa_index_scores_topk_static", "dsa_index_scores_topk_range",
-    "dsa_pool_keys_gated",
+    "dsa_pool_keys_gated", "dsa_sparse_attn_fwd_kv", "dsa_sparse_attn_bwd_kv",
 ]
 
 
@@ -143,6 +143,8 @@ def _load():
             "dsa_index_scores_topk_static": [CP, P, P, P, P, P],
             "dsa_index_scores_topk_range": [CP, P, P, P, P, I64, I64, P, P, SZ, P],
             "dsa_pool_keys_gated": [CP, P, P, P, P],
+            "dsa_sparse_attn_fwd_kv": [CP, P, P, P, P, P, P, SZ, P],
+            "dsa_sparse_attn_bwd_kv": [CP, P, P, P, P, P, P, P, P, P, SZ, P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -427,6 +429,55 @@ def sparse_attn_bwd(cfg: Config, q, k, v, o, lse, dO, topk_idx, dq=None,
                                        _ptr(dv), _ptr(ws), ws.numel(),
                                        _stream(dev)), "dsa_sparse_attn_bwd")
     return dq, dk, dv
+
+
+def sparse_attn_fwd_kv(cfg: Config, q, kv, topk_idx, o=None, lse=None, ws=None):
+    """Sparse attention forward with K = V = kv [S, d]: (o, lse)."""
+    S, H = cfg.seq_len, cfg.attn_heads
+    _need(q, "q", torch.bfloat16, (S, H, cfg.d_qk))
+    dev = q.device
+    _need(kv, "kv", torch.bfloat16, (S, cfg.d_qk), dev)
+    _need(topk_idx, "topk_idx", torch.int32, (S, cfg.topk_pools), dev)
+    if o is None:
+        o = torch.empty((S, H, cfg.d_v), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((S, H), dtype=torch.float32, device=dev)
+    _need(o, "o", torch.bfloat16, (S, H, cfg.d_v), dev)
+    _need(lse, "lse", torch.float32, (S, H), dev)
+    ws = _ws(cfg, WS_FWD, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_sparse_attn_fwd_kv(ctypes.byref(cc), _ptr(q), _ptr(kv),
+                                          _ptr(topk_idx), _ptr(o), _ptr(lse),
+                                          _ptr(ws), ws.numel(), _stream(dev)),
+           "dsa_sparse_attn_fwd_kv")
+    return o, lse
+
+
+def sparse_attn_bwd_kv(cfg: Config, q, kv, o, lse, dO, topk_idx, dq=None,
+                       dkv=None, ws=None):
+    """Sparse attention backward with K = V = kv: (dq, dkv = dK + dV)."""
+    S, H = cfg.seq_len, cfg.attn_heads
+    _need(q, "q", torch.bfloat16, (S, H, cfg.d_qk))
+    dev = q.device
+    _need(kv, "kv", torch.bfloat16, (S, cfg.d_qk), dev)
+    _need(o, "o", torch.bfloat16, (S, H, cfg.d_v), dev)
+    _need(lse, "lse", torch.float32, (S, H), dev)
+    _need(dO, "dO", torch.bfloat16, (S, H, cfg.d_v), dev)
+    _need(topk_idx, "topk_idx", torch.int32, (S, cfg.topk_pools), dev)
+    if dq is None:
+        dq = torch.empty_like(q)
+    if dkv is None:
+        dkv = torch.empty_like(kv)
+    _need(dq, "dq", torch.bfloat16, (S, H, cfg.d_qk), dev)
+    _need(dkv, "dkv", torch.bfloat16, (S, cfg.d_qk), dev)
+    ws = _ws(cfg, WS_BWD, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_sparse_attn_bwd_kv(ctypes.byref(cc), _ptr(q), _ptr(kv),
+                                          _ptr(o), _ptr(lse), _ptr(dO),
+                                          _ptr(topk_idx), _ptr(dq), _ptr(dkv),
+                                          _ptr(ws), ws.numel(), _stream(dev)),
+           "dsa_sparse_attn_bwd_kv")
+    return dq, dkv
 
 
 def get_device_status(ws: torch.Tensor) -> int:

@@ -15,7 +15,7 @@ namespace {
 __global__ void __launch_bounds__(256) bwd_delta_kernel(
     const __nv_bfloat16* __restrict__ o, const __nv_bfloat16* __restrict__ dO,
     float* __restrict__ delta, int64_t n_rows, int D, uint32_t* sched) {
-  // the backward's work counter and tile clock restart at zero every call
+  // the backward's work counter restarts at zero every call
   if (blockIdx.x == 0 && threadIdx.x < 2 && sched) sched[threadIdx.x] = 0u;
   const int lane = threadIdx.x & 31;
   const int64_t w0 = (blockIdx.x * (int64_t)blockDim.x + threadIdx.x) >> 5;
@@ -74,8 +74,9 @@ cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
   const int64_t n4 = s.S * s.D / 4;
   zero_kernel<<<(unsigned)grid_for(c, n4), 256, 0, c.stream>>>(
       reinterpret_cast<float4*>(dk_acc), n4);
-  zero_kernel<<<(unsigned)grid_for(c, n4), 256, 0, c.stream>>>(
-      reinterpret_cast<float4*>(dv_acc), n4);
+  if (dv_acc)  // (no second accumulator when K and V are one tensor)
+    zero_kernel<<<(unsigned)grid_for(c, n4), 256, 0, c.stream>>>(
+        reinterpret_cast<float4*>(dv_acc), n4);
   return cudaGetLastError();
 }
 
@@ -86,7 +87,7 @@ cudaError_t launch_attn_bwd_finalize(const LaunchCtx& c, const AttnShape& s,
   finalize_kernel<<<(unsigned)grid_for(c, n4), 256, 0, c.stream>>>(
       reinterpret_cast<const float4*>(dk_acc), reinterpret_cast<uint2*>(dk), n4);
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || !dv_acc) return e;
   finalize_kernel<<<(unsigned)grid_for(c, n4), 256, 0, c.stream>>>(
       reinterpret_cast<const float4*>(dv_acc), reinterpret_cast<uint2*>(dv), n4);
   return cudaGetLastError();

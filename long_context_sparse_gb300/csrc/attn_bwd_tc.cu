@@ -37,17 +37,24 @@
 //   18    MMA issuer A (TMEM owner): S^T, dP^T and dQ^T, in ring order.
 //   19    MMA issuer B: the dK^T and dV^T chunks.
 // Two issuers keep the chunk stream independent of the gather ring: A runs
-// up to a tile ahead of B.  Heads are padded to N = 64 (padding heads get
+// up to a tile ahead of B.
+//
+// K = V (one tensor serving as both, as an MLA latent does): S^T and dP^T
+// take their A operand from the same gathered K stage (a third less
+// gathering), and each chunk accumulates dK^T and dV^T of the same rows in
+// TMEM before one scatter into the single dKV accumulator (half the
+// reduction bytes).  Heads are padded to N = 64 (padding heads get
 // P = 0 through LSE = +inf).  Every wait is bounded (DSA_ERR_DEVICE_TIMEOUT).
 //
 // Scheduling.  CTAs take queries from a global counter in descending t, so
 // SMs that run slower take fewer.  For L2 locality every CTA should touch
 // the same band of keys at the same time: a query's key list is sorted, so
-// tile j of every recent query covers about the same key range.  A global
-// tile clock (tiles gathered so far / number of CTAs) names the current
-// band, and each query starts at that tile index and wraps around.  The
-// live part of the fp32 dK/dV accumulators and of K/V then stays small
-// without any grid-wide barrier.
+// tile j of every recent query covers about the same key range.  Query
+// number i starts at tile (i * ntiles / CTAs) mod ntiles, the band the grid
+// has reached when it is taken, and wraps around.  The live part of the
+// fp32 dK/dV accumulators and of K/V then stays small without any
+// grid-wide barrier, and a query's tile order (hence its fp32 sum order)
+// does not depend on timing.
 #include "attn_common.cuh"
 #include "dsa_internal.h"
 
@@ -112,7 +119,7 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   }
 }
 
-template <int D>
+template <int D, bool KV>
 __global__ void __maxnreg__(kMaxReg)
     attn_bwd_tc_kernel(const __grid_constant__ CUtensorMap q_map,
                        const __grid_constant__ CUtensorMap g_map,
@@ -170,8 +177,7 @@ __global__ void __maxnreg__(kMaxReg)
   int* s_nadd = misc + 5;
   int* item_s = misc + 6;  // [2] query of the buffer (>= n_items: no more)
   int* rot_s = misc + 8;   // [2] first tile of the query (rotation)
-  uint32_t* work_ctr = sched;     // next query to take
-  uint32_t* tile_clock = sched + 1;  // tiles gathered by all CTAs so far
+  uint32_t* work_ctr = sched;  // next query to take
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Waiter W{abort_flag, status, timeout_ns};
@@ -304,10 +310,13 @@ __global__ void __maxnreg__(kMaxReg)
       if (ptid == 0) {
         ntok[buf] = n;
         npool_s[buf] = npool;
-        uint32_t clk;
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(clk) : "l"(tile_clock)
-                     : "memory");
-        rot_s[buf] = ntiles > 0 ? (int)((clk / gridDim.x) % (uint32_t)ntiles) : 0;
+        // tile band of this query's generation: queries are taken in order
+        // and every CTA works through ntiles tiles per query, so about
+        // item * ntiles / gridDim.x tiles per CTA have been gathered when
+        // it starts (a pure function of the query: results repeat exactly)
+        rot_s[buf] = ntiles > 0
+                         ? (int)(((uint64_t)item * (uint64_t)ntiles / gridDim.x) % (uint64_t)ntiles)
+                         : 0;
       }
       if (!G.sync(W)) break;
       mbar_arrive(toks_full(buf));  // releases list, mask, LSE, delta, counts
@@ -339,6 +348,7 @@ __global__ void __maxnreg__(kMaxReg)
           tt[r] = tok_of(pl, lc, npool, n, jr * kTileK + r);
         if (!(ok = G.sync(W))) break;
         for (int pass = 0; pass < 3 && ok; ++pass) {
+          if (KV && pass == 1) continue;  // the V atoms are the K atoms
           const __nv_bfloat16* src = pass == 1 ? v : k;
           for (int a = 0; a < C::kAtoms; ++a, ++u) {
             const int s = (int)(u % kStages);
@@ -370,8 +380,6 @@ __global__ void __maxnreg__(kMaxReg)
             cp_async_mbar_arrive(full(s));
           }
         }
-        if (ptid == 0)
-          asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(tile_clock) : "memory");
       }
       if (!ok) break;
     }
@@ -394,7 +402,7 @@ __global__ void __maxnreg__(kMaxReg)
           // S^T / dP^T of the previous tile have been read
           if (!(ok = W.wait(sdp_free, (T & 1u) ^ 1u))) break;
           tc_fence_after();
-          for (int pass = 0; pass < 2 && ok; ++pass) {
+          for (int pass = 0; pass < (KV ? 1 : 2) && ok; ++pass) {
             const uint32_t dst = pass == 0 ? tS : tP;
             const uint32_t bsrc = pass == 0 ? sQ : sG;
             for (int a = 0; a < C::kAtoms; ++a, ++u) {
@@ -408,6 +416,12 @@ __global__ void __maxnreg__(kMaxReg)
                 tc_mma(dst, sdesc_sw128(st + kin * 32, 16, 1024),
                        sdesc_sw128(bsrc + a * (NH * 128) + kin * 32, 16, 1024), ID_KK,
                        (a | kin) != 0 ? 1u : 0u);
+              if (KV)  // dP^T = K dO^T from the same stage
+#pragma unroll
+                for (int kin = 0; kin < 4; ++kin)
+                  tc_mma(tP, sdesc_sw128(st + kin * 32, 16, 1024),
+                         sdesc_sw128(sG + a * (NH * 128) + kin * 32, 16, 1024), ID_KK,
+                         (a | kin) != 0 ? 1u : 0u);
               issued = true;
               tc_commit(empty(s));
             }
@@ -461,6 +475,34 @@ __global__ void __maxnreg__(kMaxReg)
         if (ntiles == 0) continue;
         if (!(ok = W.wait(qd_full, nq & 1u))) break;
         for (int j = 0; j < ntiles && ok; ++j, ++T) {
+          if (KV) {
+            // one chunk per (d chunk, key quarter): dK^T then dV^T into it
+            if (!(ok = W.wait(ds_full, T & 1u))) break;
+            if (!(ok = W.wait(p_full, T & 1u))) break;
+            tc_fence_after();
+            for (int q = 0; q < 4 * C::kDChunks; ++q, ++chunk) {
+              const int dc = q >> 2, kq = q & 3;
+              const int b = (int)(chunk & 3u);
+              if (!(ok = W.wait(chunk_empty(b), ((chunk >> 2) & 1u) ^ 1u))) break;
+              tc_fence_after();
+#pragma unroll
+              for (int x = 0; x < 2; ++x)
+#pragma unroll
+                for (int ks = 0; ks < NH / 16; ++ks)
+                  tc_mma(tC + b * 32,
+                         sdesc_sw128((x == 0 ? sQ : sG) + (2 * dc) * (NH * 128) + ks * 2048,
+                                     NH * 128, 1024),
+                         sdesc_sw128((x == 0 ? sDS : sP) + kq * 32 * 128 + ks * 32, 16, 1024),
+                         ID_MK, (x | ks) != 0 ? 1u : 0u);
+              issued = true;
+              tc_commit(chunk_full(b));
+            }
+            if (!ok) break;
+            tc_commit(ds_free);
+            tc_commit(p_free);
+            if (j == ntiles - 1) tc_commit(qd_empty);
+            continue;
+          }
           for (int which = 0; which < 2 && ok; ++which) {
             const uint32_t bsrc = which == 0 ? sDS : sP;
             const uint32_t asrc = which == 0 ? sQ : sG;
@@ -614,8 +656,8 @@ __global__ void __maxnreg__(kMaxReg)
       const int ntiles = (n + kTileK - 1) / kTileK;
       for (int j = 0; j < ntiles && ok; ++j) {
         const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
-        for (int which = 0; which < 2 && ok; ++which) {
-          float* acc = (which == 0 ? dk_acc : dv_acc) + di;
+        for (int which = 0; which < (KV ? 1 : 2) && ok; ++which) {
+          float* acc = (which == 0 ? dk_acc : dv_acc) + di;  // KV: dKV
           // this half's chunks: q = half, half + 2, ... (chunk parity = half)
           for (int q = half; q < 4 * C::kDChunks; q += 2) {
             const uint32_t c = chunk + (uint32_t)q;
@@ -660,7 +702,7 @@ __global__ void __maxnreg__(kMaxReg)
   if (warp == kMmaA) tmem_dealloc(tmem, 512);
 }
 
-template <int D>
+template <int D, bool KV>
 cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& qm,
                      const CUtensorMap& gm, const __nv_bfloat16* k,
                      const __nv_bfloat16* v, const float* lse, const float* delta,
@@ -669,17 +711,17 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
   using C = BwdTcCfg<D>;
   const uint32_t smem = C::smem(s.K_p);
   if (smem > 232448) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D>,
+  cudaError_t e = cudaFuncSetAttribute(attn_bwd_tc_kernel<D, KV>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)smem);
   if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_bwd_tc_kernel<D>,
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, attn_bwd_tc_kernel<D, KV>,
                                                     kThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) {
     cudaFuncAttributes fa;
-    cudaFuncGetAttributes(&fa, attn_bwd_tc_kernel<D>);
+    cudaFuncGetAttributes(&fa, attn_bwd_tc_kernel<D, KV>);
     set_error_detail("attn_bwd_tc occupancy 0: regs=%d threads=%d dyn_smem=%u "
                      "max_threads=%d",
                      fa.numRegs, kThreads, smem, fa.maxThreadsPerBlock);
@@ -689,9 +731,9 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
   const int64_t items = s.S * n_hblk;
   int64_t grid = c.num_sms;
   if (grid > items) grid = items;
-  // sched[0]: work counter, sched[1]: tile clock; zeroed by the delta kernel
+  // sched[0]: work counter; zeroed by the delta kernel
   uint32_t* sched = c.status + 32;
-  attn_bwd_tc_kernel<D><<<(unsigned)grid, kThreads, smem, c.stream>>>(
+  attn_bwd_tc_kernel<D, KV><<<(unsigned)grid, kThreads, smem, c.stream>>>(
       qm, gm, k, v, lse, delta, idx, dq, dk_acc, dv_acc, s.S, s.H, s.K_p, s.n_loc,
       s.scale, n_hblk, c.status, c.timeout_ns, sched);
   return cudaGetLastError();
@@ -705,12 +747,16 @@ cudaError_t launch_attn_bwd_tc(const LaunchCtx& c, const AttnShape& s,
                                const float* lse, const float* delta,
                                const int32_t* idx, __nv_bfloat16* dq, float* dk_acc,
                                float* dv_acc) {
-  if (s.D == 128)
-    return launch_t<128>(c, s, q_map, g_map, k, v, lse, delta, idx, dq, dk_acc, dv_acc);
-  if (s.D == 256)
-    return launch_t<256>(c, s, q_map, g_map, k, v, lse, delta, idx, dq, dk_acc, dv_acc);
-  if (s.D == 512)
-    return launch_t<512>(c, s, q_map, g_map, k, v, lse, delta, idx, dq, dk_acc, dv_acc);
+  // dv_acc == nullptr: K and V are one tensor (k == v), dk_acc receives dKV
+  const bool kv = dv_acc == nullptr;
+#define DSA_BWD_CASE(DD)                                                          \
+  if (s.D == DD)                                                                  \
+    return kv ? launch_t<DD, true>(c, s, q_map, g_map, k, k, lse, delta, idx, dq,  \
+                                   dk_acc, dk_acc)                                \
+              : launch_t<DD, false>(c, s, q_map, g_map, k, v, lse, delta, idx, dq, \
+                                    dk_acc, dv_acc);
+  DSA_BWD_CASE(128) DSA_BWD_CASE(256) DSA_BWD_CASE(512)
+#undef DSA_BWD_CASE
   return cudaErrorInvalidValue;
 }
 

@@ -32,10 +32,12 @@
 // (DSA_ERR_DEVICE_TIMEOUT).
 //
 // Scheduling: CTAs take queries from a global counter in descending t, and
-// each query starts at the tile index named by a global tile clock (tiles
-// gathered so far / CTAs), wrapping around.  A query's key list is sorted,
-// so tile j of every recent query covers about the same band of keys: the
-// CTAs then gather from the same L2-resident band of K/V at any time.
+// query number i starts at tile (i * ntiles / CTAs) mod ntiles, wrapping
+// around: the band of tiles the grid has reached when the query is taken.
+// A query's key list is sorted, so tile j of every recent query covers
+// about the same band of keys: the CTAs then gather from the same
+// L2-resident band of K/V at any time.  The order is a function of the
+// query alone, so results repeat bit for bit.
 #include "attn_common.cuh"
 #include "dsa_internal.h"
 
@@ -160,8 +162,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   volatile int* flags = misc + 4;
   int* item_s = misc + 6;  // [2] query of the buffer (>= n_items: no more)
   int* rot_s = misc + 8;   // [2] first tile of the query (rotation)
-  uint32_t* work_ctr = sched;        // next query to take
-  uint32_t* tile_clock = sched + 1;  // tiles gathered by all CTAs so far
+  uint32_t* work_ctr = sched;  // next query to take
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Waiter W{abort_flag, status, timeout_ns};
@@ -269,10 +270,13 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       if (!G.sync(W)) break;
       if (ptid == 0) {
         ntok[buf] = n;
-        uint32_t clk;
-        asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(clk) : "l"(tile_clock)
-                     : "memory");
-        rot_s[buf] = ntiles > 0 ? (int)((clk / gridDim.x) % (uint32_t)ntiles) : 0;
+        // tile band of this query's generation: queries are taken in order
+        // and every CTA works through ntiles tiles per query, so about
+        // item * ntiles / gridDim.x tiles per CTA have been gathered when
+        // it starts (a pure function of the query: results repeat exactly)
+        rot_s[buf] = ntiles > 0
+                         ? (int)(((uint64_t)item * (uint64_t)ntiles / gridDim.x) % (uint64_t)ntiles)
+                         : 0;
       }
       if (!G.sync(W)) break;
       mbar_arrive(toks_full(buf));  // release: list, mask, count, rotation
@@ -332,8 +336,6 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             cp_async_mbar_arrive(full(s));
           }
         }
-        if (ptid == 0 && j < ntiles)
-          asm volatile("red.relaxed.gpu.global.add.u32 [%0], 1;" ::"l"(tile_clock) : "memory");
       }
       if (!ok) break;
     }
@@ -673,7 +675,7 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
   const int64_t items = s.S * n_hblk;
   int64_t grid = c.num_sms;
   if (grid > items) grid = items;
-  // sched[0]: work counter, sched[1]: tile clock (workspace header words)
+  // sched[0]: work counter (a workspace header word)
   uint32_t* sched = c.status + 32;
   e = cudaMemsetAsync(sched, 0, 2 * sizeof(uint32_t), c.stream);
   if (e != cudaSuccess) return e;

@@ -435,11 +435,19 @@ dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q, const v
   return e == cudaErrorInvalidValue ? DSA_ERR_UNSUPPORTED_SHAPE : cuda_status(e);
 }
 
-dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q, const void* k,
-                                 const void* v, const void* o, const float* lse,
-                                 const void* dO, const int32_t* topk_idx, void* dq,
-                                 void* dk, void* dv, void* ws, size_t ws_bytes,
-                                 void* stream) {
+dsa_status_t dsa_sparse_attn_fwd_kv(const dsa_config_t* cfg, const void* q, const void* kv,
+                                    const int32_t* topk_idx, void* o, float* lse, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  return dsa_sparse_attn_fwd(cfg, q, kv, kv, topk_idx, o, lse, ws, ws_bytes, stream);
+}
+
+namespace {
+
+// a7-a9.  kv: K and V are the one tensor k; dk receives dK + dV (dv unused).
+dsa_status_t attn_bwd(const dsa_config_t* cfg, const void* q, const void* k,
+                      const void* v, const void* o, const float* lse, const void* dO,
+                      const int32_t* topk_idx, void* dq, void* dk, void* dv, bool kv,
+                      void* ws, size_t ws_bytes, void* stream) {
   dsa_status_t st = check_cfg(cfg, false, true);
   if (st != DSA_OK) return st;
   if (!q || !k || !v || !o || !lse || !dO || !topk_idx || !dq || !dk || !dv)
@@ -456,7 +464,7 @@ dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q, const v
   float* delta = reinterpret_cast<float*>(base + kHeader);
   float* dk_acc = reinterpret_cast<float*>(
       base + kHeader + round_up((size_t)s.S * s.H * 4, 256));
-  float* dv_acc = dk_acc + round_up((size_t)s.S * s.D * 4, 256) / 4;
+  float* dv_acc = kv ? nullptr : dk_acc + round_up((size_t)s.S * s.D * 4, 256) / 4;
   cudaError_t e = launch_attn_bwd_pre(ctx, s, static_cast<const __nv_bfloat16*>(o),
                                       static_cast<const __nv_bfloat16*>(dO), delta,
                                       dk_acc, dv_acc);
@@ -474,6 +482,25 @@ dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q, const v
   e = launch_attn_bwd_finalize(ctx, s, dk_acc, dv_acc, static_cast<__nv_bfloat16*>(dk),
                                static_cast<__nv_bfloat16*>(dv));
   return cuda_status(e);
+}
+
+}  // namespace
+
+dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q, const void* k,
+                                 const void* v, const void* o, const float* lse,
+                                 const void* dO, const int32_t* topk_idx, void* dq,
+                                 void* dk, void* dv, void* ws, size_t ws_bytes,
+                                 void* stream) {
+  return attn_bwd(cfg, q, k, v, o, lse, dO, topk_idx, dq, dk, dv, false, ws, ws_bytes,
+                  stream);
+}
+
+dsa_status_t dsa_sparse_attn_bwd_kv(const dsa_config_t* cfg, const void* q, const void* kv,
+                                    const void* o, const float* lse, const void* dO,
+                                    const int32_t* topk_idx, void* dq, void* dkv, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  return attn_bwd(cfg, q, kv, kv, o, lse, dO, topk_idx, dq, dkv, dkv, true, ws, ws_bytes,
+                  stream);
 }
 
 dsa_status_t dsa_get_device_status(void* ws, void* stream, uint32_t* device_status) {

@@ -63,7 +63,8 @@ cudaError_t launch_attn_fwd_tc(const LaunchCtx& c, const AttnShape& s,
                                const __nv_bfloat16* v, const int32_t* idx,
                                __nv_bfloat16* o, float* lse);
 
-// a7: delta = rowsum(dO * O); zero the fp32 dK/dV accumulators.
+// a7: delta = rowsum(dO * O); zero the fp32 dK/dV accumulators (dv_acc may
+// be nullptr: one dKV accumulator).
 cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
                                 const __nv_bfloat16* o,
                                 const __nv_bfloat16* dO, float* delta,
@@ -71,6 +72,7 @@ cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
 
 // a8: sparse attention backward on tcgen05 (dQ direct, dK/dV fp32 scatter).
 // q_map / g_map: q and dO viewed as [S*H, D] bf16, box {64, 64}.
+// dv_acc == nullptr: K and V are one tensor; dk_acc receives dK + dV.
 cudaError_t launch_attn_bwd_tc(const LaunchCtx& c, const AttnShape& s,
                                const CUtensorMap& q_map, const CUtensorMap& g_map,
                                const __nv_bfloat16* k, const __nv_bfloat16* v,

@@ -287,6 +287,53 @@ def test_attn_fwd_bwd_match_oracle(name, S, over):
         assert_close(f64(dq)[rows], rdq, "dq")
 
 
+@pytest.mark.parametrize("name,S,over", [
+    ("glm_s16k", 640, {}),                  # 64 heads, d = 512
+    ("padded2051_s64k", 520, {}),           # 16 heads, 2051 keys
+    ("tiny_fwd_s1k", 300, dict(K_p=16)),    # 8 heads, d = 128
+    ("glm_s16k", 4096, {}),                 # sampled rows
+])
+def test_attn_kv_aliased_matches_oracle(name, S, over):
+    """K = V = one tensor: forward as with v = k, backward dkv = dK + dV."""
+    wl, q, k, _, dO, idx = _attn_case(name, S, 23, **over)
+    cfg = _cfg(wl)
+    qd, kd, dOd, idd = (x.to(DEV) for x in (q, k, dO, idx))
+    wsf = dsa.workspace(cfg, dsa.WS_FWD, DEV)
+    o, lse = dsa.sparse_attn_fwd_kv(cfg, qd, kd, idd, ws=wsf)
+    _status_ok(wsf)
+    o2, lse2 = dsa.sparse_attn_fwd(cfg, qd, kd, kd, idd)
+    assert torch.equal(o, o2) and torch.equal(lse, lse2)
+    wsb = dsa.workspace(cfg, dsa.WS_BWD, DEV)
+    if S <= 700:
+        dq, dkv = dsa.sparse_attn_bwd_kv(cfg, qd, kd, o, lse, dOd, idd, ws=wsb)
+        _status_ok(wsb)
+        rdq, rdk, rdv = oracle.attn_bwd(bits(q), bits(k), bits(k), bits(dO),
+                                        idx.numpy(), wl.K_p, wl.n_loc, cfg.scale)
+        _, _, mdv = oracle.attn_bwd(bits(q), bits(k), bits(k), abs_bits(bits(dO)),
+                                    idx.numpy(), wl.K_p, wl.n_loc, cfg.scale)
+        assert_close(f64(dq), rdq, "dq")
+        assert_close(f64(dkv), rdk + rdv, "dkv", mag=np.abs(rdk) + np.abs(mdv))
+        return
+    rows = synth.sample_rows(wl, 24, 5).numpy()
+    rt = torch.from_numpy(rows).to(DEV)
+    dOz = torch.zeros_like(dOd)
+    dOz[rt] = dOd[rt]
+    dq, dkv = dsa.sparse_attn_bwd_kv(cfg, qd, kd, o, lse, dOz, idd, ws=wsb)
+    _status_ok(wsb)
+    idx_h = idx.numpy()
+    keys = np.array(sorted({int(s_) for t in rows for s_ in
+                            oracle.key_set(int(t), wl.K_p, wl.n_loc, idx_h[t])}),
+                    np.int64)
+    rdq, rdk, rdv = oracle.attn_bwd(bits(q)[rows], bits(k), bits(k), bits(dO)[rows],
+                                    idx_h, wl.K_p, wl.n_loc, cfg.scale, rows, keys)
+    assert_close(f64(dq[rt]), rdq, "dq")
+    kt = torch.from_numpy(keys).to(DEV)
+    assert_close(f64(dkv[kt]), rdk + rdv, "dkv")
+    untouched = torch.ones(wl.S, dtype=torch.bool, device=DEV)
+    untouched[kt] = False
+    assert not dkv[untouched].any()
+
+
 def _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, rows):
     """dK/dV are not row-local: rerun the GPU backward with dO zeroed outside
     the sampled rows and compare with the oracle's contributions of those

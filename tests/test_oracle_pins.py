@@ -493,6 +493,38 @@ def test_bwd_matches_torch_autograd(n_loc):
     np.testing.assert_allclose(dv, rv, rtol=1e-9, atol=1e-12)
 
 
+def test_bwd_with_one_tensor_as_keys_and_values_matches_autograd():
+    # K = V = c (an MLA-style shared latent): autograd through SDPA with the
+    # same leaf as K and V returns dK + dV for c; the oracle's dk + dv must
+    # equal it (and its forward is the same as with v = k)
+    S, H, d, K_p = 44, 4, 16, 4
+    q, c, _ = _attn_case(S, H, d, 61)
+    rng = np.random.default_rng(61)
+    dO = bf16_bits(rng.standard_normal((S, H, d)))
+    idx = np.full((S, K_p), -1, np.int32)
+    mask = np.zeros((S, S), np.uint8)
+    for t in range(S):
+        n = (t + 1) // 4
+        sel = np.sort(rng.choice(n, size=min(n, K_p), replace=False))
+        idx[t, :sel.size] = sel
+        for p in sel:
+            mask[t, 4 * p:4 * p + 4] = 1
+        for s_ in range(max(0, t - 2), t + 1):
+            mask[t, s_] = 1
+    scale = 1 / math.sqrt(d)
+    rows = np.arange(S)
+    dq, dk, dv = oracle.attn_bwd(q, c, c, dO, idx, K_p, 3, scale, rows)
+    Q = torch.from_numpy(bits_to_f64(q)).permute(1, 0, 2).requires_grad_()
+    Ct = torch.from_numpy(bits_to_f64(c)).requires_grad_()
+    Ce = Ct[None].expand(H, -1, -1)
+    O = F.scaled_dot_product_attention(Q, Ce, Ce, attn_mask=torch.from_numpy(
+        mask.astype(bool)), scale=scale)
+    (O * torch.from_numpy(bits_to_f64(dO)).permute(1, 0, 2)).sum().backward()
+    np.testing.assert_allclose(dq, Q.grad.permute(1, 0, 2).numpy(), rtol=1e-9,
+                               atol=1e-12)
+    np.testing.assert_allclose(dk + dv, Ct.grad.numpy(), rtol=1e-9, atol=1e-12)
+
+
 def test_bwd_row_subset_equals_zeroed_upstream_gradient():
     # the sampled-row form (dO zero outside the listed rows) used at large S
     S, H, d, K_p = 40, 2, 8, 3
