@@ -56,8 +56,10 @@ def keys_of_row(wl, t):
     return 4 * sel + min(3, t + 1)
 
 
-def work_model(wl):
-    """Algorithmic work of one step (valid causal pairs / selected keys)."""
+def work_model(wl, kv=False):
+    """Algorithmic work of one step (valid causal pairs / selected keys).
+    kv: K and V are one tensor, so a key brings one row and one reduced
+    gradient row."""
     S = wl.S
     t = np.arange(S, dtype=np.int64)
     nf = (t + 1) // 4
@@ -68,7 +70,7 @@ def work_model(wl):
     else:
         keys = np.where(sel == nf, t + 1, 4 * sel + np.minimum(3, t + 1))
     nk = float(keys.sum())
-    row_bytes = (wl.d_qk + wl.d_v) * 2
+    row_bytes = (wl.d_qk if kv else wl.d_qk + wl.d_v) * 2
     return {
         "indexer_flops": idx_flops,
         "topk_bytes": float(np.where(nf > wl.K_p, nf, 0).sum()) * 4 + S * wl.K_p * 4,
@@ -76,7 +78,7 @@ def work_model(wl):
         "fwd_gather_bytes": nk * row_bytes,
         "bwd_flops": nk * wl.H * 2 * (3 * wl.d_qk + 2 * wl.d_v),
         "bwd_gather_bytes": nk * row_bytes,
-        "bwd_scatter_bytes": nk * (wl.d_qk + wl.d_v) * 4,
+        "bwd_scatter_bytes": nk * (wl.d_qk if kv else wl.d_qk + wl.d_v) * 4,
         "keys": nk,
     }
 
@@ -204,7 +206,7 @@ def _np(t):
     return t.numpy()
 
 
-def oracle_rows_data(wl, inputs, n_rows=256, seed=99):
+def oracle_rows_data(wl, inputs, n_rows=256, seed=99, kv=False):
     """Host copies of what the oracle needs for `n_rows` late rows (last
     S/8, the steady-state cost) of the workload: the rows' queries, weights
     and upstream gradients, and the full K/V and indexer keys."""
@@ -216,6 +218,8 @@ def oracle_rows_data(wl, inputs, n_rows=256, seed=99):
            "v": _np(inputs["v"])}
     if "k_gate" in inputs:
         out["k_gate"] = _np(inputs["k_gate"])
+    if kv:
+        out["v"] = out["k"]
     for k in ("q_idx", "w", "q", "dO"):
         out[k] = _np(inputs[k][rt])
     return out
@@ -274,10 +278,11 @@ MEASURED_TRAFFIC = {
 }
 
 
-def measured_traffic(kernel, wl):
-    """Captured DRAM bytes per launch, or None if stale or another size."""
+def measured_traffic(kernel, wl, variant=""):
+    """Captured DRAM bytes per launch, or None if stale, another size or
+    another variant of the kernel (the captures are of the default one)."""
     e = MEASURED_TRAFFIC.get(kernel)
-    if e is None or e["workload"] != wl.name or e["S"] != wl.S:
+    if e is None or variant or e["workload"] != wl.name or e["S"] != wl.S:
         return None
     h = hashlib.sha256()
     for f in e["sources"]:
@@ -304,7 +309,7 @@ def make_inputs(wl, seed, device, gated=False):
     return x
 
 
-def reference_rows_data(wl, seed, n_rows=256, gated=False):
+def reference_rows_data(wl, seed, n_rows=256, gated=False, kv=False):
     """Seeded synthetic data for the oracle-only arm, generated on the host
     for the sampled rows only (same shapes and distributions)."""
     import math as _m
@@ -327,14 +332,16 @@ def reference_rows_data(wl, seed, n_rows=256, gated=False):
             "dO": nb((n_rows, wl.H, wl.d_v), 1.0)}
     if gated:
         out["k_gate"] = torch.randn(wl.S, generator=g).numpy()
+    if kv:
+        out["v"] = out["k"]
     return out
 
 
 class Step:
     """Device buffers and workspaces for one replica of the hot path."""
 
-    def __init__(self, wl, dev, inputs):
-        self.wl, self.dev = wl, dev
+    def __init__(self, wl, dev, inputs, kv=False):
+        self.wl, self.dev, self.kv = wl, dev, kv
         self.cfg = dsa.config_for(wl)
         self.x = inputs
         S, H = wl.S, wl.H
@@ -361,11 +368,18 @@ class Step:
                                   ws=self.ws_i)
         if ev is not None:
             ev[1].record()
-        dsa.sparse_attn_fwd(c, x["q"], x["k"], x["v"], self.idx, o=self.o,
-                            lse=self.lse, ws=self.ws_f)
+        if self.kv:  # one tensor as keys and values
+            dsa.sparse_attn_fwd_kv(c, x["q"], x["k"], self.idx, o=self.o,
+                                   lse=self.lse, ws=self.ws_f)
+        else:
+            dsa.sparse_attn_fwd(c, x["q"], x["k"], x["v"], self.idx, o=self.o,
+                                lse=self.lse, ws=self.ws_f)
         if ev is not None:
             ev[2].record()
-        if self.wl.backward:
+        if self.wl.backward and self.kv:
+            dsa.sparse_attn_bwd_kv(c, x["q"], x["k"], self.o, self.lse, x["dO"],
+                                   self.idx, dq=self.dq, dkv=self.dk, ws=self.ws_b)
+        elif self.wl.backward:
             dsa.sparse_attn_bwd(c, x["q"], x["k"], x["v"], self.o, self.lse,
                                 x["dO"], self.idx, dq=self.dq, dk=self.dk,
                                 dv=self.dv, ws=self.ws_b)
@@ -375,7 +389,7 @@ class Step:
     def outputs(self):
         out = [self.idx, self.o, self.lse]
         if self.wl.backward:
-            out += [self.dq, self.dk, self.dv]
+            out += [self.dq, self.dk] + ([] if self.kv else [self.dv])
         return out
 
     def status(self):
@@ -403,6 +417,8 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--pool", default="mean", choices=["mean", "gated"],
                     help="pool keys by their mean (default) or by gate scores")
+    ap.add_argument("--kv", default="separate", choices=["separate", "aliased"],
+                    help="K and V as two tensors (default) or one (K = V)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -412,12 +428,13 @@ def main():
     wl = synth.WORKLOADS[args.workload]
     if args.seq_len:
         wl = synth.scaled(wl, args.seq_len)
-    wm = work_model(wl)
+    kv = args.kv == "aliased"
+    wm = work_model(wl, kv)
     base_cfg = {"workload": wl.name, "S": wl.S, "indexer": f"{wl.H_I}x{wl.D_I}",
                 "topk_pools": wl.K_p, "keys": wl.keys_per_query,
                 "heads": wl.H, "d_qk": wl.d_qk, "d_v": wl.d_v,
                 "chunk_q": wl.chunk_q, "passes": "fwd+bwd" if wl.backward else "fwd",
-                "pool": args.pool,
+                "pool": args.pool, "kv": args.kv,
                 "replica_per_gpu": True,
                 "l2": "inputs larger than L2 (q 8 GiB, k/v 256 MiB at S=131072)"
                       if wl.S >= 65536 else "working set may fit L2"}
@@ -428,7 +445,7 @@ def main():
         if args.warmup < 0 or args.steps < 1:
             raise SystemExit("bad steps")
         cores = max(1, min(16, os.cpu_count() or 1))
-        data = reference_rows_data(wl, 20262, gated=args.pool == "gated")
+        data = reference_rows_data(wl, 20262, gated=args.pool == "gated", kv=kv)
         per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
         vals = []
         for i in range(args.warmup + args.steps):
@@ -460,7 +477,7 @@ def main():
     torch.cuda.set_device(dev)
     seed = 20262 + rank
     inputs = make_inputs(wl, seed, dev, gated=args.pool == "gated")
-    step = Step(wl, dev, inputs)
+    step = Step(wl, dev, inputs, kv=kv)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
            for _ in range(args.steps)]
     for _ in range(args.warmup):
@@ -541,6 +558,8 @@ def main():
         return
 
     pk, pk_kind = peaks()
+    variant = ",".join(x for x in (
+        "gated" if args.pool == "gated" else "", "kv" if kv else "") if x)
     parts = {"index_topk_ms": t_idx, "attn_fwd_ms": t_fwd, "attn_bwd_ms": t_bwd}
     # dominant call and its roofline (algorithmic bytes / flops per launch)
     dom = max(parts, key=parts.get)
@@ -554,7 +573,7 @@ def main():
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
                 "unit": "GB/s",
                 "kernel": "attn_fwd_tc_kernel (gathered K/V bytes)",
-                "traffic": measured_traffic("attn_fwd_tc", wl)}
+                "traffic": measured_traffic("attn_fwd_tc", wl, variant)}
     else:
         achieved = wm["bwd_gather_bytes"] / (t_bwd / 1e3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"],
@@ -562,7 +581,7 @@ def main():
                 "kernel": "attn_bwd_tc_kernel, timed as the whole "
                           "dsa_sparse_attn_bwd call (delta + zero + main + "
                           "finalize launches; gathered K/V bytes)",
-                "traffic": measured_traffic("attn_bwd_tc", wl),
+                "traffic": measured_traffic("attn_bwd_tc", wl, variant),
                 "achieved_with_scatter": (wm["bwd_gather_bytes"] +
                                           wm["bwd_scatter_bytes"]) /
                                          (t_bwd / 1e3) / 1e9}
@@ -593,7 +612,7 @@ def main():
     if not args.no_cpu:
         cores = max(1, min(16, os.cpu_count() or 1))
         v, rows, used, wall = run_oracle_sample(
-            wl, oracle_rows_data(wl, inputs), args.cpu_seconds, cores)
+            wl, oracle_rows_data(wl, inputs, kv=kv), args.cpu_seconds, cores)
         line["cpu_baseline"] = {
             "value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": f"{rows} late query rows (last S/8) of the same workload, "
