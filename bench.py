@@ -83,11 +83,13 @@ def work_model(wl, kv=False):
     }
 
 
-def launches_per_step(wl):
+def launches_per_step(wl, streaming=False):
     """Kernel launches of one step, mirroring the library's host loop."""
     C = min(wl.chunk_q, wl.S)
     n = 1 if wl.S >= 4 else 0                   # pool
-    for t0 in range(0, wl.S, C):
+    if streaming:
+        n += 1                                  # fused indexer + selection
+    for t0 in range(0, wl.S if not streaming else 0, C):
         rows = min(C, wl.S - t0)
         if n_full(t0 + rows - 1) > wl.K_p:
             n += 1                              # indexer chunk
@@ -340,8 +342,8 @@ def reference_rows_data(wl, seed, n_rows=256, gated=False, kv=False):
 class Step:
     """Device buffers and workspaces for one replica of the hot path."""
 
-    def __init__(self, wl, dev, inputs, kv=False):
-        self.wl, self.dev, self.kv = wl, dev, kv
+    def __init__(self, wl, dev, inputs, kv=False, streaming=False):
+        self.wl, self.dev, self.kv, self.streaming = wl, dev, kv, streaming
         self.cfg = dsa.config_for(wl)
         self.x = inputs
         S, H = wl.S, wl.H
@@ -354,12 +356,18 @@ class Step:
         self.ws_i = dsa.workspace(self.cfg, dsa.WS_INDEX, dev)
         self.ws_f = dsa.workspace(self.cfg, dsa.WS_FWD, dev)
         self.ws_b = dsa.workspace(self.cfg, dsa.WS_BWD, dev)
+        if streaming:
+            self.ws_i = dsa.workspace(self.cfg, dsa.WS_STREAM, dev)
 
     def run(self, ev=None):
         x, c = self.x, self.cfg
         if ev is not None:
             ev[0].record()
-        if "k_gate" in x:  # gated pools: the range entry over every query
+        if self.streaming:  # selection fused into the indexer, no scores stored
+            dsa.index_topk_streaming(c, x["q_idx"], x["k_idx"], x["w"], 0,
+                                     self.wl.S, k_gate=x.get("k_gate"),
+                                     out=self.idx, ws=self.ws_i)
+        elif "k_gate" in x:  # gated pools: the range entry over every query
             dsa.index_scores_topk_range(c, x["q_idx"], x["k_idx"], x["w"], 0,
                                         self.wl.S, k_gate=x["k_gate"],
                                         out=self.idx, ws=self.ws_i)
@@ -417,6 +425,9 @@ def main():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--pool", default="mean", choices=["mean", "gated"],
                     help="pool keys by their mean (default) or by gate scores")
+    ap.add_argument("--select", default="chunked", choices=["chunked", "streaming"],
+                    help="top-k over stored score chunks (default) or fused "
+                         "into the indexer")
     ap.add_argument("--kv", default="separate", choices=["separate", "aliased"],
                     help="K and V as two tensors (default) or one (K = V)")
     args = ap.parse_args()
@@ -434,7 +445,7 @@ def main():
                 "topk_pools": wl.K_p, "keys": wl.keys_per_query,
                 "heads": wl.H, "d_qk": wl.d_qk, "d_v": wl.d_v,
                 "chunk_q": wl.chunk_q, "passes": "fwd+bwd" if wl.backward else "fwd",
-                "pool": args.pool, "kv": args.kv,
+                "pool": args.pool, "kv": args.kv, "select": args.select,
                 "replica_per_gpu": True,
                 "l2": "inputs larger than L2 (q 8 GiB, k/v 256 MiB at S=131072)"
                       if wl.S >= 65536 else "working set may fit L2"}
@@ -477,7 +488,7 @@ def main():
     torch.cuda.set_device(dev)
     seed = 20262 + rank
     inputs = make_inputs(wl, seed, dev, gated=args.pool == "gated")
-    step = Step(wl, dev, inputs, kv=kv)
+    step = Step(wl, dev, inputs, kv=kv, streaming=args.select == "streaming")
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
            for _ in range(args.steps)]
     for _ in range(args.warmup):
@@ -606,7 +617,8 @@ def main():
             "breakdown_ms": parts, "rates": aux,
             "roofline": roof,
             "clocks": clk.summary(),
-            "gpu_launches": launches_per_step(wl) * args.steps,
+            "gpu_launches": launches_per_step(
+                wl, args.select == "streaming") * args.steps,
             "e2e": e2e}
 
     if not args.no_cpu:

@@ -89,6 +89,7 @@ typedef struct dsa_config {
 #define DSA_WS_FWD 1   /* dsa_sparse_attn_fwd */
 #define DSA_WS_BWD 2   /* dsa_sparse_attn_bwd */
 #define DSA_WS_STATUS 3 /* dsa_index_scores, dsa_topk_from_scores */
+#define DSA_WS_STREAM 4 /* dsa_index_topk_streaming */
 
 /* Bytes of device workspace the call `which` needs for `cfg`.  Every
  * workspace begins with a 256-byte header holding the device status word;
@@ -167,6 +168,20 @@ DSA_API dsa_status_t dsa_index_scores_topk(const dsa_config_t* cfg,
  * <= S, else DSA_ERR_INVALID_ARG; an empty range does nothing.
  * ws: DSA_WS_INDEX (pooled keys of all S tokens plus one score chunk). */
 DSA_API dsa_status_t dsa_index_scores_topk_range(
+    const dsa_config_t* cfg, const void* q_idx, const void* k_idx, const float* k_gate,
+    const float* w, int64_t t_begin, int64_t t_end, int32_t* topk_idx, void* ws,
+    size_t ws_bytes, void* stream);
+
+/* Steps 1-4 with the selection fused into the indexer: no score is ever
+ * stored (the chunking of "Scaling Training to 1M Token Context on
+ * GLM-5.3-Flash", section "Splitting the DSA Indexer / Over Time: Chunking",
+ * taken to the end: each query's running selection lives in on-chip
+ * memory while the pools stream past).  Same arguments and result, row for
+ * row bit-identical, as dsa_index_scores_topk_range; the workspace holds
+ * only the pooled keys (DSA_WS_STREAM), so there is no scratch cap.
+ * Supported: H_I in {32, 64}, D_I in {64, 128}, K_p <= 768; otherwise
+ * DSA_ERR_UNSUPPORTED_SHAPE (use dsa_index_scores_topk_range). */
+DSA_API dsa_status_t dsa_index_topk_streaming(
     const dsa_config_t* cfg, const void* q_idx, const void* k_idx, const float* k_gate,
     const float* w, int64_t t_begin, int64_t t_end, int32_t* topk_idx, void* ws,
     size_t ws_bytes, void* stream);

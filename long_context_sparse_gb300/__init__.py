@@ -35,7 +35,7 @@ _LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
 _lock = threading.Lock()
 _lib = None
 
-WS_INDEX, WS_FWD, WS_BWD, WS_STATUS = 0, 1, 2, 3
+WS_INDEX, WS_FWD, WS_BWD, WS_STATUS, WS_STREAM = 0, 1, 2, 3, 4
 
 STATUS_NAMES = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED_SHAPE",
@@ -52,6 +52,7 @@ EXPORTS = [
     "dsa_status_string", "dsa_abi_version", "dsa_last_cuda_error",
     "dsa_index_scores_topk_static", "dsa_index_scores_topk_range",
     "dsa_pool_keys_gated", "dsa_sparse_attn_fwd_kv", "dsa_sparse_attn_bwd_kv",
+    "dsa_index_topk_streaming",
 ]
 
 
@@ -144,6 +145,7 @@ def _load():
             "dsa_index_scores_topk_range": [CP, P, P, P, P, I64, I64, P, P, SZ, P],
             "dsa_pool_keys_gated": [CP, P, P, P, P],
             "dsa_sparse_attn_fwd_kv": [CP, P, P, P, P, P, P, SZ, P],
+            "dsa_index_topk_streaming": [CP, P, P, P, P, I64, I64, P, P, SZ, P],
             "dsa_sparse_attn_bwd_kv": [CP, P, P, P, P, P, P, P, P, P, SZ, P],
         }
         for name, args in sig.items():
@@ -321,6 +323,33 @@ def index_scores_topk_range(cfg: Config, q_idx, k_idx, w, t_begin: int,
         _ptr(k_gate) if k_gate is not None else None, _ptr(w), t_begin, t_end,
         _ptr(out), _ptr(ws), ws.numel(), _stream(dev)),
         "dsa_index_scores_topk_range")
+    return out
+
+
+def index_topk_streaming(cfg: Config, q_idx, k_idx, w, t_begin: int = 0,
+                         t_end: int = None, k_gate=None, out=None,
+                         ws=None) -> torch.Tensor:
+    """As index_scores_topk_range, with the selection fused into the
+    indexer (no score stored; workspace: the pooled keys only)."""
+    S = cfg.seq_len
+    t_end = S if t_end is None else t_end
+    n = t_end - t_begin
+    _need(q_idx, "q_idx", torch.bfloat16, (n, cfg.idx_heads, cfg.idx_dim))
+    dev = q_idx.device
+    _need(k_idx, "k_idx", torch.bfloat16, (S, cfg.idx_dim), dev)
+    _need(w, "w", torch.float32, (n, cfg.idx_heads), dev)
+    if k_gate is not None:
+        _need(k_gate, "k_gate", torch.float32, (S,), dev)
+    if out is None:
+        out = torch.empty((n, cfg.topk_pools), dtype=torch.int32, device=dev)
+    _need(out, "topk_idx", torch.int32, (n, cfg.topk_pools), dev)
+    ws = _ws(cfg, WS_STREAM, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_index_topk_streaming(
+        ctypes.byref(cc), _ptr(q_idx), _ptr(k_idx),
+        _ptr(k_gate) if k_gate is not None else None, _ptr(w), t_begin, t_end,
+        _ptr(out), _ptr(ws), ws.numel(), _stream(dev)),
+        "dsa_index_topk_streaming")
     return out
 
 

@@ -17,7 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa_gb300.so")
-SOURCES = ["select.cu", "indexer.cu", "attn_fwd_tc.cu", "attn_bwd.cu",
+SOURCES = ["select.cu", "indexer.cu", "indexer_topk.cu", "attn_fwd_tc.cu", "attn_bwd.cu",
            "attn_bwd_tc.cu", "dsa_api.cu",
            "dsa_static.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -159,6 +159,8 @@ size_t ws_bytes_for(const dsa_config_t* c, int which) {
     case DSA_WS_FWD:
     case DSA_WS_STATUS:
       return kHeader;
+    case DSA_WS_STREAM:  // pooled keys only: no score is stored
+      return kHeader + round_up((size_t)(S / 4) * c->idx_dim * 2, 256);
     case DSA_WS_BWD: {
       const size_t dl = round_up((size_t)S * c->attn_heads * 4, 256);
       const size_t acc = round_up((size_t)S * c->d_qk * 4, 256);
@@ -246,9 +248,9 @@ const char* dsa_status_string(dsa_status_t s) {
 
 dsa_status_t dsa_workspace_size(const dsa_config_t* cfg, int32_t which, size_t* bytes) {
   if (!bytes) return DSA_ERR_INVALID_ARG;
-  if (which < DSA_WS_INDEX || which > DSA_WS_STATUS) return DSA_ERR_INVALID_ARG;
-  dsa_status_t st = check_cfg(cfg, which == DSA_WS_INDEX, which == DSA_WS_FWD ||
-                                                               which == DSA_WS_BWD);
+  if (which < DSA_WS_INDEX || which > DSA_WS_STREAM) return DSA_ERR_INVALID_ARG;
+  dsa_status_t st = check_cfg(cfg, which == DSA_WS_INDEX || which == DSA_WS_STREAM,
+                              which == DSA_WS_FWD || which == DSA_WS_BWD);
   if (st != DSA_OK) return st;
   *bytes = ws_bytes_for(cfg, which);
   return DSA_OK;
@@ -410,6 +412,43 @@ dsa_status_t dsa_index_scores_topk_range(const dsa_config_t* cfg, const void* q_
                                          void* stream) {
   return index_topk_rows(cfg, q_idx, k_idx, k_gate, w, t_begin, t_end, topk_idx, ws,
                          ws_bytes, stream);
+}
+
+dsa_status_t dsa_index_topk_streaming(const dsa_config_t* cfg, const void* q_idx,
+                                      const void* k_idx, const float* k_gate,
+                                      const float* w, int64_t t_begin, int64_t t_end,
+                                      int32_t* topk_idx, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  dsa_status_t st = check_cfg(cfg, true, false);
+  if (st != DSA_OK) return st;
+  if (!indexer_topk_supported(cfg->idx_heads, cfg->idx_dim, cfg->topk_pools))
+    return DSA_ERR_UNSUPPORTED_SHAPE;
+  if (t_begin < 0 || t_end < t_begin || t_end > cfg->seq_len) return DSA_ERR_INVALID_ARG;
+  if (t_end == t_begin) return DSA_OK;  // nothing is read or written
+  if (!q_idx || !k_idx || !w || !topk_idx) return DSA_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, DSA_WS_STREAM, ws, ws_bytes)) != DSA_OK) return st;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx) ||
+      (k_gate && !aligned16(k_gate)))
+    return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  const int64_t S = cfg->seq_len, P = S / 4, n_q = t_end - t_begin;
+  __nv_bfloat16* k_pool = reinterpret_cast<__nv_bfloat16*>(static_cast<uint8_t*>(ws) +
+                                                           kHeader);
+  const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(k_idx);
+  cudaError_t e = k_gate ? launch_pool_gated(ctx, kb, k_gate, k_pool, S, cfg->idx_dim)
+                         : launch_pool(ctx, kb, k_pool, S, cfg->idx_dim);
+  if (e != cudaSuccess) return cuda_status(e);
+  CUtensorMap qm, km;
+  if ((st = encode_2d(&qm, q_idx, (uint64_t)(n_q * cfg->idx_heads), cfg->idx_dim, 256)) !=
+      DSA_OK)
+    return st;
+  if ((st = encode_2d(&km, P > 0 ? (const void*)k_pool : k_idx, (uint64_t)(P > 0 ? P : 1),
+                      cfg->idx_dim, 128)) != DSA_OK)
+    return st;
+  e = launch_indexer_topk(ctx, qm, km, w, cfg->idx_heads, cfg->idx_dim, t_begin, t_end,
+                          cfg->topk_pools, topk_idx);
+  return cuda_status(e);
 }
 
 dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q, const void* k,

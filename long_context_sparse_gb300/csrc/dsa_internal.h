@@ -30,6 +30,15 @@ cudaError_t launch_pool_gated(const LaunchCtx& c, const __nv_bfloat16* k_idx,
                               const float* gate, __nv_bfloat16* k_pool, int64_t S,
                               int D_I);
 
+// a2 + a4 fused: the indexer whose epilogue keeps each query's selection
+// in shared memory (no score is stored).  q_map over the range's rows
+// [n_q*H_I, D_I] box {64, 256}; w [n_q, H_I]; out [n_q, K_p].
+bool indexer_topk_supported(int H_I, int D_I, int K_p);
+cudaError_t launch_indexer_topk(const LaunchCtx& c, const CUtensorMap& q_map,
+                                const CUtensorMap& k_map, const float* w, int H_I,
+                                int D_I, int64_t t_begin, int64_t t_end, int K_p,
+                                int32_t* out);
+
 // a4: per-row top-k over fp32 scores (row r <-> query row0 + r).
 cudaError_t launch_topk(const LaunchCtx& c, const float* scores, int64_t ld,
                         int64_t row0, int64_t rows, int K_p, int32_t* out);

@@ -28,7 +28,7 @@
 // the B tile stays resident while consecutive tiles share it; accumulators
 // are double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
 // overlaps the MMAs of the next.
-#include "dsa_common.cuh"
+#include "index_common.cuh"
 #include "dsa_internal.h"
 
 namespace dsa {
@@ -55,19 +55,6 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
     if (globaltimer_ns() - t0 > timeout_ns) return false;
   }
   return true;
-}
-
-// (a0, a1) += (w0, w1) * (x0, x1) with one packed fp32 FMA (each lane of
-// the pair rounds exactly like fmaf).
-__device__ __forceinline__ void fma2(float& a0, float& a1, float w0, float w1,
-                                     float x0, float x1) {
-  asm("{\n\t.reg .b64 ww, xx, aa;\n\t"
-      "mov.b64 ww, {%2, %3};\n\tmov.b64 xx, {%4, %5};\n\t"
-      "mov.b64 aa, {%0, %1};\n\t"
-      "fma.rn.f32x2 aa, ww, xx, aa;\n\t"
-      "mov.b64 {%0, %1}, aa;\n\t}"
-      : "+f"(a0), "+f"(a1)
-      : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
 }
 
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {

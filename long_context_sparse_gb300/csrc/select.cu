@@ -11,7 +11,7 @@
 // "Across GPUs: Sharding").  Exact radix select on an order-preserving u32
 // image of the fp32 score, then one index-ordered compaction pass: the
 // result is bit-identical to a stable sort on (score desc, index asc).
-#include "dsa_common.cuh"
+#include "index_common.cuh"
 #include "dsa_internal.h"
 
 namespace dsa {
@@ -108,14 +108,6 @@ constexpr int kTopkWarps = kTopkThreads / 32;
 // Rows of up to this many candidates are staged in shared memory once.
 constexpr int kTopkCacheMax = 48 * 1024;
 constexpr int kBins = 2048;  // 11-bit digits: bits 31-21, 20-10, 9-0
-
-// Order-preserving image of an fp32 score: larger float -> larger key.
-// -0.0 is first made +0.0 so the two compare equal (lower index wins).
-__device__ __forceinline__ uint32_t order_key(float f) {
-  uint32_t b = __float_as_uint(f);
-  if (b == 0x80000000u) b = 0u;
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
 
 // Digit d of the highest bins that holds the kk-th largest key; *above =
 // number of keys in higher bins.  Warp 0 only: lane l first sums the 64

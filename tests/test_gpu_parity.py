@@ -218,6 +218,56 @@ def test_index_topk_gated_matches_oracle(name, S, t0, t1):
     assert eq + ex == rows.size and eq >= 0.9 * rows.size
 
 
+@pytest.mark.parametrize("S,over,t0,t1", [
+    (6000, {}, 0, 6000),                          # 32 x 128, K_p = 512
+    (4103, dict(H_I=64), 5, 4103),               # 4 queries per tile, ragged ends
+    (3000, dict(D_I=64, K_p=100), 0, 3000),
+    (2500, dict(K_p=16), 1, 2),                   # one row
+    (9000, dict(K_p=512), 7000, 9000),           # long rows: several compactions
+    (9000, dict(K_p=768), 6000, 9000),           # the largest supported K_p
+    (20, dict(K_p=8), 0, 20),                     # empty and full-budget rows
+])
+def test_index_topk_streaming_equals_chunked_bit_exact(S, over, t0, t1):
+    """The fused selection sees the same fp32 scores as the chunked path:
+    its rows must be bit-identical, and within the tie band of the oracle."""
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], S, **over)
+    cfg = _cfg(wl)
+    q_idx, k_idx, w = synth.indexer_inputs(wl, 13, "cpu")
+    qd, kd = q_idx[t0:t1].contiguous().to(DEV), k_idx.to(DEV)
+    wd = w[t0:t1].contiguous().to(DEV)
+    ws = dsa.workspace(cfg, dsa.WS_STREAM, DEV)
+    got = dsa.index_topk_streaming(cfg, qd, kd, wd, t0, t1, ws=ws)
+    _status_ok(ws)
+    ref_gpu = dsa.index_scores_topk_range(cfg, qd, kd, wd, t0, t1)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref_gpu)
+    rows = np.unique(np.linspace(t0, t1 - 1, 16).astype(np.int64))
+    ref, sc = oracle.index_topk(bits(q_idx), bits(k_idx), w.numpy(), wl.K_p, rows)
+    eq, ex = check_index_rows(got.cpu().numpy()[rows - t0], ref, sc, rows, wl.K_p)
+    assert eq + ex == rows.size
+
+
+def test_index_topk_streaming_gated_and_unsupported():
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], 5000)
+    cfg = _cfg(wl)
+    q_idx, k_idx, w = (x.to(DEV) for x in synth.indexer_inputs(wl, 17, "cpu"))
+    gate = synth.gate_inputs(wl, 17, "cpu").to(DEV)
+    got = dsa.index_topk_streaming(cfg, q_idx, k_idx, w, k_gate=gate)
+    ref = dsa.index_scores_topk_range(cfg, q_idx, k_idx, w, 0, wl.S, k_gate=gate)
+    torch.cuda.synchronize()
+    assert torch.equal(got, ref)
+    small = synth.scaled(synth.WORKLOADS["tiny_fwd_s1k"], 512)   # H_I = 4
+    with pytest.raises(dsa.DsaError) as e:
+        qs, ks, ws_ = (x.to(DEV) for x in synth.indexer_inputs(small, 1, "cpu"))
+        dsa.index_topk_streaming(_cfg(small), qs, ks, ws_)
+    assert e.value.code == 2
+    big = synth.scaled(synth.WORKLOADS["glm_s16k"], 4096, K_p=769)  # above the list cap
+    with pytest.raises(dsa.DsaError) as e:
+        qb, kb, wb = (x.to(DEV) for x in synth.indexer_inputs(big, 1, "cpu"))
+        dsa.index_topk_streaming(_cfg(big), qb, kb, wb)
+    assert e.value.code == 2
+
+
 def test_index_topk_full_budget_selects_every_pool():
     wl = synth.scaled(synth.WORKLOADS["tiny_fwd_s1k"], 256, K_p=64)
     cfg = _cfg(wl)
