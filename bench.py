@@ -422,6 +422,8 @@ def main():
                     help="override S (smaller runs for profiling)")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--e2e-chunks", type=int, default=8,
+                    help="query ranges of the host-buffer step (1..64)")
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--pool", default="mean", choices=["mean", "gated"],
                     help="pool keys by their mean (default) or by gate scores")
@@ -537,13 +539,35 @@ def main():
         e_start = torch.cuda.Event(enable_timing=True)
         e_stop = torch.cuda.Event(enable_timing=True)
         n_e2e = max(1, min(args.steps, 3))
+        # dsa_step_host: query ranges whose copies overlap the kernels (the
+        # fused streaming selection has no host-step form: serial copies)
+        pipelined = args.select == "chunked"
+        if pipelined:
+            names = ["topk_idx", "o", "lse"] + (
+                ["dq", "dk"] + ([] if kv else ["dv"]) if wl.backward else [])
+            host_step = dict(host_in, **dict(zip(names, host_out)))
+            dev_step = dict(inputs, **dict(zip(names, step.outputs())))
+            if kv:  # one tensor as keys and values: v is not an input
+                host_step.pop("v", None)
+                dev_step.pop("v", None)
+            if not wl.backward:  # forward only: no upstream gradient
+                host_step.pop("dO", None)
+                dev_step.pop("dO", None)
+            h2d = sum(t.numel() * t.element_size() for k, t in host_step.items()
+                      if k not in names)
+            ws_step = dsa.workspace(step.cfg, dsa.WS_STEP, dev)
+            copy_streams = (torch.cuda.Stream(dev), torch.cuda.Stream(dev))
 
-        def one():
-            for k in host_in:
-                inputs[k].copy_(host_in[k], non_blocking=True)
-            step.run()
-            for h, d in zip(host_out, step.outputs()):
-                h.copy_(d, non_blocking=True)
+            def one():
+                dsa.step_host(step.cfg, host_step, dev_step, args.e2e_chunks,
+                              ws=ws_step, copy_streams=copy_streams)
+        else:
+            def one():
+                for k in host_in:
+                    inputs[k].copy_(host_in[k], non_blocking=True)
+                step.run()
+                for h, d in zip(host_out, step.outputs()):
+                    h.copy_(d, non_blocking=True)
 
         one()
         torch.cuda.synchronize()
@@ -560,7 +584,10 @@ def main():
             e_ms = float(tt.item())
         e2e = {"value": world * wl.S / (e_ms / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms}
+               "ms_per_step": e_ms,
+               "path": (f"dsa_step_host, {args.e2e_chunks} query ranges, "
+                        "copies overlapped on two side streams") if pipelined
+                       else "serial copies around the device calls"}
         del host_in, host_out
 
     if rank != 0:

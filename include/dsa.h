@@ -90,6 +90,8 @@ typedef struct dsa_config {
 #define DSA_WS_BWD 2   /* dsa_sparse_attn_bwd */
 #define DSA_WS_STATUS 3 /* dsa_index_scores, dsa_topk_from_scores */
 #define DSA_WS_STREAM 4 /* dsa_index_topk_streaming */
+#define DSA_WS_BWD_ROWS 5 /* dsa_sparse_attn_bwd_range */
+#define DSA_WS_STEP 6   /* dsa_step, dsa_step_host */
 
 /* Bytes of device workspace the call `which` needs for `cfg`.  Every
  * workspace begins with a 256-byte header holding the device status word;
@@ -231,6 +233,100 @@ DSA_API dsa_status_t dsa_sparse_attn_bwd_kv(const dsa_config_t* cfg, const void*
                                     const void* dO, const int32_t* topk_idx, void* dq,
                                     void* dkv, void* ws, size_t ws_bytes,
                                     void* stream);
+
+/* Step 5 for the queries [t_begin, t_end) only: the form a rank takes when
+ * attention is split by query across GPUs ("Scaling Training to 1M Token
+ * Context on GLM-5.3-Flash", section "Across GPUs: Sharding"), and the unit
+ * dsa_step_host pipelines.  q [n, H, d_qk], topk_idx [n, K_p], o [n, H, d_v]
+ * and lse [n, H] hold the range's rows (n = t_end - t_begin, row r <->
+ * query t_begin + r); k, v [S, d] hold every key.  Every row is
+ * bit-identical to the same row of dsa_sparse_attn_fwd.  0 <= t_begin <=
+ * t_end <= S, else DSA_ERR_INVALID_ARG; an empty range does nothing.
+ * ws: DSA_WS_FWD. */
+DSA_API dsa_status_t dsa_sparse_attn_fwd_range(const dsa_config_t* cfg, const void* q,
+                                       const void* k, const void* v,
+                                       const int32_t* topk_idx, int64_t t_begin,
+                                       int64_t t_end, void* o, float* lse, void* ws,
+                                       size_t ws_bytes, void* stream);
+
+/* Step 6 for the queries [t_begin, t_end) only.  q, o, lse, dO, topk_idx
+ * and dq hold the range's rows (as in dsa_sparse_attn_fwd_range); k, v
+ * every key.  dq rows are bit-identical to dsa_sparse_attn_bwd's.  The
+ * range's contributions to dK and dV are ADDED into the caller's fp32
+ * accumulators dk_acc, dv_acc [S, d]: zero them before the first range and
+ * convert them with dsa_accum_to_bf16 after the last (across GPUs, reduce
+ * them first).  Over ranges that partition [0, S) the sums equal the
+ * accumulators of dsa_sparse_attn_bwd up to the order of the fp32
+ * additions, which the atomic scatter leaves unspecified in every case.
+ * dv_acc == NULL requires v == k (K = V): dk_acc then receives dK + dV.
+ * ws: DSA_WS_BWD_ROWS (the range's delta rows). */
+DSA_API dsa_status_t dsa_sparse_attn_bwd_range(const dsa_config_t* cfg, const void* q,
+                                       const void* k, const void* v, const void* o,
+                                       const float* lse, const void* dO,
+                                       const int32_t* topk_idx, int64_t t_begin,
+                                       int64_t t_end, void* dq, float* dk_acc,
+                                       float* dv_acc, void* ws, size_t ws_bytes,
+                                       void* stream);
+
+/* out[i] = bf16_rne(acc[i]) for n fp32 values, n a multiple of 4 (acc
+ * 16-byte aligned, out 8-byte aligned). */
+DSA_API dsa_status_t dsa_accum_to_bf16(const float* acc, void* out, int64_t n,
+                               void* stream);
+
+/* The tensors of one whole step (steps 1-6), all [S, ...] rows, dense:
+ *   inputs : q_idx [S,H_I,D_I] bf16, k_idx [S,D_I] bf16, w [S,H_I] fp32,
+ *            k_gate [S] fp32 or NULL (mean pools; else gated pools as in
+ *            dsa_pool_keys_gated), q [S,H,d_qk] bf16, k [S,d_qk] bf16,
+ *            v [S,d_v] bf16 (v == k: K = V, as in dsa_sparse_attn_fwd_kv),
+ *            dO [S,H,d_v] bf16 or NULL (forward only);
+ *   outputs: topk_idx [S,K_p] int32, o [S,H,d_v] bf16, lse [S,H] fp32, and
+ *            with dO: dq [S,H,d_qk] bf16, dk [S,d_qk] bf16 (K = V: dK + dV),
+ *            dv [S,d_v] bf16 (unused when K = V). */
+typedef struct dsa_step_tensors {
+  void* q_idx;
+  void* k_idx;
+  float* w;
+  float* k_gate;
+  void* q;
+  void* k;
+  void* v;
+  void* dO;
+  int32_t* topk_idx;
+  void* o;
+  float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+} dsa_step_tensors_t;
+
+/* One whole step on device-resident tensors `dev`: dsa_index_scores_topk
+ * (or the gated range call over every query), dsa_sparse_attn_fwd, and when
+ * dO != NULL dsa_sparse_attn_bwd, in that order on `stream`, with one
+ * workspace (ws: DSA_WS_STEP) and one status word.  Results equal those
+ * calls'. */
+DSA_API dsa_status_t dsa_step(const dsa_config_t* cfg, const dsa_step_tensors_t* dev,
+                      void* ws, size_t ws_bytes, void* stream);
+
+/* dsa_step with the inputs in and the outputs out of HOST memory: `host`
+ * holds host pointers (page-locked, e.g. cudaHostAlloc, for the copies to
+ * overlap anything), `dev` device buffers of the same shapes, which the call
+ * fills and uses.  The queries are cut into n_chunks ranges (1..64) and
+ * the copies run on h2d_stream and d2h_stream while the kernels run on
+ * `stream`: the indexer inputs and K, V go first, then for each range its
+ * q and dO rows; the forward and the backward of a range start as soon as
+ * its rows have landed, and its o, lse and dq rows are copied back as soon
+ * as they are final (the top-k indices after the indexer, dK and dV after
+ * the last range).  The call orders itself after work already queued on
+ * `stream`, and work queued on `stream` after it waits for the
+ * last copy back, so synchronising `stream` makes every host output
+ * valid.  Results equal dsa_step's, up to the order of dK/dV's fp32
+ * additions.  The three streams must be distinct.  CUDA events are created
+ * and released inside the call; no memory is allocated.  ws: DSA_WS_STEP. */
+DSA_API dsa_status_t dsa_step_host(const dsa_config_t* cfg,
+                           const dsa_step_tensors_t* host,
+                           const dsa_step_tensors_t* dev, int32_t n_chunks, void* ws,
+                           size_t ws_bytes, void* stream, void* h2d_stream,
+                           void* d2h_stream);
 
 /* Allocation-free variant of dsa_index_scores_topk (the pages have no
  * counterpart: it exists for callers that cannot allocate device memory,

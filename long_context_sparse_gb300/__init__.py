@@ -35,7 +35,7 @@ _LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
 _lock = threading.Lock()
 _lib = None
 
-WS_INDEX, WS_FWD, WS_BWD, WS_STATUS, WS_STREAM = 0, 1, 2, 3, 4
+WS_INDEX, WS_FWD, WS_BWD, WS_STATUS, WS_STREAM, WS_BWD_ROWS, WS_STEP = range(7)
 
 STATUS_NAMES = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED_SHAPE",
@@ -52,7 +52,9 @@ EXPORTS = [
     "dsa_status_string", "dsa_abi_version", "dsa_last_cuda_error",
     "dsa_index_scores_topk_static", "dsa_index_scores_topk_range",
     "dsa_pool_keys_gated", "dsa_sparse_attn_fwd_kv", "dsa_sparse_attn_bwd_kv",
-    "dsa_index_topk_streaming",
+    "dsa_index_topk_streaming", "dsa_sparse_attn_fwd_range",
+    "dsa_sparse_attn_bwd_range", "dsa_accum_to_bf16", "dsa_step",
+    "dsa_step_host",
 ]
 
 
@@ -75,6 +77,14 @@ class _CConfig(ctypes.Structure):
 
 
 assert ctypes.sizeof(_CConfig) == 56
+
+# dsa_step_tensors_t: the step's tensors, in declaration order
+STEP_FIELDS = ("q_idx", "k_idx", "w", "k_gate", "q", "k", "v", "dO",
+               "topk_idx", "o", "lse", "dq", "dk", "dv")
+
+
+class _CStepTensors(ctypes.Structure):
+    _fields_ = [(f, ctypes.c_void_p) for f in STEP_FIELDS]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -147,6 +157,15 @@ def _load():
             "dsa_sparse_attn_fwd_kv": [CP, P, P, P, P, P, P, SZ, P],
             "dsa_index_topk_streaming": [CP, P, P, P, P, I64, I64, P, P, SZ, P],
             "dsa_sparse_attn_bwd_kv": [CP, P, P, P, P, P, P, P, P, P, SZ, P],
+            "dsa_sparse_attn_fwd_range": [CP, P, P, P, P, I64, I64, P, P, P,
+                                          SZ, P],
+            "dsa_sparse_attn_bwd_range": [CP, P, P, P, P, P, P, P, I64, I64,
+                                          P, P, P, P, SZ, P],
+            "dsa_accum_to_bf16": [P, P, I64, P],
+            "dsa_step": [CP, ctypes.POINTER(_CStepTensors), P, SZ, P],
+            "dsa_step_host": [CP, ctypes.POINTER(_CStepTensors),
+                              ctypes.POINTER(_CStepTensors), I32, P, SZ, P, P,
+                              P],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -507,6 +526,154 @@ def sparse_attn_bwd_kv(cfg: Config, q, kv, o, lse, dO, topk_idx, dq=None,
                                           _ptr(ws), ws.numel(), _stream(dev)),
            "dsa_sparse_attn_bwd_kv")
     return dq, dkv
+
+
+def sparse_attn_fwd_range(cfg: Config, q, k, v, topk_idx, t_begin: int,
+                          t_end: int, o=None, lse=None, ws=None):
+    """Sparse attention forward for queries t_begin .. t_end-1 only: q
+    [n,H,d_qk] and topk_idx [n,K_p] hold the range's rows, k and v every
+    key; returns (o [n,H,d_v], lse [n,H]), rows bit-identical to the
+    whole-sequence call's."""
+    S, H, n = cfg.seq_len, cfg.attn_heads, t_end - t_begin
+    _need(q, "q", torch.bfloat16, (n, H, cfg.d_qk))
+    dev = q.device
+    _need(k, "k", torch.bfloat16, (S, cfg.d_qk), dev)
+    _need(v, "v", torch.bfloat16, (S, cfg.d_v), dev)
+    _need(topk_idx, "topk_idx", torch.int32, (n, cfg.topk_pools), dev)
+    if o is None:
+        o = torch.empty((n, H, cfg.d_v), dtype=torch.bfloat16, device=dev)
+    if lse is None:
+        lse = torch.empty((n, H), dtype=torch.float32, device=dev)
+    _need(o, "o", torch.bfloat16, (n, H, cfg.d_v), dev)
+    _need(lse, "lse", torch.float32, (n, H), dev)
+    ws = _ws(cfg, WS_FWD, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_sparse_attn_fwd_range(
+        ctypes.byref(cc), _ptr(q), _ptr(k), _ptr(v), _ptr(topk_idx), t_begin,
+        t_end, _ptr(o), _ptr(lse), _ptr(ws), ws.numel(), _stream(dev)),
+        "dsa_sparse_attn_fwd_range")
+    return o, lse
+
+
+def sparse_attn_bwd_range(cfg: Config, q, k, v, o, lse, dO, topk_idx,
+                          t_begin: int, t_end: int, dk_acc, dv_acc=None,
+                          dq=None, ws=None):
+    """Sparse attention backward for queries t_begin .. t_end-1 only
+    (row-indexed q, o, lse, dO, topk_idx, dq as in sparse_attn_fwd_range):
+    returns dq [n,H,d_qk] and ADDS the range's dK/dV contributions into the
+    fp32 accumulators dk_acc, dv_acc [S, d] (dv_acc None with v is k:
+    dk_acc receives dK + dV)."""
+    S, H, n = cfg.seq_len, cfg.attn_heads, t_end - t_begin
+    _need(q, "q", torch.bfloat16, (n, H, cfg.d_qk))
+    dev = q.device
+    _need(k, "k", torch.bfloat16, (S, cfg.d_qk), dev)
+    _need(v, "v", torch.bfloat16, (S, cfg.d_v), dev)
+    _need(o, "o", torch.bfloat16, (n, H, cfg.d_v), dev)
+    _need(lse, "lse", torch.float32, (n, H), dev)
+    _need(dO, "dO", torch.bfloat16, (n, H, cfg.d_v), dev)
+    _need(topk_idx, "topk_idx", torch.int32, (n, cfg.topk_pools), dev)
+    _need(dk_acc, "dk_acc", torch.float32, (S, cfg.d_qk), dev)
+    if dv_acc is not None:
+        _need(dv_acc, "dv_acc", torch.float32, (S, cfg.d_v), dev)
+    if dq is None:
+        dq = torch.empty_like(q)
+    _need(dq, "dq", torch.bfloat16, (n, H, cfg.d_qk), dev)
+    ws = _ws(cfg, WS_BWD_ROWS, ws, dev)
+    cc = cfg.c()
+    _check(_load().dsa_sparse_attn_bwd_range(
+        ctypes.byref(cc), _ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(lse),
+        _ptr(dO), _ptr(topk_idx), t_begin, t_end, _ptr(dq), _ptr(dk_acc),
+        _ptr(dv_acc) if dv_acc is not None else None, _ptr(ws), ws.numel(),
+        _stream(dev)), "dsa_sparse_attn_bwd_range")
+    return dq
+
+
+def accum_to_bf16(acc: torch.Tensor, out=None) -> torch.Tensor:
+    """bf16 (round to nearest even) copy of an fp32 accumulator."""
+    _need(acc, "acc", torch.float32)
+    if out is None:
+        out = torch.empty(acc.shape, dtype=torch.bfloat16, device=acc.device)
+    _need(out, "out", torch.bfloat16, tuple(acc.shape), acc.device)
+    _check(_load().dsa_accum_to_bf16(_ptr(acc), _ptr(out), acc.numel(),
+                                     _stream(acc.device)), "dsa_accum_to_bf16")
+    return out
+
+
+def step_shapes(cfg: Config, kv: bool = False, backward: bool = True,
+                gated: bool = False) -> dict:
+    """Name -> (shape, dtype) of the tensors of one whole step."""
+    S, H, HI, DI = cfg.seq_len, cfg.attn_heads, cfg.idx_heads, cfg.idx_dim
+    bf, f32 = torch.bfloat16, torch.float32
+    shapes = {"q_idx": ((S, HI, DI), bf), "k_idx": ((S, DI), bf),
+              "w": ((S, HI), f32), "q": ((S, H, cfg.d_qk), bf),
+              "k": ((S, cfg.d_qk), bf), "topk_idx": ((S, cfg.topk_pools),
+                                                      torch.int32),
+              "o": ((S, H, cfg.d_v), bf), "lse": ((S, H), f32)}
+    if gated:
+        shapes["k_gate"] = ((S,), f32)
+    if not kv:
+        shapes["v"] = ((S, cfg.d_v), bf)
+    if backward:
+        shapes.update({"dO": ((S, H, cfg.d_v), bf), "dq": ((S, H, cfg.d_qk), bf),
+                       "dk": ((S, cfg.d_qk), bf)})
+        if not kv:
+            shapes["dv"] = ((S, cfg.d_v), bf)
+    return shapes
+
+
+def _step_struct(cfg: Config, t: dict, device: bool) -> _CStepTensors:
+    kv = "v" not in t or t["v"] is t["k"]
+    shapes = step_shapes(cfg, kv, t.get("dO") is not None,
+                         t.get("k_gate") is not None)
+    for name, (shape, dtype) in shapes.items():
+        x = t.get(name)
+        if x is None:
+            raise ValueError(f"step tensor {name} is missing")
+        if device:
+            _need(x, name, dtype, shape, t["q"].device)
+        elif x.device.type != "cpu" or x.dtype != dtype or \
+                tuple(x.shape) != shape or not x.is_contiguous():
+            raise ValueError(f"host {name} must be a contiguous CPU {dtype} "
+                             f"tensor of shape {shape}")
+    vals = {f: (t[f].data_ptr() if t.get(f) is not None else None)
+            for f in STEP_FIELDS}
+    if kv:
+        vals["v"] = vals["k"]
+    return _CStepTensors(*[vals[f] for f in STEP_FIELDS])
+
+
+def step(cfg: Config, dev: dict, ws=None) -> dict:
+    """One whole step (indexer + top-k, forward, and the backward when dev
+    has "dO") on device tensors named as in step_shapes(); outputs are
+    written into dev's output tensors.  K = V when dev has no "v"."""
+    d = dev["q"].device
+    ws = _ws(cfg, WS_STEP, ws, d)
+    st = _step_struct(cfg, dev, True)
+    cc = cfg.c()
+    _check(_load().dsa_step(ctypes.byref(cc), ctypes.byref(st), _ptr(ws),
+                            ws.numel(), _stream(d)), "dsa_step")
+    return dev
+
+
+def step_host(cfg: Config, host: dict, dev: dict, n_chunks: int = 8, ws=None,
+              copy_streams=None) -> dict:
+    """step() with inputs read from and outputs written to host tensors
+    (pinned for the copies to overlap the kernels), staged through the
+    device tensors `dev`; copies run on two side streams, kernels on the
+    current stream, which is ordered after the last copy back."""
+    d = dev["q"].device
+    ws = _ws(cfg, WS_STEP, ws, d)
+    if copy_streams is None:
+        copy_streams = (torch.cuda.Stream(d), torch.cuda.Stream(d))
+    hs, ds = copy_streams
+    sh = _step_struct(cfg, host, False)
+    sd = _step_struct(cfg, dev, True)
+    cc = cfg.c()
+    _check(_load().dsa_step_host(
+        ctypes.byref(cc), ctypes.byref(sh), ctypes.byref(sd), n_chunks,
+        _ptr(ws), ws.numel(), _stream(d), ctypes.c_void_p(hs.cuda_stream),
+        ctypes.c_void_p(ds.cuda_stream)), "dsa_step_host")
+    return host
 
 
 def get_device_status(ws: torch.Tensor) -> int:

@@ -63,20 +63,40 @@ int64_t grid_for(const LaunchCtx& c, int64_t n) {
 
 }  // namespace
 
-cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
-                                const __nv_bfloat16* o, const __nv_bfloat16* dO,
-                                float* delta, float* dk_acc, float* dv_acc) {
-  const int64_t rows = s.S * s.H;
+cudaError_t launch_attn_bwd_delta(const LaunchCtx& c, const AttnShape& s,
+                                  const __nv_bfloat16* o, const __nv_bfloat16* dO,
+                                  float* delta) {
+  const int64_t rows = (s.t_hi - s.t_lo) * s.H;  // the call's query rows
   bwd_delta_kernel<<<(unsigned)grid_for(c, rows * 32), 256, 0, c.stream>>>(
       o, dO, delta, rows, s.D, c.status ? c.status + 32 : nullptr);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_zero(const LaunchCtx& c, const AttnShape& s, float* dk_acc,
+                                 float* dv_acc) {
   const int64_t n4 = s.S * s.D / 4;
   zero_kernel<<<(unsigned)grid_for(c, n4), 256, 0, c.stream>>>(
       reinterpret_cast<float4*>(dk_acc), n4);
   if (dv_acc)  // (no second accumulator when K and V are one tensor)
     zero_kernel<<<(unsigned)grid_for(c, n4), 256, 0, c.stream>>>(
         reinterpret_cast<float4*>(dv_acc), n4);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
+                                const __nv_bfloat16* o, const __nv_bfloat16* dO,
+                                float* delta, float* dk_acc, float* dv_acc) {
+  cudaError_t e = launch_attn_bwd_delta(c, s, o, dO, delta);
+  if (e != cudaSuccess) return e;
+  return launch_attn_bwd_zero(c, s, dk_acc, dv_acc);
+}
+
+cudaError_t launch_f32_to_bf16(const LaunchCtx& c, const float* a, __nv_bfloat16* out,
+                               int64_t n) {
+  const int64_t n4 = n / 4;
+  if (n4 == 0) return cudaSuccess;
+  finalize_kernel<<<(unsigned)grid_for(c, n4), 256, 0, c.stream>>>(
+      reinterpret_cast<const float4*>(a), reinterpret_cast<uint2*>(out), n4);
   return cudaGetLastError();
 }
 

@@ -129,7 +129,8 @@ __global__ void __maxnreg__(kMaxReg)
                        const float* __restrict__ delta,
                        const int32_t* __restrict__ idx,
                        __nv_bfloat16* __restrict__ dq, float* __restrict__ dk_acc,
-                       float* __restrict__ dv_acc, int64_t S, int H, int K_p,
+                       float* __restrict__ dv_acc, int64_t t_lo, int64_t t_hi,
+                       int64_t item0, int rot_div, int H, int K_p,
                        int n_loc, float scale, int n_hblk, uint32_t* status,
                        uint64_t timeout_ns, uint32_t* sched) {
   using C = BwdTcCfg<D>;
@@ -181,7 +182,10 @@ __global__ void __maxnreg__(kMaxReg)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Waiter W{abort_flag, status, timeout_ns};
-  const int64_t n_items = S * n_hblk;
+  // queries t_lo .. t_hi-1, latest first; row r = t - t_lo of q, dO, idx,
+  // lse, delta and dq; item0 + item numbers the query as a whole-sequence
+  // call would
+  const int64_t n_items = (t_hi - t_lo) * n_hblk;
   const float c2 = scale * kLog2e;
   // every consumer of a query's key list releases it once
   constexpr uint32_t kToksUsers = kSmThreads + kScThreads + 2;
@@ -254,10 +258,10 @@ __global__ void __maxnreg__(kMaxReg)
         mbar_arrive(toks_full(buf));
         break;
       }
-      const int64_t t = S - 1 - item / n_hblk;
+      const int64_t t = t_hi - 1 - item / n_hblk, r = t - t_lo;
       const int hb = (int)(item % n_hblk);
       // ---- key list of query t as pool ids + local tokens; LSE/delta rows
-      const int32_t* row = idx + t * K_p;
+      const int32_t* row = idx + r * K_p;
       const int64_t nf = n_full(t);
       int32_t* pl = pools + buf * (K_p + 8);
       int32_t* lc = pl + K_p;
@@ -269,8 +273,8 @@ __global__ void __maxnreg__(kMaxReg)
       for (int w = ptid; w < kMaskWords; w += kProdThreads) vm[w] = 0u;
       for (int h = ptid; h < NH; h += kProdThreads) {
         const int hg = hb * 64 + h;
-        lse2_s[buf * NH + h] = hg < H ? __ldg(lse + t * H + hg) * kLog2e : INFINITY;
-        delta_s[buf * NH + h] = hg < H ? __ldg(delta + t * H + hg) : 0.f;
+        lse2_s[buf * NH + h] = hg < H ? __ldg(lse + r * H + hg) * kLog2e : INFINITY;
+        delta_s[buf * NH + h] = hg < H ? __ldg(delta + r * H + hg) : 0.f;
       }
       if (!G.sync(W)) break;
       for (int i = ptid; i < K_p; i += kProdThreads) {
@@ -315,7 +319,8 @@ __global__ void __maxnreg__(kMaxReg)
         // item * ntiles / gridDim.x tiles per CTA have been gathered when
         // it starts (a pure function of the query: results repeat exactly)
         rot_s[buf] = ntiles > 0
-                         ? (int)(((uint64_t)item * (uint64_t)ntiles / gridDim.x) % (uint64_t)ntiles)
+                         ? (int)(((uint64_t)(item0 + item) * (uint64_t)ntiles / (uint64_t)rot_div) %
+                                 (uint64_t)ntiles)
                          : 0;
       }
       if (!G.sync(W)) break;
@@ -326,9 +331,9 @@ __global__ void __maxnreg__(kMaxReg)
         mbar_expect_tx(qd_full, 2 * C::kQBytes);
 #pragma unroll
         for (int a = 0; a < C::kAtoms; ++a) {
-          tma_load_2d(sQ + a * (NH * 128), &q_map, a * 64, (int32_t)(t * H + hb * 64),
+          tma_load_2d(sQ + a * (NH * 128), &q_map, a * 64, (int32_t)(r * H + hb * 64),
                       qd_full);
-          tma_load_2d(sG + a * (NH * 128), &g_map, a * 64, (int32_t)(t * H + hb * 64),
+          tma_load_2d(sG + a * (NH * 128), &g_map, a * 64, (int32_t)(r * H + hb * 64),
                       qd_full);
         }
       }
@@ -549,7 +554,7 @@ __global__ void __maxnreg__(kMaxReg)
       if (!(ok = W.wait(toks_full(buf), (qi >> 1) & 1))) break;
       const int64_t item = item_s[buf];
       if (item >= n_items) break;
-      const int64_t t = S - 1 - item / n_hblk;
+      const int64_t r = t_hi - 1 - item / n_hblk - t_lo;  // row of dq
       const int hb = (int)(item % n_hblk);
       const int n = ntok[buf];
       const int rot = rot_s[buf];
@@ -560,7 +565,7 @@ __global__ void __maxnreg__(kMaxReg)
       const int hcount = H - hb * 64 < 64 ? H - hb * 64 : 64;
       if (ntiles == 0) {  // empty key set: dQ = 0, no dK/dV contribution
         for (int e = i; e < hcount * D; e += kSmThreads)
-          dq[(t * H + hb * 64) * (int64_t)D + e] = __float2bfloat16_rn(0.f);
+          dq[(r * H + hb * 64) * (int64_t)D + e] = __float2bfloat16_rn(0.f);
         mbar_arrive(toks_empty(buf));
         continue;
       }
@@ -627,7 +632,7 @@ __global__ void __maxnreg__(kMaxReg)
           for (int e = 0; e < 32; ++e) {
             const int h = hh * 32 + e;
             if (h < hcount)
-              dq[(t * H + hb * 64 + h) * (int64_t)D + d] = __float2bfloat16_rn(qv[e]);
+              dq[(r * H + hb * 64 + h) * (int64_t)D + d] = __float2bfloat16_rn(qv[e]);
           }
         }
       }
@@ -728,13 +733,17 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
     return cudaErrorLaunchOutOfResources;
   }
   const int n_hblk = (s.H + 63) / 64;
-  const int64_t items = s.S * n_hblk;
+  const int64_t items = (s.t_hi - s.t_lo) * n_hblk;
+  // the whole-sequence CTA count sets the tile rotation of every query
+  const int64_t rot_div = (int64_t)c.num_sms < s.S * n_hblk ? c.num_sms : s.S * n_hblk;
   int64_t grid = c.num_sms;
   if (grid > items) grid = items;
+  if (items <= 0) return cudaSuccess;
   // sched[0]: work counter; zeroed by the delta kernel
   uint32_t* sched = c.status + 32;
   attn_bwd_tc_kernel<D, KV><<<(unsigned)grid, kThreads, smem, c.stream>>>(
-      qm, gm, k, v, lse, delta, idx, dq, dk_acc, dv_acc, s.S, s.H, s.K_p, s.n_loc,
+      qm, gm, k, v, lse, delta, idx, dq, dk_acc, dv_acc, s.t_lo, s.t_hi,
+      (s.S - s.t_hi) * n_hblk, (int)rot_div, s.H, s.K_p, s.n_loc,
       s.scale, n_hblk, c.status, c.timeout_ns, sched);
   return cudaGetLastError();
 }

@@ -107,7 +107,8 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
                        const __nv_bfloat16* __restrict__ v,
                        const int32_t* __restrict__ idx,
                        __nv_bfloat16* __restrict__ o, float* __restrict__ lse,
-                       int64_t S, int H, int K_p, int n_loc, float scale_log2,
+                       int64_t t_lo, int64_t t_hi, int64_t item0, int rot_div,
+                       int H, int K_p, int n_loc, float scale_log2,
                        int n_hblk, uint32_t* status,
                        uint64_t timeout_ns, uint32_t* sched) {
   using C = TcFwdCfg<D, NH>;
@@ -166,7 +167,9 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const Waiter W{abort_flag, status, timeout_ns};
-  const int64_t n_items = S * n_hblk;
+  // queries t_lo .. t_hi-1, latest first; row r = t - t_lo of q, idx, o
+  // and lse; item0 + item numbers the query as a whole-sequence call would
+  const int64_t n_items = (t_hi - t_lo) * n_hblk;
 
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
@@ -220,11 +223,11 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         mbar_arrive(toks_full(buf));
         break;
       }
-      const int64_t t = S - 1 - item / n_hblk;
+      const int64_t t = t_hi - 1 - item / n_hblk, r = t - t_lo;
       const int hb = (int)(item % n_hblk);
       // ---- key list of query t: tokens of the selected pools, then the
       // local tokens no selected pool covers; validity bits for softmax
-      const int32_t* row = idx + t * K_p;
+      const int32_t* row = idx + r * K_p;
       const int64_t nf = n_full(t);
       uint32_t* vm = vmask + buf * kMaskWords;
       if (ptid == 0) {
@@ -272,10 +275,13 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
         ntok[buf] = n;
         // tile band of this query's generation: queries are taken in order
         // and every CTA works through ntiles tiles per query, so about
-        // item * ntiles / gridDim.x tiles per CTA have been gathered when
-        // it starts (a pure function of the query: results repeat exactly)
+        // item * ntiles / CTAs tiles per CTA have been gathered when it
+        // starts; counted in whole-sequence items over the whole-sequence
+        // CTA count, a pure function of the query, so that results repeat
+        // exactly, whatever range the call covers
         rot_s[buf] = ntiles > 0
-                         ? (int)(((uint64_t)item * (uint64_t)ntiles / gridDim.x) % (uint64_t)ntiles)
+                         ? (int)(((uint64_t)(item0 + item) * (uint64_t)ntiles / (uint64_t)rot_div) %
+                                 (uint64_t)ntiles)
                          : 0;
       }
       if (!G.sync(W)) break;
@@ -287,7 +293,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
 #pragma unroll
         for (int a = 0; a < D / 64; ++a)
           tma_load_2d(sQ + a * (NH * 128), &q_map, a * 64,
-                      (int32_t)(t * H + hb * 64), q_full);
+                      (int32_t)(r * H + hb * 64), q_full);
       }
       ++nq;
       // ---- K then V slices of every tile through the stage ring; thread
@@ -444,18 +450,18 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       if (!W.wait(toks_full(buf), (qi >> 1) & 1)) break;
       const int64_t item = item_s[buf];
       if (item >= n_items) break;
-      const int64_t t = S - 1 - item / n_hblk;
+      const int64_t r = t_hi - 1 - item / n_hblk - t_lo;  // row of o and lse
       const int hb = (int)(item % n_hblk);
       const int hcount = min(NH, H - hb * 64);
       const int n = ntok[buf];
       const int rot = rot_s[buf];
       const uint32_t* vm = vmask + buf * kMaskWords;
       const int ntiles = (n + kTileK - 1) / kTileK;
-      __nv_bfloat16* orow = o + (t * H + hb * 64) * (int64_t)D;
+      __nv_bfloat16* orow = o + (r * H + hb * 64) * (int64_t)D;
       if (ntiles == 0) {  // empty key set: O = 0, LSE = -inf
         for (int e = tid; e < hcount * D; e += kSoftmaxThreads)
           orow[e] = __float2bfloat16_rn(0.f);
-        if (tid < hcount) lse[t * H + hb * 64 + tid] = -INFINITY;
+        if (tid < hcount) lse[r * H + hb * 64 + tid] = -INFINITY;
         mbar_arrive(toks_empty(buf));
         continue;
       }
@@ -615,7 +621,7 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
             red[tid] + red[NH + tid] + red[2 * NH + tid] + red[3 * NH + tid];
         inv_s[tid] = lt > 0.f ? 1.f / lt : 0.f;
         if (tid < hcount)
-          lse[t * H + hb * 64 + tid] =
+          lse[r * H + hb * 64 + tid] =
               lt > 0.f ? (m_s[tid] + log2f(lt)) * kLn2 : -INFINITY;
       }
       if (!G.sync(W)) break;
@@ -672,15 +678,19 @@ cudaError_t launch_t(const LaunchCtx& c, const AttnShape& s, const CUtensorMap& 
     return cudaErrorLaunchOutOfResources;
   }
   const int n_hblk = (s.H + 63) / 64;
-  const int64_t items = s.S * n_hblk;
+  const int64_t items = (s.t_hi - s.t_lo) * n_hblk;
+  // the whole-sequence CTA count sets the tile rotation of every query
+  const int64_t rot_div = (int64_t)c.num_sms < s.S * n_hblk ? c.num_sms : s.S * n_hblk;
   int64_t grid = c.num_sms;
   if (grid > items) grid = items;
+  if (items <= 0) return cudaSuccess;
   // sched[0]: work counter (a workspace header word)
   uint32_t* sched = c.status + 32;
   e = cudaMemsetAsync(sched, 0, 2 * sizeof(uint32_t), c.stream);
   if (e != cudaSuccess) return e;
   attn_fwd_tc_kernel<D, NH><<<(unsigned)grid, C::kThreads, smem, c.stream>>>(
-      qm, k, v, idx, o, lse, s.S, s.H, s.K_p, s.n_loc, s.scale * kLog2e, n_hblk,
+      qm, k, v, idx, o, lse, s.t_lo, s.t_hi, (s.S - s.t_hi) * n_hblk, (int)rot_div, s.H,
+      s.K_p, s.n_loc, s.scale * kLog2e, n_hblk,
       c.status, c.timeout_ns, sched);
   return cudaGetLastError();
 }

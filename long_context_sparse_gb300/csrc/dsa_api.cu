@@ -166,6 +166,10 @@ size_t ws_bytes_for(const dsa_config_t* c, int which) {
       const size_t acc = round_up((size_t)S * c->d_qk * 4, 256);
       return kHeader + dl + 2 * acc;
     }
+    case DSA_WS_BWD_ROWS:  // delta rows only: the accumulators are the caller's
+      return kHeader + round_up((size_t)S * c->attn_heads * 4, 256);
+    case DSA_WS_STEP:  // one header, the indexer's regions, then the backward's
+      return ws_bytes_for(c, DSA_WS_INDEX) + ws_bytes_for(c, DSA_WS_BWD) - kHeader;
     default:
       return 0;
   }
@@ -208,6 +212,8 @@ AttnShape attn_shape(const dsa_config_t* c) {
   s.K_p = c->topk_pools;
   s.n_loc = c->n_local;
   s.scale = c->sm_scale > 0.f ? c->sm_scale : 1.0f / sqrtf((float)c->d_qk);
+  s.t_lo = 0;
+  s.t_hi = c->seq_len;
   return s;
 }
 
@@ -248,9 +254,11 @@ const char* dsa_status_string(dsa_status_t s) {
 
 dsa_status_t dsa_workspace_size(const dsa_config_t* cfg, int32_t which, size_t* bytes) {
   if (!bytes) return DSA_ERR_INVALID_ARG;
-  if (which < DSA_WS_INDEX || which > DSA_WS_STREAM) return DSA_ERR_INVALID_ARG;
-  dsa_status_t st = check_cfg(cfg, which == DSA_WS_INDEX || which == DSA_WS_STREAM,
-                              which == DSA_WS_FWD || which == DSA_WS_BWD);
+  if (which < DSA_WS_INDEX || which > DSA_WS_STEP) return DSA_ERR_INVALID_ARG;
+  dsa_status_t st = check_cfg(
+      cfg, which == DSA_WS_INDEX || which == DSA_WS_STREAM || which == DSA_WS_STEP,
+      which == DSA_WS_FWD || which == DSA_WS_BWD || which == DSA_WS_BWD_ROWS ||
+          which == DSA_WS_STEP);
   if (st != DSA_OK) return st;
   *bytes = ws_bytes_for(cfg, which);
   return DSA_OK;
@@ -343,31 +351,18 @@ dsa_status_t dsa_topk_from_scores(const dsa_config_t* cfg, const float* scores,
 
 namespace {
 
-// Steps 1-4 for the query rows [t_begin, t_end): pool every key, then one
-// indexer + one top-k launch per chunk of C queries.  q_idx / w / topk_idx
-// hold the range's rows only (row r <-> query t_begin + r).
-dsa_status_t index_topk_rows(const dsa_config_t* cfg, const void* q_idx,
-                             const void* k_idx, const float* k_gate, const float* w,
-                             int64_t t_begin, int64_t t_end, int32_t* topk_idx,
-                             void* ws, size_t ws_bytes, void* stream) {
-  dsa_status_t st = check_cfg(cfg, true, false);
-  if (st != DSA_OK) return st;
-  if (t_begin < 0 || t_end < t_begin || t_end > cfg->seq_len) return DSA_ERR_INVALID_ARG;
-  if (t_end == t_begin) return DSA_OK;  // nothing is read or written
-  if (!q_idx || !k_idx || !w || !topk_idx) return DSA_ERR_INVALID_ARG;
-  if ((st = check_ws(cfg, DSA_WS_INDEX, ws, ws_bytes)) != DSA_OK) return st;
-  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx) ||
-      (k_gate && !aligned16(k_gate)))
-    return DSA_ERR_MISALIGNED;
+// Steps 1-4 for the query rows [t_begin, t_end) on validated arguments: pool
+// every key into k_pool, then one indexer + one top-k launch per chunk of C
+// queries through the score chunk `scores`.  q_idx / w / topk_idx hold the
+// range's rows only (row r <-> query t_begin + r).
+dsa_status_t index_rows(const LaunchCtx& ctx, const dsa_config_t* cfg, const void* q_idx,
+                        const void* k_idx, const float* k_gate, const float* w,
+                        int64_t t_begin, int64_t t_end, int32_t* topk_idx,
+                        __nv_bfloat16* k_pool, float* scores) {
   const int64_t S = cfg->seq_len, P = S / 4, C = chunk_rows(cfg), ld = score_ld(cfg);
-  if ((uint64_t)C * (uint64_t)ld * 4u > cfg->scratch_cap) return DSA_ERR_SCRATCH_CAP;
-  LaunchCtx ctx;
-  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  __nv_bfloat16* k_pool = reinterpret_cast<__nv_bfloat16*>(base + kHeader);
-  float* scores = reinterpret_cast<float*>(
-      base + kHeader + round_up((size_t)P * cfg->idx_dim * 2, 256));
   const int64_t n_q = t_end - t_begin;
+  if (n_q == 0) return DSA_OK;
+  dsa_status_t st;
   CUtensorMap qm, km;
   if (P > 0) {
     const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(k_idx);
@@ -393,6 +388,38 @@ dsa_status_t index_topk_rows(const dsa_config_t* cfg, const void* q_idx,
     if (e != cudaSuccess) return cuda_status(e);
   }
   return DSA_OK;
+}
+
+// The indexer's payload regions (after a header): pooled keys, score chunk.
+__nv_bfloat16* index_k_pool(uint8_t* payload) {
+  return reinterpret_cast<__nv_bfloat16*>(payload);
+}
+float* index_scores(const dsa_config_t* cfg, uint8_t* payload) {
+  return reinterpret_cast<float*>(
+      payload + round_up((size_t)(cfg->seq_len / 4) * cfg->idx_dim * 2, 256));
+}
+
+// Steps 1-4 for the query rows [t_begin, t_end), arguments checked.
+dsa_status_t index_topk_rows(const dsa_config_t* cfg, const void* q_idx,
+                             const void* k_idx, const float* k_gate, const float* w,
+                             int64_t t_begin, int64_t t_end, int32_t* topk_idx,
+                             void* ws, size_t ws_bytes, void* stream) {
+  dsa_status_t st = check_cfg(cfg, true, false);
+  if (st != DSA_OK) return st;
+  if (t_begin < 0 || t_end < t_begin || t_end > cfg->seq_len) return DSA_ERR_INVALID_ARG;
+  if (t_end == t_begin) return DSA_OK;  // nothing is read or written
+  if (!q_idx || !k_idx || !w || !topk_idx) return DSA_ERR_INVALID_ARG;
+  if ((st = check_ws(cfg, DSA_WS_INDEX, ws, ws_bytes)) != DSA_OK) return st;
+  if (!aligned16(q_idx) || !aligned16(k_idx) || !aligned16(w) || !aligned16(topk_idx) ||
+      (k_gate && !aligned16(k_gate)))
+    return DSA_ERR_MISALIGNED;
+  const int64_t C = chunk_rows(cfg), ld = score_ld(cfg);
+  if ((uint64_t)C * (uint64_t)ld * 4u > cfg->scratch_cap) return DSA_ERR_SCRATCH_CAP;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  uint8_t* payload = static_cast<uint8_t*>(ws) + kHeader;
+  return index_rows(ctx, cfg, q_idx, k_idx, k_gate, w, t_begin, t_end, topk_idx,
+                    index_k_pool(payload), index_scores(cfg, payload));
 }
 
 }  // namespace
@@ -451,11 +478,79 @@ dsa_status_t dsa_index_topk_streaming(const dsa_config_t* cfg, const void* q_idx
   return cuda_status(e);
 }
 
-dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q, const void* k,
-                                 const void* v, const int32_t* topk_idx, void* o,
-                                 float* lse, void* ws, size_t ws_bytes, void* stream) {
+namespace {
+
+bool valid_range(const dsa_config_t* cfg, int64_t t_begin, int64_t t_end) {
+  return t_begin >= 0 && t_begin <= t_end && t_end <= cfg->seq_len;
+}
+
+// Step 5 for the queries s.t_lo .. s.t_hi - 1; q, idx, o and lse hold those
+// rows (row r <-> query s.t_lo + r), k and v every key.
+dsa_status_t fwd_rows(const LaunchCtx& ctx, const AttnShape& s, const void* q,
+                      const void* k, const void* v, const int32_t* idx, void* o,
+                      float* lse) {
+  const int64_t n = s.t_hi - s.t_lo;
+  if (n == 0) return DSA_OK;
+  CUtensorMap qm;
+  dsa_status_t st = encode_2d(&qm, q, (uint64_t)(n * s.H), (uint64_t)s.D,
+                              (uint32_t)attn_tc_heads(s.H));
+  if (st != DSA_OK) return st;
+  cudaError_t e = launch_attn_fwd_tc(ctx, s, qm, static_cast<const __nv_bfloat16*>(k),
+                                     static_cast<const __nv_bfloat16*>(v), idx,
+                                     static_cast<__nv_bfloat16*>(o), lse);
+  return e == cudaErrorInvalidValue ? DSA_ERR_UNSUPPORTED_SHAPE : cuda_status(e);
+}
+
+// a7-a8 for the queries s.t_lo .. s.t_hi - 1 (row-indexed buffers as in
+// fwd_rows; delta holds the rows too): dq rows, and the rows' dK/dV
+// contributions added into dk_acc / dv_acc (dv_acc == nullptr: K = V,
+// dk_acc receives dK + dV).
+dsa_status_t bwd_rows(const LaunchCtx& ctx, const AttnShape& s, const void* q,
+                      const void* k, const void* v, const void* o, const float* lse,
+                      const void* dO, const int32_t* idx, void* dq, float* delta,
+                      float* dk_acc, float* dv_acc) {
+  const int64_t n = s.t_hi - s.t_lo;
+  if (n == 0) return DSA_OK;
+  cudaError_t e = launch_attn_bwd_delta(ctx, s, static_cast<const __nv_bfloat16*>(o),
+                                        static_cast<const __nv_bfloat16*>(dO), delta);
+  if (e != cudaSuccess) return cuda_status(e);
+  CUtensorMap qm, gm;
+  dsa_status_t st;
+  if ((st = encode_2d(&qm, q, (uint64_t)(n * s.H), (uint64_t)s.D, 64)) != DSA_OK)
+    return st;
+  if ((st = encode_2d(&gm, dO, (uint64_t)(n * s.H), (uint64_t)s.D, 64)) != DSA_OK)
+    return st;
+  e = launch_attn_bwd_tc(ctx, s, qm, gm, static_cast<const __nv_bfloat16*>(k),
+                         static_cast<const __nv_bfloat16*>(v), lse, delta, idx,
+                         static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc);
+  if (e == cudaErrorInvalidValue) return DSA_ERR_UNSUPPORTED_SHAPE;
+  return cuda_status(e);
+}
+
+// Payload regions of a backward workspace (after the header).
+struct BwdRegions {
+  float* delta;
+  float* dk_acc;
+  float* dv_acc;
+};
+BwdRegions bwd_regions(const dsa_config_t* cfg, uint8_t* payload, bool kv) {
+  const int64_t S = cfg->seq_len;
+  BwdRegions r;
+  r.delta = reinterpret_cast<float*>(payload);
+  r.dk_acc = reinterpret_cast<float*>(payload +
+                                      round_up((size_t)S * cfg->attn_heads * 4, 256));
+  r.dv_acc = kv ? nullptr : r.dk_acc + round_up((size_t)S * cfg->d_qk * 4, 256) / 4;
+  return r;
+}
+
+dsa_status_t fwd_checked(const dsa_config_t* cfg, const void* q, const void* k,
+                         const void* v, const int32_t* topk_idx, int64_t t_begin,
+                         int64_t t_end, void* o, float* lse, void* ws, size_t ws_bytes,
+                         void* stream) {
   dsa_status_t st = check_cfg(cfg, false, true);
   if (st != DSA_OK) return st;
+  if (!valid_range(cfg, t_begin, t_end)) return DSA_ERR_INVALID_ARG;
+  if (t_end == t_begin) return DSA_OK;  // nothing is read or written
   if (!q || !k || !v || !topk_idx || !o || !lse) return DSA_ERR_INVALID_ARG;
   if ((st = check_ws(cfg, DSA_WS_FWD, ws, ws_bytes)) != DSA_OK) return st;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(topk_idx) ||
@@ -463,26 +558,14 @@ dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q, const v
     return DSA_ERR_MISALIGNED;
   LaunchCtx ctx;
   if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
-  const AttnShape s = attn_shape(cfg);
-  CUtensorMap qm;
-  if ((st = encode_2d(&qm, q, (uint64_t)(s.S * s.H), (uint64_t)s.D,
-                      (uint32_t)attn_tc_heads(s.H))) != DSA_OK)
-    return st;
-  cudaError_t e = launch_attn_fwd_tc(ctx, s, qm, static_cast<const __nv_bfloat16*>(k),
-                                     static_cast<const __nv_bfloat16*>(v), topk_idx,
-                                     static_cast<__nv_bfloat16*>(o), lse);
-  return e == cudaErrorInvalidValue ? DSA_ERR_UNSUPPORTED_SHAPE : cuda_status(e);
+  AttnShape s = attn_shape(cfg);
+  s.t_lo = t_begin;
+  s.t_hi = t_end;
+  return fwd_rows(ctx, s, q, k, v, topk_idx, o, lse);
 }
 
-dsa_status_t dsa_sparse_attn_fwd_kv(const dsa_config_t* cfg, const void* q, const void* kv,
-                                    const int32_t* topk_idx, void* o, float* lse, void* ws,
-                                    size_t ws_bytes, void* stream) {
-  return dsa_sparse_attn_fwd(cfg, q, kv, kv, topk_idx, o, lse, ws, ws_bytes, stream);
-}
-
-namespace {
-
-// a7-a9.  kv: K and V are the one tensor k; dk receives dK + dV (dv unused).
+// a7-a9 over every query.  kv: K and V are the one tensor k; dk receives
+// dK + dV (dv unused).
 dsa_status_t attn_bwd(const dsa_config_t* cfg, const void* q, const void* k,
                       const void* v, const void* o, const float* lse, const void* dO,
                       const int32_t* topk_idx, void* dq, void* dk, void* dv, bool kv,
@@ -499,31 +582,41 @@ dsa_status_t attn_bwd(const dsa_config_t* cfg, const void* q, const void* k,
   LaunchCtx ctx;
   if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
   const AttnShape s = attn_shape(cfg);
-  uint8_t* base = static_cast<uint8_t*>(ws);
-  float* delta = reinterpret_cast<float*>(base + kHeader);
-  float* dk_acc = reinterpret_cast<float*>(
-      base + kHeader + round_up((size_t)s.S * s.H * 4, 256));
-  float* dv_acc = kv ? nullptr : dk_acc + round_up((size_t)s.S * s.D * 4, 256) / 4;
-  cudaError_t e = launch_attn_bwd_pre(ctx, s, static_cast<const __nv_bfloat16*>(o),
-                                      static_cast<const __nv_bfloat16*>(dO), delta,
-                                      dk_acc, dv_acc);
+  const BwdRegions r = bwd_regions(cfg, static_cast<uint8_t*>(ws) + kHeader, kv);
+  cudaError_t e = launch_attn_bwd_zero(ctx, s, r.dk_acc, r.dv_acc);
   if (e != cudaSuccess) return cuda_status(e);
-  CUtensorMap qm, gm;
-  if ((st = encode_2d(&qm, q, (uint64_t)(s.S * s.H), (uint64_t)s.D, 64)) != DSA_OK)
+  if ((st = bwd_rows(ctx, s, q, k, v, o, lse, dO, topk_idx, dq, r.delta, r.dk_acc,
+                     r.dv_acc)) != DSA_OK)
     return st;
-  if ((st = encode_2d(&gm, dO, (uint64_t)(s.S * s.H), (uint64_t)s.D, 64)) != DSA_OK)
-    return st;
-  e = launch_attn_bwd_tc(ctx, s, qm, gm, static_cast<const __nv_bfloat16*>(k),
-                         static_cast<const __nv_bfloat16*>(v), lse, delta, topk_idx,
-                         static_cast<__nv_bfloat16*>(dq), dk_acc, dv_acc);
-  if (e == cudaErrorInvalidValue) return DSA_ERR_UNSUPPORTED_SHAPE;
-  if (e != cudaSuccess) return cuda_status(e);
-  e = launch_attn_bwd_finalize(ctx, s, dk_acc, dv_acc, static_cast<__nv_bfloat16*>(dk),
+  e = launch_attn_bwd_finalize(ctx, s, r.dk_acc, r.dv_acc, static_cast<__nv_bfloat16*>(dk),
                                static_cast<__nv_bfloat16*>(dv));
   return cuda_status(e);
 }
 
 }  // namespace
+
+dsa_status_t dsa_sparse_attn_fwd(const dsa_config_t* cfg, const void* q, const void* k,
+                                 const void* v, const int32_t* topk_idx, void* o,
+                                 float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (!cfg) return DSA_ERR_INVALID_ARG;
+  return fwd_checked(cfg, q, k, v, topk_idx, 0, cfg->seq_len, o, lse, ws, ws_bytes,
+                     stream);
+}
+
+dsa_status_t dsa_sparse_attn_fwd_range(const dsa_config_t* cfg, const void* q,
+                                       const void* k, const void* v,
+                                       const int32_t* topk_idx, int64_t t_begin,
+                                       int64_t t_end, void* o, float* lse, void* ws,
+                                       size_t ws_bytes, void* stream) {
+  return fwd_checked(cfg, q, k, v, topk_idx, t_begin, t_end, o, lse, ws, ws_bytes,
+                     stream);
+}
+
+dsa_status_t dsa_sparse_attn_fwd_kv(const dsa_config_t* cfg, const void* q, const void* kv,
+                                    const int32_t* topk_idx, void* o, float* lse, void* ws,
+                                    size_t ws_bytes, void* stream) {
+  return dsa_sparse_attn_fwd(cfg, q, kv, kv, topk_idx, o, lse, ws, ws_bytes, stream);
+}
 
 dsa_status_t dsa_sparse_attn_bwd(const dsa_config_t* cfg, const void* q, const void* k,
                                  const void* v, const void* o, const float* lse,
@@ -540,6 +633,246 @@ dsa_status_t dsa_sparse_attn_bwd_kv(const dsa_config_t* cfg, const void* q, cons
                                     size_t ws_bytes, void* stream) {
   return attn_bwd(cfg, q, kv, kv, o, lse, dO, topk_idx, dq, dkv, dkv, true, ws, ws_bytes,
                   stream);
+}
+
+dsa_status_t dsa_sparse_attn_bwd_range(const dsa_config_t* cfg, const void* q,
+                                       const void* k, const void* v, const void* o,
+                                       const float* lse, const void* dO,
+                                       const int32_t* topk_idx, int64_t t_begin,
+                                       int64_t t_end, void* dq, float* dk_acc,
+                                       float* dv_acc, void* ws, size_t ws_bytes,
+                                       void* stream) {
+  dsa_status_t st = check_cfg(cfg, false, true);
+  if (st != DSA_OK) return st;
+  if (!valid_range(cfg, t_begin, t_end)) return DSA_ERR_INVALID_ARG;
+  if (t_end == t_begin) return DSA_OK;  // nothing is read or written
+  if (!q || !k || !v || !o || !lse || !dO || !topk_idx || !dq || !dk_acc)
+    return DSA_ERR_INVALID_ARG;
+  if (!dv_acc && v != k) return DSA_ERR_INVALID_ARG;  // one accumulator: K = V only
+  if ((st = check_ws(cfg, DSA_WS_BWD_ROWS, ws, ws_bytes)) != DSA_OK) return st;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) ||
+      !aligned16(lse) || !aligned16(dO) || !aligned16(topk_idx) || !aligned16(dq) ||
+      !aligned16(dk_acc) || (dv_acc && !aligned16(dv_acc)))
+    return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  AttnShape s = attn_shape(cfg);
+  s.t_lo = t_begin;
+  s.t_hi = t_end;
+  float* delta = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + kHeader);
+  return bwd_rows(ctx, s, q, k, v, o, lse, dO, topk_idx, dq, delta, dk_acc, dv_acc);
+}
+
+dsa_status_t dsa_accum_to_bf16(const float* acc, void* out, int64_t n, void* stream) {
+  if (n < 0 || (n & 3) != 0) return DSA_ERR_INVALID_ARG;
+  if (n == 0) return DSA_OK;
+  if (!acc || !out) return DSA_ERR_INVALID_ARG;
+  if (!aligned16(acc) || (reinterpret_cast<uintptr_t>(out) & 7u) != 0)
+    return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  dsa_status_t st = make_ctx(nullptr, stream, &ctx);
+  if (st != DSA_OK) return st;
+  return cuda_status(launch_f32_to_bf16(ctx, acc, static_cast<__nv_bfloat16*>(out), n));
+}
+
+namespace {
+
+// Which optional parts a step has, from its tensor set.
+struct StepKind {
+  bool kv;     // v == k: one tensor as keys and values
+  bool bwd;    // dO given: run the backward
+  bool gated;  // k_gate given: gated pools
+};
+
+dsa_status_t check_step_tensors(const dsa_step_tensors_t* t, bool device, StepKind* kind) {
+  if (!t) return DSA_ERR_INVALID_ARG;
+  if (!t->q_idx || !t->k_idx || !t->w || !t->q || !t->k || !t->v || !t->topk_idx ||
+      !t->o || !t->lse)
+    return DSA_ERR_INVALID_ARG;
+  kind->kv = t->v == t->k;
+  kind->bwd = t->dO != nullptr;
+  kind->gated = t->k_gate != nullptr;
+  if (kind->bwd && (!t->dq || !t->dk || (!kind->kv && !t->dv))) return DSA_ERR_INVALID_ARG;
+  if (device) {
+    const void* ps[] = {t->q_idx, t->k_idx, t->w, t->k_gate, t->q, t->k, t->v, t->dO,
+                        t->topk_idx, t->o, t->lse, t->dq, t->dk, t->dv};
+    for (const void* p : ps)
+      if (p && !aligned16(p)) return DSA_ERR_MISALIGNED;
+  }
+  return DSA_OK;
+}
+
+// Regions of a DSA_WS_STEP workspace: one header, then the indexer's
+// payload (pooled keys, score chunk), then the backward's (delta, dK, dV).
+struct StepRegions {
+  __nv_bfloat16* k_pool;
+  float* scores;
+  BwdRegions bwd;
+};
+StepRegions step_regions(const dsa_config_t* cfg, void* ws, bool kv) {
+  uint8_t* payload = static_cast<uint8_t*>(ws) + kHeader;
+  StepRegions r;
+  r.k_pool = index_k_pool(payload);
+  r.scores = index_scores(cfg, payload);
+  r.bwd = bwd_regions(cfg, payload + (ws_bytes_for(cfg, DSA_WS_INDEX) - kHeader), kv);
+  return r;
+}
+
+dsa_status_t check_step_common(const dsa_config_t* cfg, void* ws, size_t ws_bytes) {
+  dsa_status_t st = check_cfg(cfg, true, true);
+  if (st != DSA_OK) return st;
+  if ((uint64_t)chunk_rows(cfg) * (uint64_t)score_ld(cfg) * 4u > cfg->scratch_cap)
+    return DSA_ERR_SCRATCH_CAP;
+  return check_ws(cfg, DSA_WS_STEP, ws, ws_bytes);
+}
+
+// Events of one call, released when the call returns (a recorded event
+// that is still pending is released by CUDA once it completes).
+struct EventPool {
+  cudaEvent_t ev[320];
+  int n = 0;
+  ~EventPool() {
+    for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
+  }
+  // Record a new event on `from` and make `to` wait for it.
+  cudaError_t link(cudaStream_t from, cudaStream_t to) {
+    if (n == (int)(sizeof ev / sizeof ev[0])) return cudaErrorInvalidValue;
+    cudaError_t e = cudaEventCreateWithFlags(&ev[n], cudaEventDisableTiming);
+    if (e != cudaSuccess) return e;
+    cudaEvent_t x = ev[n++];
+    if ((e = cudaEventRecord(x, from)) != cudaSuccess) return e;
+    return cudaStreamWaitEvent(to, x, 0);
+  }
+};
+
+}  // namespace
+
+dsa_status_t dsa_step(const dsa_config_t* cfg, const dsa_step_tensors_t* dev, void* ws,
+                      size_t ws_bytes, void* stream) {
+  dsa_status_t st = check_step_common(cfg, ws, ws_bytes);
+  if (st != DSA_OK) return st;
+  StepKind kind;
+  if ((st = check_step_tensors(dev, true, &kind)) != DSA_OK) return st;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  const StepRegions r = step_regions(cfg, ws, kind.kv);
+  const int64_t S = cfg->seq_len;
+  if ((st = index_rows(ctx, cfg, dev->q_idx, dev->k_idx, dev->k_gate, dev->w, 0, S,
+                       dev->topk_idx, r.k_pool, r.scores)) != DSA_OK)
+    return st;
+  const AttnShape s = attn_shape(cfg);
+  if ((st = fwd_rows(ctx, s, dev->q, dev->k, dev->v, dev->topk_idx, dev->o, dev->lse)) !=
+      DSA_OK)
+    return st;
+  if (!kind.bwd) return DSA_OK;
+  cudaError_t e = launch_attn_bwd_zero(ctx, s, r.bwd.dk_acc, r.bwd.dv_acc);
+  if (e != cudaSuccess) return cuda_status(e);
+  if ((st = bwd_rows(ctx, s, dev->q, dev->k, dev->v, dev->o, dev->lse, dev->dO,
+                     dev->topk_idx, dev->dq, r.bwd.delta, r.bwd.dk_acc, r.bwd.dv_acc)) !=
+      DSA_OK)
+    return st;
+  return cuda_status(launch_attn_bwd_finalize(ctx, s, r.bwd.dk_acc, r.bwd.dv_acc,
+                                              static_cast<__nv_bfloat16*>(dev->dk),
+                                              static_cast<__nv_bfloat16*>(dev->dv)));
+}
+
+dsa_status_t dsa_step_host(const dsa_config_t* cfg, const dsa_step_tensors_t* host,
+                           const dsa_step_tensors_t* dev, int32_t n_chunks, void* ws,
+                           size_t ws_bytes, void* stream, void* h2d_stream,
+                           void* d2h_stream) {
+  dsa_status_t st = check_step_common(cfg, ws, ws_bytes);
+  if (st != DSA_OK) return st;
+  StepKind kh, kd;
+  if ((st = check_step_tensors(host, false, &kh)) != DSA_OK) return st;
+  if ((st = check_step_tensors(dev, true, &kd)) != DSA_OK) return st;
+  if (kh.kv != kd.kv || kh.bwd != kd.bwd || kh.gated != kd.gated)
+    return DSA_ERR_INVALID_ARG;  // the two tensor sets describe different steps
+  if (n_chunks < 1 || n_chunks > 64) return DSA_ERR_INVALID_ARG;
+  if (stream == h2d_stream || stream == d2h_stream || h2d_stream == d2h_stream)
+    return DSA_ERR_INVALID_ARG;
+  LaunchCtx ctx;
+  if ((st = make_ctx(ws, stream, &ctx)) != DSA_OK) return st;
+  const StepRegions r = step_regions(cfg, ws, kd.kv);
+  const cudaStream_t cs = ctx.stream;
+  const cudaStream_t hs = reinterpret_cast<cudaStream_t>(h2d_stream);
+  const cudaStream_t ds = reinterpret_cast<cudaStream_t>(d2h_stream);
+  const int64_t S = cfg->seq_len, H = cfg->attn_heads, D = cfg->d_qk;
+  const int64_t HI = cfg->idx_heads, DI = cfg->idx_dim, Kp = cfg->topk_pools;
+  const size_t q_row = (size_t)H * D * 2, lse_row = (size_t)H * 4;
+  // query ranges: equal shares rounded to multiples of 4 rows, which keeps
+  // every row-offset pointer 16-byte aligned
+  int64_t per = (S + n_chunks - 1) / n_chunks;
+  per = (per + 3) / 4 * 4;
+  EventPool ev;
+  cudaError_t e;
+  auto up = [&](void* d, const void* h, size_t bytes) {
+    return cudaMemcpyAsync(d, h, bytes, cudaMemcpyHostToDevice, hs);
+  };
+  auto down = [&](void* h, const void* d, size_t bytes) {
+    return cudaMemcpyAsync(h, d, bytes, cudaMemcpyDeviceToHost, ds);
+  };
+#define DSA_TRY(x)                                  \
+  do {                                              \
+    if ((e = (x)) != cudaSuccess) return cuda_status(e); \
+  } while (0)
+  // everything queued on `stream` before the call comes first
+  DSA_TRY(ev.link(cs, hs));
+  DSA_TRY(ev.link(cs, ds));
+  // ---- host -> device: indexer inputs, then K and V
+  DSA_TRY(up(dev->k_idx, host->k_idx, (size_t)S * DI * 2));
+  DSA_TRY(up(dev->q_idx, host->q_idx, (size_t)S * HI * DI * 2));
+  DSA_TRY(up(dev->w, host->w, (size_t)S * HI * 4));
+  if (kd.gated) DSA_TRY(up(dev->k_gate, host->k_gate, (size_t)S * 4));
+  DSA_TRY(ev.link(hs, cs));  // indexer inputs have landed
+  if (kd.bwd) DSA_TRY(launch_attn_bwd_zero(ctx, attn_shape(cfg), r.bwd.dk_acc, r.bwd.dv_acc));
+  if ((st = index_rows(ctx, cfg, dev->q_idx, dev->k_idx, dev->k_gate, dev->w, 0, S,
+                       dev->topk_idx, r.k_pool, r.scores)) != DSA_OK)
+    return st;
+  DSA_TRY(ev.link(cs, ds));  // the selection is final
+  DSA_TRY(down(host->topk_idx, dev->topk_idx, (size_t)S * Kp * 4));
+  DSA_TRY(up(dev->k, host->k, (size_t)S * D * 2));
+  if (!kd.kv) DSA_TRY(up(dev->v, host->v, (size_t)S * D * 2));
+  // ---- per query range: q (and dO) up, forward (and backward), rows down
+  for (int64_t t0 = 0; t0 < S; t0 += per) {
+    const int64_t t1 = t0 + per < S ? t0 + per : S, n = t1 - t0;
+    AttnShape s = attn_shape(cfg);
+    s.t_lo = t0;
+    s.t_hi = t1;
+    uint8_t* dq_rows = static_cast<uint8_t*>(dev->q) + t0 * q_row;
+    uint8_t* do_rows = kd.bwd ? static_cast<uint8_t*>(dev->dO) + t0 * q_row : nullptr;
+    uint8_t* o_rows = static_cast<uint8_t*>(dev->o) + t0 * q_row;
+    float* lse_rows = dev->lse + t0 * H;
+    int32_t* idx_rows = dev->topk_idx + t0 * Kp;
+    DSA_TRY(up(dq_rows, static_cast<const uint8_t*>(host->q) + t0 * q_row, n * q_row));
+    DSA_TRY(ev.link(hs, cs));  // K, V (first range) and this range's q
+    if ((st = fwd_rows(ctx, s, dq_rows, dev->k, dev->v, idx_rows, o_rows, lse_rows)) !=
+        DSA_OK)
+      return st;
+    DSA_TRY(ev.link(cs, ds));  // o and lse rows are final
+    DSA_TRY(down(static_cast<uint8_t*>(host->o) + t0 * q_row, o_rows, n * q_row));
+    DSA_TRY(down(host->lse + t0 * H, lse_rows, n * lse_row));
+    if (!kd.bwd) continue;
+    DSA_TRY(up(do_rows, static_cast<const uint8_t*>(host->dO) + t0 * q_row, n * q_row));
+    DSA_TRY(ev.link(hs, cs));  // this range's dO
+    uint8_t* dqr = static_cast<uint8_t*>(dev->dq) + t0 * q_row;
+    if ((st = bwd_rows(ctx, s, dq_rows, dev->k, dev->v, o_rows, lse_rows, do_rows,
+                       idx_rows, dqr, r.bwd.delta, r.bwd.dk_acc, r.bwd.dv_acc)) != DSA_OK)
+      return st;
+    DSA_TRY(ev.link(cs, ds));  // dq rows are final
+    DSA_TRY(down(static_cast<uint8_t*>(host->dq) + t0 * q_row, dqr, n * q_row));
+  }
+  if (kd.bwd) {
+    DSA_TRY(launch_attn_bwd_finalize(ctx, attn_shape(cfg), r.bwd.dk_acc, r.bwd.dv_acc,
+                                     static_cast<__nv_bfloat16*>(dev->dk),
+                                     static_cast<__nv_bfloat16*>(dev->dv)));
+    DSA_TRY(ev.link(cs, ds));
+    DSA_TRY(down(host->dk, dev->dk, (size_t)S * D * 2));
+    if (!kd.kv) DSA_TRY(down(host->dv, dev->dv, (size_t)S * D * 2));
+  }
+  // work queued on `stream` after the call waits for the last copy back
+  DSA_TRY(ev.link(ds, cs));
+#undef DSA_TRY
+  return DSA_OK;
 }
 
 dsa_status_t dsa_get_device_status(void* ws, void* stream, uint32_t* device_status) {

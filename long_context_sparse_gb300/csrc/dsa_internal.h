@@ -59,6 +59,10 @@ struct AttnShape {
   int K_p;
   int n_loc;
   float scale;
+  // queries [t_lo, t_hi) of the call; the per-query buffers (q, idx, o,
+  // lse, dO, dq, delta) hold those rows only, row r <-> query t_lo + r
+  int64_t t_lo = 0;
+  int64_t t_hi = 0;
 };
 
 // Heads per tensor-core tile (N) of the attention kernels: H, or 64 per
@@ -71,6 +75,16 @@ cudaError_t launch_attn_fwd_tc(const LaunchCtx& c, const AttnShape& s,
                                const CUtensorMap& q_map, const __nv_bfloat16* k,
                                const __nv_bfloat16* v, const int32_t* idx,
                                __nv_bfloat16* o, float* lse);
+
+// a7 for the call's query rows: delta = rowsum(dO * O); also restarts the
+// backward's work counter.
+cudaError_t launch_attn_bwd_delta(const LaunchCtx& c, const AttnShape& s,
+                                  const __nv_bfloat16* o, const __nv_bfloat16* dO,
+                                  float* delta);
+
+// Zero the fp32 dK/dV accumulators of all S keys (dv_acc may be nullptr).
+cudaError_t launch_attn_bwd_zero(const LaunchCtx& c, const AttnShape& s, float* dk_acc,
+                                 float* dv_acc);
 
 // a7: delta = rowsum(dO * O); zero the fp32 dK/dV accumulators (dv_acc may
 // be nullptr: one dKV accumulator).
@@ -88,6 +102,10 @@ cudaError_t launch_attn_bwd_tc(const LaunchCtx& c, const AttnShape& s,
                                const float* lse, const float* delta,
                                const int32_t* idx, __nv_bfloat16* dq, float* dk_acc,
                                float* dv_acc);
+
+// a9 on n values (n a multiple of 4, 16-byte aligned): bf16 round to nearest even.
+cudaError_t launch_f32_to_bf16(const LaunchCtx& c, const float* a, __nv_bfloat16* out,
+                               int64_t n);
 
 // a9: fp32 accumulators -> bf16 dK, dV.
 cudaError_t launch_attn_bwd_finalize(const LaunchCtx& c, const AttnShape& s,

@@ -122,3 +122,76 @@ def test_bad_pointers_and_sizes_fail_before_launch(lib):
                                    ctypes.c_void_p(4096), ws_bytes, None)
     assert rc == 8
     assert lib.dsa_get_device_status(None, None, None) == 1
+
+
+def test_range_and_step_workspace_sizes(lib):
+    c = _cfg()
+    assert dsa.workspace_size(c, dsa.WS_BWD_ROWS) == 256 + 16384 * 64 * 4
+    assert dsa.workspace_size(c, dsa.WS_STEP) == (
+        dsa.workspace_size(c, dsa.WS_INDEX) + dsa.workspace_size(c, dsa.WS_BWD) - 256)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.workspace_size(c, 7)
+    assert e.value.code == 1
+
+
+def _fake_step(base):
+    """A dsa_step_tensors_t of distinct, 256-byte aligned fake addresses
+    (never dereferenced: these calls fail in argument checking)."""
+    vals = [base + 4096 * i for i in range(len(dsa.STEP_FIELDS))]
+    return dsa._CStepTensors(*vals)
+
+
+def test_step_argument_checks_before_launch(lib):
+    c = _cfg()
+    cc = c.c()
+    wsb = dsa.workspace_size(c, dsa.WS_STEP)
+    host, dev = _fake_step(1 << 20), _fake_step(1 << 30)
+    ws = ctypes.c_void_p(1 << 40)
+    s0, s1, s2 = (ctypes.c_void_p(x) for x in (0x1000, 0x2000, 0x3000))
+
+    def call(h=host, d=dev, n=8, wsz=wsb, a=s0, b=s1, cc_=cc):
+        return lib.dsa_step_host(ctypes.byref(cc_), ctypes.byref(h), ctypes.byref(d),
+                                 n, ws, wsz, a, b, s2)
+    assert call(n=0) == 1 and call(n=65) == 1            # range count
+    assert call(a=s1) == 1 and call(b=s2) == 1            # streams must differ
+    assert call(wsz=wsb - 1) == 3                         # workspace too small
+    d_kv = _fake_step(1 << 30)
+    d_kv.v = d_kv.k                                       # device says K = V,
+    assert call(d=d_kv) == 1                              # host does not
+    d_fwd = _fake_step(1 << 30)
+    d_fwd.dO = None                                       # forward only on one side
+    assert call(d=d_fwd) == 1
+    d_mis = _fake_step(1 << 30)
+    d_mis.o = (1 << 30) + 8                               # misaligned device tensor
+    assert call(d=d_mis) == 4
+    h_null = _fake_step(1 << 20)
+    h_null.q = None
+    assert call(h=h_null) == 1
+    bad = _cfg(d_qk=576).c()
+    assert call(cc_=bad) == 2
+    assert lib.dsa_step(ctypes.byref(cc), ctypes.byref(d_mis), ws, wsb, s0) == 4
+
+
+def test_range_argument_checks_before_launch(lib):
+    c = _cfg()
+    cc = c.c()
+    p = ctypes.c_void_p(256)
+    wsf = ctypes.c_void_p(4096)
+    # t_end beyond S, t_begin after t_end
+    assert lib.dsa_sparse_attn_fwd_range(ctypes.byref(cc), p, p, p, p, 0, 16385, p, p,
+                                         wsf, 256, None) == 1
+    assert lib.dsa_sparse_attn_fwd_range(ctypes.byref(cc), p, p, p, p, 9, 8, p, p, wsf,
+                                         256, None) == 1
+    # an empty range touches nothing, whatever the pointers
+    assert lib.dsa_sparse_attn_fwd_range(ctypes.byref(cc), None, None, None, None, 5, 5,
+                                         None, None, None, 0, None) == 0
+    rows = dsa.workspace_size(c, dsa.WS_BWD_ROWS)
+    args = [p] * 7
+    # one accumulator needs v == k
+    assert lib.dsa_sparse_attn_bwd_range(ctypes.byref(cc), p, p, ctypes.c_void_p(512),
+                                         p, p, p, p, 0, 8, p, p, None, wsf, rows,
+                                         None) == 1
+    assert lib.dsa_sparse_attn_bwd_range(ctypes.byref(cc), *args, 0, 8, p, p, p, wsf,
+                                         rows - 1, None) == 3
+    assert lib.dsa_accum_to_bf16(p, p, 6, None) == 1      # not a multiple of 4
+    assert lib.dsa_accum_to_bf16(ctypes.c_void_p(260), p, 8, None) == 4

@@ -443,3 +443,163 @@ def test_unsupported_shapes_raise_before_launch():
     with pytest.raises(dsa.DsaError) as e:
         dsa.workspace(_cfg(wl, d_qk=576, d_v=512), dsa.WS_FWD, DEV)
     assert e.value.code == 2
+
+
+# ------------------------------------------- query ranges and whole steps
+
+
+def _close_bf16(got, ref):
+    """Equal up to one bf16 rounding: fp32 sums accumulated in another
+    order can straddle a rounding boundary."""
+    g, r = f64(got), f64(ref)
+    scale = np.abs(r).max() if r.size else 0.0
+    assert np.all(np.abs(g - r) <= 2.0 ** -7 * np.abs(r) + 2.0 ** -20 * scale)
+    assert np.mean(g == r) > 0.9
+
+
+@pytest.mark.parametrize("name,S,over,cuts", [
+    ("glm_s16k", 3000, {}, [0, 1000, 1004, 1004, 2999, 3000]),
+    ("tiny_fwd_s1k", 77, dict(K_p=5, n_loc=3), [0, 12, 77]),  # 16-byte rows
+    ("glm_s16k", 300, dict(H=80), [0, 150, 300]),     # two head blocks
+    ("padded2051_s64k", 1100, {}, [0, 512, 1100]),    # 16 heads, 2051 keys
+])
+def test_attn_ranges_equal_whole_call(name, S, over, cuts):
+    """Forward rows and dq rows of range calls are bit-identical to the
+    whole-sequence call's; the fp32 dK/dV contributions of ranges that
+    partition the queries add up to the whole call's dK/dV."""
+    wl, q, k, v, dO, idx = _attn_case(name, S, 31, **over)
+    cfg = _cfg(wl)
+    qd, kd, vd, dOd, idd = (x.to(DEV) for x in (q, k, v, dO, idx))
+    o, lse = dsa.sparse_attn_fwd(cfg, qd, kd, vd, idd)
+    dq, dk, dv = dsa.sparse_attn_bwd(cfg, qd, kd, vd, o, lse, dOd, idd)
+    dk_acc = torch.zeros((S, cfg.d_qk), dtype=torch.float32, device=DEV)
+    dv_acc = torch.zeros_like(dk_acc)
+    wsf = dsa.workspace(cfg, dsa.WS_FWD, DEV)
+    wsr = dsa.workspace(cfg, dsa.WS_BWD_ROWS, DEV)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        o_r, lse_r = dsa.sparse_attn_fwd_range(cfg, qd[a:b], kd, vd, idd[a:b], a, b,
+                                               ws=wsf)
+        dq_r = dsa.sparse_attn_bwd_range(cfg, qd[a:b], kd, vd, o_r, lse_r, dOd[a:b],
+                                         idd[a:b], a, b, dk_acc, dv_acc, ws=wsr)
+        torch.cuda.synchronize()
+        assert torch.equal(o_r, o[a:b]) and torch.equal(lse_r, lse[a:b]), (a, b)
+        assert torch.equal(dq_r, dq[a:b]), (a, b)
+    _status_ok(wsf)
+    _status_ok(wsr)
+    _close_bf16(dsa.accum_to_bf16(dk_acc), dk)
+    _close_bf16(dsa.accum_to_bf16(dv_acc), dv)
+    # K = V: one accumulator receives dK + dV
+    o2, lse2 = dsa.sparse_attn_fwd_kv(cfg, qd, kd, idd)
+    _, dkv = dsa.sparse_attn_bwd_kv(cfg, qd, kd, o2, lse2, dOd, idd)
+    acc = torch.zeros_like(dk_acc)
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        dsa.sparse_attn_bwd_range(cfg, qd[a:b], kd, kd, o2[a:b], lse2[a:b], dOd[a:b],
+                                  idd[a:b], a, b, acc, None, ws=wsr)
+    _close_bf16(dsa.accum_to_bf16(acc), dkv)
+
+
+def test_attn_bwd_range_rejects_one_accumulator_for_separate_kv():
+    wl, q, k, v, dO, idx = _attn_case("tiny_fwd_s1k", 64, 3)
+    cfg = _cfg(wl)
+    qd, kd, vd, dOd, idd = (x.to(DEV) for x in (q, k, v, dO, idx))
+    o, lse = dsa.sparse_attn_fwd(cfg, qd, kd, vd, idd)
+    acc = torch.zeros((64, cfg.d_qk), dtype=torch.float32, device=DEV)
+    with pytest.raises(dsa.DsaError) as e:
+        dsa.sparse_attn_bwd_range(cfg, qd, kd, vd, o, lse, dOd, idd, 0, 64, acc, None)
+    assert e.value.code == 1
+
+
+def _step_tensors(wl, seed, gated=False, kv=False, backward=True):
+    q_idx, k_idx, w = synth.indexer_inputs(wl, seed, "cpu")
+    q, k, v, dO = synth.attention_inputs(wl, seed, "cpu")
+    x = {"q_idx": q_idx, "k_idx": k_idx, "w": w, "q": q, "k": k}
+    if not kv:
+        x["v"] = v
+    if gated:
+        x["k_gate"] = synth.gate_inputs(wl, seed, "cpu")
+    if backward:
+        x["dO"] = dO
+    return x
+
+
+def _step_outputs(cfg, shapes, like, device):
+    out = {}
+    for name in ("topk_idx", "o", "lse", "dq", "dk", "dv"):
+        if name in shapes:
+            shape, dtype = shapes[name]
+            out[name] = torch.empty(shape, dtype=dtype, device=device,
+                                    pin_memory=device == "cpu")
+    return out
+
+
+@pytest.mark.parametrize("S,gated,kv,backward", [
+    (3000, False, False, True),
+    (2500, True, False, True),
+    (2000, False, True, True),
+    (1800, False, False, False),
+])
+def test_step_equals_separate_calls(S, gated, kv, backward):
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], S)
+    cfg = _cfg(wl)
+    x = {n: t.to(DEV) for n, t in _step_tensors(wl, 41, gated, kv, backward).items()}
+    shapes = dsa.step_shapes(cfg, kv, backward, gated)
+    dev = dict(x, **_step_outputs(cfg, shapes, x, DEV))
+    ws = dsa.workspace(cfg, dsa.WS_STEP, DEV)
+    dsa.step(cfg, dev, ws=ws)
+    _status_ok(ws)
+    if gated:
+        idx = dsa.index_scores_topk_range(cfg, x["q_idx"], x["k_idx"], x["w"], 0, S,
+                                          k_gate=x["k_gate"])
+    else:
+        idx = dsa.index_scores_topk(cfg, x["q_idx"], x["k_idx"], x["w"])
+    v = x["k"] if kv else x["v"]
+    o, lse = dsa.sparse_attn_fwd(cfg, x["q"], x["k"], v, idx)
+    torch.cuda.synchronize()
+    assert torch.equal(dev["topk_idx"], idx)
+    assert torch.equal(dev["o"], o) and torch.equal(dev["lse"], lse)
+    if not backward:
+        return
+    if kv:
+        dq, dkv = dsa.sparse_attn_bwd_kv(cfg, x["q"], x["k"], o, lse, x["dO"], idx)
+        _close_bf16(dev["dk"], dkv)
+    else:
+        dq, dk, dv = dsa.sparse_attn_bwd(cfg, x["q"], x["k"], v, o, lse, x["dO"], idx)
+        _close_bf16(dev["dk"], dk)
+        _close_bf16(dev["dv"], dv)
+    assert torch.equal(dev["dq"], dq)
+
+
+@pytest.mark.parametrize("S,n_chunks,gated,kv,backward", [
+    (3000, 1, False, False, True),
+    (3000, 3, False, False, True),
+    (16384, 8, False, False, True),           # the 16k configuration, 8 ranges
+    (2049, 64, True, False, True),            # more ranges than CTAs per range
+    (2000, 5, False, True, True),
+    (1800, 4, False, False, False),
+])
+def test_step_host_equals_device_step(S, n_chunks, gated, kv, backward):
+    """Inputs from pinned host memory, outputs back to it, copies overlapped
+    with the kernels on side streams: the same results as dsa_step."""
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], S)
+    cfg = _cfg(wl)
+    shapes = dsa.step_shapes(cfg, kv, backward, gated)
+    inp = _step_tensors(wl, 43, gated, kv, backward)
+    host = {n: t.pin_memory() for n, t in inp.items()}
+    host.update(_step_outputs(cfg, shapes, host, "cpu"))
+    dev = {n: torch.empty(shape, dtype=dtype, device=DEV)
+           for n, (shape, dtype) in shapes.items()}
+    ws = dsa.workspace(cfg, dsa.WS_STEP, DEV)
+    dsa.step_host(cfg, host, dev, n_chunks, ws=ws)
+    torch.cuda.synchronize()
+    _status_ok(ws)
+    ref = {n: t.to(DEV) for n, t in inp.items()}
+    ref.update(_step_outputs(cfg, shapes, ref, DEV))
+    dsa.step(cfg, ref, ws=ws)
+    torch.cuda.synchronize()
+    _status_ok(ws)
+    for name in ("topk_idx", "o", "lse") + (("dq",) if backward else ()):
+        assert torch.equal(host[name], ref[name].cpu()), name
+    if backward:
+        _close_bf16(host["dk"], ref["dk"].cpu())
+        if not kv:
+            _close_bf16(host["dv"], ref["dv"].cpu())
