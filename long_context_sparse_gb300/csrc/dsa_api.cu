@@ -729,7 +729,7 @@ dsa_status_t check_step_common(const dsa_config_t* cfg, void* ws, size_t ws_byte
 // Events of one call, released when the call returns (a recorded event
 // that is still pending is released by CUDA once it completes).
 struct EventPool {
-  cudaEvent_t ev[320];
+  cudaEvent_t ev[6 * 64 + 8];  // 6 per query range + 4 (at most 64 ranges)
   int n = 0;
   ~EventPool() {
     for (int i = 0; i < n; ++i) cudaEventDestroy(ev[i]);
@@ -818,18 +818,25 @@ dsa_status_t dsa_step_host(const dsa_config_t* cfg, const dsa_step_tensors_t* ho
   // everything queued on `stream` before the call comes first
   DSA_TRY(ev.link(cs, hs));
   DSA_TRY(ev.link(cs, ds));
-  // ---- host -> device: indexer inputs, then K and V
+  if (kd.bwd) DSA_TRY(launch_attn_bwd_zero(ctx, attn_shape(cfg), r.bwd.dk_acc, r.bwd.dv_acc));
+  // ---- the indexer, range by range as each range's q_idx rows land (the
+  // keys and weights first: every range pools all keys)
   DSA_TRY(up(dev->k_idx, host->k_idx, (size_t)S * DI * 2));
-  DSA_TRY(up(dev->q_idx, host->q_idx, (size_t)S * HI * DI * 2));
   DSA_TRY(up(dev->w, host->w, (size_t)S * HI * 4));
   if (kd.gated) DSA_TRY(up(dev->k_gate, host->k_gate, (size_t)S * 4));
-  DSA_TRY(ev.link(hs, cs));  // indexer inputs have landed
-  if (kd.bwd) DSA_TRY(launch_attn_bwd_zero(ctx, attn_shape(cfg), r.bwd.dk_acc, r.bwd.dv_acc));
-  if ((st = index_rows(ctx, cfg, dev->q_idx, dev->k_idx, dev->k_gate, dev->w, 0, S,
-                       dev->topk_idx, r.k_pool, r.scores)) != DSA_OK)
-    return st;
-  DSA_TRY(ev.link(cs, ds));  // the selection is final
-  DSA_TRY(down(host->topk_idx, dev->topk_idx, (size_t)S * Kp * 4));
+  const size_t qi_row = (size_t)HI * DI * 2;
+  for (int64_t t0 = 0; t0 < S; t0 += per) {
+    const int64_t t1 = t0 + per < S ? t0 + per : S, n = t1 - t0;
+    DSA_TRY(up(static_cast<uint8_t*>(dev->q_idx) + t0 * qi_row,
+               static_cast<const uint8_t*>(host->q_idx) + t0 * qi_row, n * qi_row));
+    DSA_TRY(ev.link(hs, cs));  // keys, weights and this range's q_idx
+    if ((st = index_rows(ctx, cfg, static_cast<const uint8_t*>(dev->q_idx) + t0 * qi_row,
+                         dev->k_idx, dev->k_gate, dev->w + t0 * HI, t0, t1,
+                         dev->topk_idx + t0 * Kp, r.k_pool, r.scores)) != DSA_OK)
+      return st;
+    DSA_TRY(ev.link(cs, ds));  // this range's selection is final
+    DSA_TRY(down(host->topk_idx + t0 * Kp, dev->topk_idx + t0 * Kp, n * Kp * 4));
+  }
   DSA_TRY(up(dev->k, host->k, (size_t)S * D * 2));
   if (!kd.kv) DSA_TRY(up(dev->v, host->v, (size_t)S * D * 2));
   // ---- per query range: q (and dO) up, forward (and backward), rows down

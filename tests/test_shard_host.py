@@ -80,3 +80,51 @@ def test_sharded_selection_on_two_gloo_ranks_equals_unsharded(tmp_path):
     q_idx, k_idx, w = synth.indexer_inputs(wl, 5, "cpu")
     ref, _ = oracle.index_topk(bits(q_idx), bits(k_idx), w.numpy(), K_p)
     np.testing.assert_array_equal(gathered, ref)
+
+
+def _attn_rank_main(rank, world, port, S, out_path):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        wl = synth.scaled(synth.WORKLOADS["tiny_fwd_s1k"], S, K_p=8, n_loc=3)
+        q, k, v, dO = synth.attention_inputs(wl, 7, "cpu")
+        idx = synth.random_selection(wl, 7, "cpu").numpy()
+        scale = 1.0 / np.sqrt(wl.d_qk)
+        t0, t1 = dsa.query_shard(S, world, rank)
+        rows = np.arange(t0, t1, dtype=np.int64)
+        # this rank's queries: dq rows, and partial dK/dV over every key
+        dq, dk, dv = oracle.attn_bwd(bits(q)[rows], bits(k), bits(v), bits(dO)[rows],
+                                     idx, wl.K_p, wl.n_loc, scale, rows)
+        part = torch.from_numpy(np.concatenate([dk, dv], axis=1))
+        dist.all_reduce(part)                 # the exchange: a sum over ranks
+        n_max = max(b - a for a, b in (dsa.query_shard(S, world, r)
+                                       for r in range(world)))
+        buf = torch.zeros((n_max,) + dq.shape[1:], dtype=torch.float64)
+        buf[: t1 - t0] = torch.from_numpy(dq)
+        parts = [torch.empty_like(buf) for _ in range(world)]
+        dist.all_gather(parts, buf)
+        if rank == 0:
+            full_dq = torch.cat([p[: b - a] for p, (a, b) in zip(
+                parts, (dsa.query_shard(S, world, r) for r in range(world)))])
+            np.savez(out_path, dq=full_dq.numpy(), dkv=part.numpy())
+    finally:
+        dist.destroy_process_group()
+
+
+def test_query_sharded_attention_backward_on_two_gloo_ranks(tmp_path):
+    """Attention backward split by query (the form of
+    dsa_sparse_attn_bwd_range): per-rank dq rows gathered and per-rank
+    partial dK/dV summed over ranks equal the unsharded backward."""
+    S, world = 203, 2
+    out = str(tmp_path / "bwd.npz")
+    mp.spawn(_attn_rank_main, args=(world, _free_port(), S, out), nprocs=world,
+             join=True)
+    got = np.load(out)
+    wl = synth.scaled(synth.WORKLOADS["tiny_fwd_s1k"], S, K_p=8, n_loc=3)
+    q, k, v, dO = synth.attention_inputs(wl, 7, "cpu")
+    idx = synth.random_selection(wl, 7, "cpu").numpy()
+    dq, dk, dv = oracle.attn_bwd(bits(q), bits(k), bits(v), bits(dO), idx, wl.K_p,
+                                 wl.n_loc, 1.0 / np.sqrt(wl.d_qk))
+    np.testing.assert_array_equal(got["dq"], dq)      # row-local: exact
+    ref = np.concatenate([dk, dv], axis=1)
+    assert np.allclose(got["dkv"], ref, rtol=1e-12, atol=1e-14 * np.abs(ref).max())
