@@ -57,10 +57,6 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
   return true;
 }
 
-__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
-
 template <int HI, int DI>
 __global__ void __launch_bounds__(kThreads, 1)
     indexer_kernel(const __grid_constant__ CUtensorMap q_map,

@@ -10,7 +10,10 @@
 // (same page, sections "DeepSeek Sparse Attention (DSA) Optimizations" and
 // "Across GPUs: Sharding").  Exact radix select on an order-preserving u32
 // image of the fp32 score, then one index-ordered compaction pass: the
-// result is bit-identical to a stable sort on (score desc, index asc).
+// result is bit-identical to a stable sort on (score desc, index asc).  A
+// cut placed from evenly spaced samples first shrinks a long row to the few
+// thousand candidates that can matter (checked, not assumed: a row where
+// fewer than K_p keys pass the cut is selected in full).
 #include "index_common.cuh"
 #include "dsa_internal.h"
 
@@ -105,25 +108,24 @@ cudaError_t launch_pool_gated(const LaunchCtx& c, const __nv_bfloat16* k_idx,
 // ----------------------------------------------------------------- top-k
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
-// Rows of up to this many candidates are staged in shared memory once.
-constexpr int kTopkCacheMax = 48 * 1024;
-constexpr int kBins = 2048;  // 11-bit digits: bits 31-21, 20-10, 9-0
+constexpr int kBins = 2048;     // 11-bit digits: bits 31-21, 20-10, 9-0
+constexpr int kSub = 256;                 // candidate slots of one warp
+constexpr int kCand = kSub * kTopkWarps;  // candidate (key, pool) slots of a row
+constexpr int kSamples = 1024;            // evenly spaced keys that place the cut
 
 // Digit d of the highest bins that holds the kk-th largest key; *above =
 // number of keys in higher bins.  Warp 0 only: lane l first sums the 64
-// bins kBins-64(l+1) .. kBins-64l-1 (lane 0: the top 64), a warp scan finds
-// the lane whose range holds the kk-th key, then the whole warp scans that
-// range two bins per lane, highest first.
+// bins kBins-64(l+1) .. kBins-64l-1 (lane 0: the top 64), starting at its
+// own offset l so that the 32 lanes read 32 different banks; a warp scan
+// finds the lane whose range holds the kk-th key, then the whole warp scans
+// that range two bins per lane, highest first.
 __device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t kk,
                                            uint32_t* sel_digit, uint32_t* sel_above) {
   const int lane = threadIdx.x & 31;
   const int base = kBins - 64 * (lane + 1);
   uint32_t s = 0u;
-#pragma unroll
-  for (int j = 0; j < 64; j += 4) {
-    const uint4 v = *reinterpret_cast<const uint4*>(hist + base + j);
-    s += v.x + v.y + v.z + v.w;
-  }
+#pragma unroll 16
+  for (int j = 0; j < 64; ++j) s += hist[base + ((j + lane) & 63)];
   uint32_t incl = s;
 #pragma unroll
   for (int d = 1; d < 32; d <<= 1) {
@@ -156,17 +158,135 @@ __device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t kk,
   }
 }
 
-__global__ void __launch_bounds__(kTopkThreads, 1)
-    topk_rows_kernel(const float* __restrict__ scores, int64_t ld, int64_t row0,
-                     int64_t rows, int K_p, int32_t* __restrict__ out,
-                     int cache_cap) {
-  extern __shared__ __align__(16) uint32_t cache[];
-  __shared__ __align__(16) uint32_t hist[kBins];
-  __shared__ uint32_t wcnt[2][kTopkWarps];
-  __shared__ uint32_t sel_digit, sel_above;
+// Shared state of one top-k CTA (static shared memory, ~45 KB; two CTAs of
+// 16 warps per SM, so the 256 rows of a score chunk run in one wave).
+// Candidates live in one sub-buffer per warp; warp w's sub-buffer holds
+// keys of a contiguous stretch of the row that precedes warp w+1's, so the
+// sub-buffers read in warp order are in pool order.
+struct TopkShared {
+  uint32_t hist[kBins];
+  uint32_t ckey[kCand];
+  int32_t cidx[kCand];
+  uint32_t samp[kSamples];
+  uint32_t cnt[kTopkWarps];  // entries of each sub-buffer
+  uint32_t wcnt[2][kTopkWarps];
+  uint32_t sel_digit, sel_above;
+};
 
+// The kk-th largest of a set of keys by radix select.  visit(f) calls
+// f(key) for each key this thread owns (every key exactly once over the
+// CTA).  The bits every key shares (the common prefix of the set's minimum
+// and maximum) are known at once; the rest are resolved in digits of up to
+// 11 bits from the top, so the first histogram spreads over many bins
+// (a set of close keys would otherwise pile onto one) and a narrow set
+// takes fewer passes.  *T = that key, *ties = how many keys equal to T rank
+// among the kk largest (ties broken by position).
+//
+// With max_passes = 1 the result is only a cut: *T is the lower edge of the
+// first digit's bin that holds the kk-th largest key (at least kk keys are
+// >= *T); *ties is then meaningless.
+template <class Visit>
+__device__ void radix_kth(Visit visit, uint32_t kk, TopkShared& sm, uint32_t* T,
+                          uint32_t* ties, int max_passes = 3) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t lane_lt = (1u << lane) - 1u;
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  visit([&](uint32_t key) {
+    lo = min(lo, key);
+    hi = max(hi, key);
+  });
+  lo = __reduce_min_sync(0xffffffffu, lo);
+  hi = __reduce_max_sync(0xffffffffu, hi);
+  if (lane == 0) {
+    sm.wcnt[0][warp] = lo;
+    sm.wcnt[1][warp] = hi;
+  }
+  __syncthreads();
+  for (int w = 0; w < kTopkWarps; ++w) {
+    lo = min(lo, sm.wcnt[0][w]);
+    hi = max(hi, sm.wcnt[1][w]);
+  }
+  const int L = hi == lo ? 32 : __clz(hi ^ lo);  // bits shared by every key
+  uint32_t pmask = L == 32 ? 0xffffffffu : ~(0xffffffffu >> L);
+  uint32_t prefix = hi & pmask;
+  int start = 32 - L;  // bits start-1 .. 0 are still open
+#pragma unroll 1
+  for (int pass = 0; start > 0 && pass < max_passes; ++pass) {
+    const int shift = start > 11 ? start - 11 : 0;
+    const uint32_t dmask = (1u << (start - shift)) - 1u;
+    for (int i = tid; i < kBins; i += kTopkThreads) sm.hist[i] = 0u;
+    __syncthreads();
+    visit([&](uint32_t key) {
+      if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & dmask], 1u);
+    });
+    __syncthreads();
+    if (warp == 0) find_digit(sm.hist, kk, &sm.sel_digit, &sm.sel_above);
+    __syncthreads();
+    prefix |= sm.sel_digit << shift;
+    pmask |= dmask << shift;
+    kk -= sm.sel_above;
+    start = shift;
+  }
+  __syncthreads();  // every thread has read the bounds and the digits
+  prefix &= pmask;  // (a cut: the bits below the resolved digits are zero)
+  *T = prefix;
+  *ties = kk;
+}
+
+// Index-ordered selection: keys above T, then the first `ties` keys equal
+// to T, each handed to emit(position, i) with its rank in order.  Warp w
+// owns the keys key_at(i), i in [b0, b1), a stretch that precedes warp
+// w+1's: one counting sweep, one exclusive sum over the warps, one emitting
+// sweep with ballots.
+template <class KeyAt, class Emit>
+__device__ void ordered_take(KeyAt key_at, int64_t b0, int64_t b1, uint32_t T,
+                             uint32_t ties, TopkShared& sm, Emit emit) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t lt = (1u << lane) - 1u;
+  uint32_t cg = 0u, ct = 0u;
+  for (int64_t i = b0 + lane; i < b1; i += 32) {
+    const uint32_t key = key_at(i);
+    cg += key > T;
+    ct += key == T;
+  }
+  cg = __reduce_add_sync(0xffffffffu, cg);
+  ct = __reduce_add_sync(0xffffffffu, ct);
+  if (lane == 0) {
+    sm.wcnt[0][warp] = cg;
+    sm.wcnt[1][warp] = ct;
+  }
+  __syncthreads();
+  uint32_t g = 0u, t = 0u;
+  for (int w = 0; w < warp; ++w) {
+    g += sm.wcnt[0][w];
+    t += sm.wcnt[1][w];
+  }
+  for (int64_t i0 = b0; i0 < b1; i0 += 32) {
+    const int64_t i = i0 + lane;
+    const uint32_t key = i < b1 ? key_at(i) : 0u;
+    const bool gt = i < b1 && key > T, eq = i < b1 && key == T;
+    const uint32_t bg = __ballot_sync(0xffffffffu, gt), bt = __ballot_sync(0xffffffffu, eq);
+    const uint32_t g_before = g + __popc(bg & lt), t_before = t + __popc(bt & lt);
+    if (gt) emit(g_before + min(t_before, ties), i);
+    else if (eq && t_before < ties) emit(g_before + t_before, i);
+    g += __popc(bg);
+    t += __popc(bt);
+  }
+  __syncthreads();  // wcnt is reused by the next call
+}
+
+// One CTA per query row (several resident per SM).  Exact whatever the
+// data: a cut T0 taken from evenly spaced samples keeps every key >= T0 as
+// a candidate, in pool order; when at least K_p keys pass and they fit,
+// the K_p-th largest key of the row is the K_p-th largest candidate and
+// the answer is read off the candidates.  Otherwise (a flat or skewed row)
+// the row is selected directly from global memory.
+__global__ void __launch_bounds__(kTopkThreads, 2)
+    topk_rows_kernel(const float* __restrict__ scores, int64_t ld, int64_t row0,
+                     int64_t rows, int K_p, int32_t* __restrict__ out) {
+  __shared__ TopkShared sm;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  uint32_t* my_key = sm.ckey + warp * kSub;
+  int32_t* my_idx = sm.cidx + warp * kSub;
 
   for (int64_t r = blockIdx.x; r < rows; r += gridDim.x) {
     const int64_t t = row0 + r;
@@ -174,214 +294,156 @@ __global__ void __launch_bounds__(kTopkThreads, 1)
     if (n > ld) n = ld;
     int32_t* o = out + r * (int64_t)K_p;
     const float* row = scores + r * ld;
-
     if (n <= K_p) {  // every earlier pool is selected
       for (int i = tid; i < K_p; i += kTopkThreads) o[i] = i < n ? i : -1;
       continue;
     }
-    const bool cached = n <= cache_cap;
-    // 16-byte rows (the library's own score chunks always are) are read as
-    // float4, four loads in flight per thread, so the first pass does not
-    // wait on one L2 round trip per element
-    const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
-    const int64_t n4 = vec ? n / 4 : 0;
-
-    // ---- radix select of the K_p-th largest key: digits of 11, 11, 10 bits
-    uint32_t prefix = 0u, pmask = 0u, kk = (uint32_t)K_p;
-#pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-      const uint32_t dmask = pass == 2 ? 1023u : 2047u;
-      for (int i = tid; i < kBins; i += kTopkThreads) hist[i] = 0u;
-      __syncthreads();
-      if (pass == 0) {
-        // first touch of the row: load, map, cache, count
-        const float4* row4 = reinterpret_cast<const float4*>(row);
-        const int64_t nb = (n4 + 4 * kTopkThreads - 1) / (4 * kTopkThreads);
-        for (int64_t bi = 0; bi < nb; ++bi) {
-          const int64_t b = bi * 4 * kTopkThreads + tid;
-          float4 x[4];
+    auto row_key = [&](int64_t i) { return order_key(__ldg(row + i)); };
+    bool ok = true;
+    if (n <= kCand) {
+      // ---- the whole row is the candidate set: warp w takes a stretch of
+      // at most kSub keys
+      const int64_t per = (n + kTopkWarps - 1) / kTopkWarps;
+      const int64_t b0 = warp * per < n ? warp * per : n;
+      const int64_t b1 = b0 + per < n ? b0 + per : n;
+      for (int64_t i = b0 + lane; i < b1; i += 32) {
+        my_key[i - b0] = row_key(i);
+        my_idx[i - b0] = (int32_t)i;
+      }
+      if (lane == 0) sm.cnt[warp] = (uint32_t)(b1 - b0);
+    } else {
+      // ---- the cut: the lower edge of the first-digit bin that holds the
+      // rank-th largest of kSamples evenly spaced keys, rank chosen so that
+      // about K_p (1 + 4/sqrt(a)) + 4 n/kSamples keys pass, a = K_p
+      // kSamples / n being the expected samples above the answer
+      {
+        float x[kSamples / kTopkThreads];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int64_t j = b + u * kTopkThreads;
-            x[u] = j < n4 ? __ldg(row4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int u = 0; u < kSamples / kTopkThreads; ++u)
+          x[u] = __ldg(row + (int64_t)(tid + u * kTopkThreads) * n / kSamples);
+#pragma unroll
+        for (int u = 0; u < kSamples / kTopkThreads; ++u)
+          sm.samp[tid + u * kTopkThreads] = order_key(x[u]);
+      }
+      const float a = (float)K_p * (float)kSamples / (float)n;
+      uint32_t rank = (uint32_t)ceilf(a + 4.f * sqrtf(a) + 4.f);
+      if (rank > (uint32_t)kSamples) rank = kSamples;
+      uint32_t T0, ties0;
+      radix_kth(
+          [&](auto f) {
+            for (int j = tid; j < kSamples; j += kTopkThreads) f(sm.samp[j]);
+          },
+          rank, sm, &T0, &ties0, 1);
+      // ---- one sweep: warp w appends the keys >= T0 of its stretch (whole
+      // 512-key blocks, four float4 loads in flight per lane) to its own
+      // sub-buffer, in order
+      constexpr int kU = 4;
+      const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
+      const int64_t nblk = (n + 128 * kU - 1) / (128 * kU);
+      const int64_t bpw = (nblk + kTopkWarps - 1) / kTopkWarps;
+      const int64_t b0 = warp * bpw * 128 * kU < n ? warp * bpw * 128 * kU : n;
+      const int64_t b1 = b0 + bpw * 128 * kU < n ? b0 + bpw * 128 * kU : n;
+      // keys i0 + 128u + 4 lane + e of a 512-key block (zero past b1)
+      auto load_block = [&](int64_t i0, float4 (&f)[kU]) {
+        if (vec && i0 + 128 * kU <= b1) {
+#pragma unroll
+          for (int u = 0; u < kU; ++u)
+            f[u] = __ldg(reinterpret_cast<const float4*>(row + i0 + 128 * u + 4 * lane));
+        } else {
+#pragma unroll
+          for (int u = 0; u < kU; ++u) {
+            const int64_t i = i0 + 128 * u + 4 * lane;
+            f[u].x = i < b1 ? __ldg(row + i) : 0.f;
+            f[u].y = i + 1 < b1 ? __ldg(row + i + 1) : 0.f;
+            f[u].z = i + 2 < b1 ? __ldg(row + i + 2) : 0.f;
+            f[u].w = i + 3 < b1 ? __ldg(row + i + 3) : 0.f;
           }
+        }
+      };
+      const uint32_t lt = (1u << lane) - 1u;
+      uint32_t c = 0u;
+      float4 cur[kU], nxt[kU];
+      if (b0 < b1) load_block(b0, cur);
+      for (int64_t i0 = b0; i0 < b1; i0 += 128 * kU) {
+        if (i0 + 128 * kU < b1) load_block(i0 + 128 * kU, nxt);  // in flight meanwhile
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int64_t j = b + u * kTopkThreads;
-            const bool in = j < n4;
-            const uint32_t k4[4] = {order_key(x[u].x), order_key(x[u].y),
-                                    order_key(x[u].z), order_key(x[u].w)};
-            if (cached && in)
-              *reinterpret_cast<uint4*>(cache + 4 * j) = make_uint4(k4[0], k4[1], k4[2], k4[3]);
-            if (in) {
+        for (int u = 0; u < kU; ++u) {
+          const int64_t i = i0 + 128 * u + 4 * lane;
+          const uint32_t k0 = order_key(cur[u].x), k1 = order_key(cur[u].y),
+                         k2 = order_key(cur[u].z), k3 = order_key(cur[u].w);
+          const bool p0 = i < b1 && k0 >= T0, p1 = i + 1 < b1 && k1 >= T0,
+                     p2 = i + 2 < b1 && k2 >= T0, p3 = i + 3 < b1 && k3 >= T0;
+          const uint32_t q0 = __ballot_sync(0xffffffffu, p0), q1 = __ballot_sync(0xffffffffu, p1),
+                         q2 = __ballot_sync(0xffffffffu, p2), q3 = __ballot_sync(0xffffffffu, p3);
+          if ((q0 | q1 | q2 | q3) == 0u) continue;  // the usual case: nothing passes
+          // keys of earlier lanes first, then this lane's in order
+          uint32_t pos = c + __popc(q0 & lt) + __popc(q1 & lt) + __popc(q2 & lt) +
+                         __popc(q3 & lt);
+          const uint32_t kk4[4] = {k0, k1, k2, k3};
+          const bool pp4[4] = {p0, p1, p2, p3};
 #pragma unroll
-              for (int e = 0; e < 4; ++e) atomicAdd(&hist[k4[e] >> 21], 1u);
+          for (int e = 0; e < 4; ++e) {
+            if (pp4[e]) {
+              if (pos < (uint32_t)kSub) {
+                my_key[pos] = kk4[e];
+                my_idx[pos] = (int32_t)(i + e);
+              }
+              ++pos;
             }
           }
+          c += __popc(q0) + __popc(q1) + __popc(q2) + __popc(q3);
         }
-        for (int64_t i = 4 * n4 + tid; i < n; i += kTopkThreads) {
-          const uint32_t key = order_key(__ldg(row + i));
-          if (cached) cache[i] = key;
-          atomicAdd(&hist[key >> 21], 1u);
-        }
-      } else if (cached) {
-        for (int64_t i = tid; i < n; i += kTopkThreads) {
-          const uint32_t key = cache[i];
-          if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
-        }
-      } else {
-        const float4* row4 = reinterpret_cast<const float4*>(row);
-        for (int64_t b = tid; b < n4; b += 4 * kTopkThreads) {
-          float4 x[4];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int64_t j = b + u * kTopkThreads;
-            x[u] = j < n4 ? __ldg(row4 + j) : make_float4(0.f, 0.f, 0.f, 0.f);
-          }
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            if (b + u * kTopkThreads >= n4) continue;
-            const uint32_t k4[4] = {order_key(x[u].x), order_key(x[u].y),
-                                    order_key(x[u].z), order_key(x[u].w)};
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              if ((k4[e] & pmask) == prefix) atomicAdd(&hist[(k4[e] >> shift) & dmask], 1u);
-          }
-        }
-        for (int64_t i = 4 * n4 + tid; i < n; i += kTopkThreads) {
-          const uint32_t key = order_key(__ldg(row + i));
-          if ((key & pmask) == prefix) atomicAdd(&hist[(key >> shift) & dmask], 1u);
-        }
+        for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
       }
+      if (lane == 0) sm.cnt[warp] = c;
       __syncthreads();
-      if (warp == 0) find_digit(hist, kk, &sel_digit, &sel_above);
-      __syncthreads();
-      prefix |= sel_digit << shift;
-      pmask |= dmask << shift;
-      kk -= sel_above;
-    }
-    // prefix = key of the K_p-th best; take every key above it and the kk
-    // lowest-index keys equal to it, in index order.  Each warp owns one
-    // contiguous segment of whole 128-key blocks (lane l: keys 4l .. 4l+3
-    // of a block): count, one block-wide exclusive scan, then write with a
-    // warp scan per block.
-    const uint32_t T = prefix;
-    const float4* row4 = reinterpret_cast<const float4*>(row);
-    auto keys4 = [&](int64_t i, int64_t lim, uint32_t (&kq)[4]) {
-      if (i + 3 < lim && (cached || vec)) {
-        if (cached) {
-          const uint4 c4 = *reinterpret_cast<const uint4*>(cache + i);
-          kq[0] = c4.x; kq[1] = c4.y; kq[2] = c4.z; kq[3] = c4.w;
-        } else {
-          const float4 f4 = __ldg(row4 + (i >> 2));
-          kq[0] = order_key(f4.x); kq[1] = order_key(f4.y);
-          kq[2] = order_key(f4.z); kq[3] = order_key(f4.w);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          kq[e] = i + e < lim ? (cached ? cache[i + e] : order_key(__ldg(row + i + e))) : 0u;
+      uint32_t total = 0u;
+      for (int w = 0; w < kTopkWarps; ++w) {
+        total += sm.cnt[w];
+        ok = ok && sm.cnt[w] <= (uint32_t)kSub;
       }
-    };
-    const int64_t nblk = (n + 127) / 128;
-    const int64_t bpw = (nblk + kTopkWarps - 1) / kTopkWarps;
-    const int64_t b0 = warp * bpw * 128;
-    const int64_t b1 = b0 + bpw * 128 < n ? b0 + bpw * 128 : n;
-    uint32_t cg = 0u, ct = 0u;
-    for (int64_t i0 = b0; i0 < b1; i0 += 128) {
-      const int64_t i = i0 + 4 * lane;
-      uint32_t kq[4];
-      keys4(i, b1, kq);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool in = i + e < b1;
-        cg += in && kq[e] > T;
-        ct += in && kq[e] == T;
-      }
-    }
-    cg = __reduce_add_sync(0xffffffffu, cg);
-    ct = __reduce_add_sync(0xffffffffu, ct);
-    if (lane == 0) {
-      wcnt[0][warp] = cg;
-      wcnt[1][warp] = ct;
+      ok = ok && total >= (uint32_t)K_p;  // else the cut was too high
     }
     __syncthreads();
-    uint32_t g_base = 0u, t_base = 0u;
-#pragma unroll
-    for (int w = 0; w < kTopkWarps; ++w) {
-      if (w < warp) {
-        g_base += wcnt[0][w];
-        t_base += wcnt[1][w];
-      }
+    // (positions are < K_p by construction; the guards keep a row that
+    // changed under the kernel from writing into its neighbour)
+    uint32_t T, ties;
+    if (ok) {
+      const int mine = (int)sm.cnt[warp];  // each warp visits its own sub-buffer
+      radix_kth(
+          [&](auto f) {
+            for (int j = lane; j < mine; j += 32) f(my_key[j]);
+          },
+          (uint32_t)K_p, sm, &T, &ties);
+      ordered_take([&](int64_t j) { return my_key[j]; }, 0, sm.cnt[warp], T, ties, sm,
+                   [&](uint32_t pos, int64_t j) {
+                     if (pos < (uint32_t)K_p) o[pos] = my_idx[j];
+                   });
+    } else {
+      radix_kth(
+          [&](auto f) {
+            for (int64_t i = tid; i < n; i += kTopkThreads) f(row_key(i));
+          },
+          (uint32_t)K_p, sm, &T, &ties);
+      const int64_t per = (n + kTopkWarps - 1) / kTopkWarps;
+      const int64_t b0 = warp * per < n ? warp * per : n;
+      const int64_t b1 = b0 + per < n ? b0 + per : n;
+      ordered_take(row_key, b0, b1, T, ties, sm, [&](uint32_t pos, int64_t i) {
+        if (pos < (uint32_t)K_p) o[pos] = (int32_t)i;
+      });
     }
-    for (int64_t i0 = b0; i0 < b1; i0 += 128) {
-      if (t_base >= kk && g_base + kk >= (uint32_t)K_p) break;  // warp-uniform
-      const int64_t i = i0 + 4 * lane;
-      uint32_t kq[4];
-      keys4(i, b1, kq);
-      uint32_t gl = 0u, tl = 0u;
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const bool in = i + e < b1;
-        gl += in && kq[e] > T;
-        tl += in && kq[e] == T;
-      }
-      // (above, ties) counts packed as hi/lo 16 bits: at most 128 each
-      const uint32_t v = (gl << 16) | tl;
-      uint32_t incl = v;
-#pragma unroll
-      for (int d = 1; d < 32; d <<= 1) {
-        const uint32_t x = __shfl_up_sync(0xffffffffu, incl, d);
-        if (lane >= d) incl += x;
-      }
-      const uint32_t excl = incl - v;
-      uint32_t g_before = g_base + (excl >> 16), t_before = t_base + (excl & 0xFFFFu);
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        if (i + e >= b1) break;
-        // (positions are < K_p by construction; the guard keeps a corrupted
-        // row from writing into its neighbour)
-        if (kq[e] > T) {
-          const uint32_t pos = g_before + min(t_before, kk);
-          if (pos < (uint32_t)K_p) o[pos] = (int32_t)(i + e);
-          ++g_before;
-        } else if (kq[e] == T) {
-          if (t_before < kk && g_before + t_before < (uint32_t)K_p)
-            o[g_before + t_before] = (int32_t)(i + e);
-          ++t_before;
-        }
-      }
-      const uint32_t tot = __shfl_sync(0xffffffffu, incl, 31);
-      g_base += tot >> 16;
-      t_base += tot & 0xFFFFu;
-    }
-    __syncthreads();
   }
 }
 
 cudaError_t launch_topk(const LaunchCtx& c, const float* scores, int64_t ld,
                         int64_t row0, int64_t rows, int K_p, int32_t* out) {
   if (rows <= 0) return cudaSuccess;
-  int64_t nmax = n_full(row0 + rows - 1);
-  if (nmax > ld) nmax = ld;
-  int cache_cap = nmax <= kTopkCacheMax ? (int)nmax : 0;
-  const size_t smem = (size_t)cache_cap * sizeof(uint32_t);
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(topk_rows_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)(kTopkCacheMax * sizeof(uint32_t)));
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
   int64_t grid = rows;
-  const int64_t cap = (int64_t)c.num_sms * 8;
+  const int64_t cap = (int64_t)c.num_sms * 2;
   if (grid > cap) grid = cap;
-  topk_rows_kernel<<<(unsigned)grid, kTopkThreads, smem, c.stream>>>(
-      scores, ld, row0, rows, K_p, out, cache_cap);
+  topk_rows_kernel<<<(unsigned)grid, kTopkThreads, 0, c.stream>>>(scores, ld, row0, rows,
+                                                                  K_p, out);
   return cudaGetLastError();
 }
 
