@@ -356,6 +356,15 @@ DSA_API dsa_status_t dsa_index_scores_topk_static(const dsa_config_t* cfg,
 DSA_API dsa_status_t dsa_get_device_status(void* ws, void* stream,
                                    uint32_t* device_status);
 
+/* Check on this device that a bounded wait ends: one kernel thread waits,
+ * through the waiter every kernel of the library uses, on an mbarrier that
+ * nothing arrives on, for timeout_ms (1..10000) milliseconds, then latches
+ * DSA_ERR_DEVICE_TIMEOUT in the workspace status word (any workspace; read
+ * it with dsa_get_device_status) and returns.  Nothing faults or hangs and
+ * the context stays usable. */
+DSA_API dsa_status_t dsa_check_wait_timeout(void* ws, size_t ws_bytes, uint32_t timeout_ms,
+                                    void* stream);
+
 /* Static, human-readable name of a status code. */
 DSA_API const char* dsa_status_string(dsa_status_t status);
 

@@ -54,7 +54,7 @@ EXPORTS = [
     "dsa_pool_keys_gated", "dsa_sparse_attn_fwd_kv", "dsa_sparse_attn_bwd_kv",
     "dsa_index_topk_streaming", "dsa_sparse_attn_fwd_range",
     "dsa_sparse_attn_bwd_range", "dsa_accum_to_bf16", "dsa_step",
-    "dsa_step_host",
+    "dsa_step_host", "dsa_check_wait_timeout",
 ]
 
 
@@ -162,6 +162,7 @@ def _load():
             "dsa_sparse_attn_bwd_range": [CP, P, P, P, P, P, P, P, I64, I64,
                                           P, P, P, P, SZ, P],
             "dsa_accum_to_bf16": [P, P, I64, P],
+            "dsa_check_wait_timeout": [P, SZ, ctypes.c_uint32, P],
             "dsa_step": [CP, ctypes.POINTER(_CStepTensors), P, SZ, P],
             "dsa_step_host": [CP, ctypes.POINTER(_CStepTensors),
                               ctypes.POINTER(_CStepTensors), I32, P, SZ, P, P,
@@ -674,6 +675,16 @@ def step_host(cfg: Config, host: dict, dev: dict, n_chunks: int = 8, ws=None,
         _ptr(ws), ws.numel(), _stream(d), ctypes.c_void_p(hs.cuda_stream),
         ctypes.c_void_p(ds.cuda_stream)), "dsa_step_host")
     return host
+
+
+def check_wait_timeout(ws: torch.Tensor, timeout_ms: int = 50) -> None:
+    """Run the library's bounded-wait check: a kernel waits on an mbarrier
+    nothing arrives on for timeout_ms and latches DSA_ERR_DEVICE_TIMEOUT in
+    the status word of `ws` (read it with get_device_status)."""
+    _need(ws, "ws", torch.uint8)
+    _check(_load().dsa_check_wait_timeout(_ptr(ws), ws.numel(), int(timeout_ms),
+                                          _stream(ws.device)),
+           "dsa_check_wait_timeout")
 
 
 def get_device_status(ws: torch.Tensor) -> int:

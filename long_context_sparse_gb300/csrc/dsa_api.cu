@@ -227,6 +227,26 @@ void set_error_detail(const char* fmt, ...) {
   t_detail_set = true;
 }
 
+namespace {
+
+// One thread waits, through the same bounded waiter every kernel uses, on an
+// mbarrier that nothing arrives on: the wait must run out after timeout_ns,
+// latch DSA_ERR_DEVICE_TIMEOUT and return.
+__global__ void wait_timeout_kernel(uint32_t* status, uint64_t timeout_ns) {
+  __shared__ uint64_t bar;
+  __shared__ uint32_t abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0u;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const Waiter W{&abort_flag, status, timeout_ns};
+  if (threadIdx.x == 0) W.wait(smem_u32(&bar), 0);
+}
+
+}  // namespace
+
 }  // namespace dsa
 
 using namespace dsa;
@@ -880,6 +900,18 @@ dsa_status_t dsa_step_host(const dsa_config_t* cfg, const dsa_step_tensors_t* ho
   DSA_TRY(ev.link(ds, cs));
 #undef DSA_TRY
   return DSA_OK;
+}
+
+dsa_status_t dsa_check_wait_timeout(void* ws, size_t ws_bytes, uint32_t timeout_ms,
+                                    void* stream) {
+  if (!ws || ws_bytes < kHeader || timeout_ms < 1 || timeout_ms > 10000)
+    return DSA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return DSA_ERR_MISALIGNED;
+  LaunchCtx ctx;
+  dsa_status_t st = make_ctx(ws, stream, &ctx);
+  if (st != DSA_OK) return st;
+  wait_timeout_kernel<<<1, 32, 0, ctx.stream>>>(ctx.status, (uint64_t)timeout_ms * 1000000u);
+  return cuda_status(cudaGetLastError());
 }
 
 dsa_status_t dsa_get_device_status(void* ws, void* stream, uint32_t* device_status) {

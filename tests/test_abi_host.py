@@ -195,3 +195,45 @@ def test_range_argument_checks_before_launch(lib):
                                          rows - 1, None) == 3
     assert lib.dsa_accum_to_bf16(p, p, 6, None) == 1      # not a multiple of 4
     assert lib.dsa_accum_to_bf16(ctypes.c_void_p(260), p, 8, None) == 4
+
+
+def test_wait_timeout_check_arguments(lib):
+    ws = ctypes.c_void_p(1 << 20)
+    assert lib.dsa_check_wait_timeout(None, 256, 50, None) == 1
+    assert lib.dsa_check_wait_timeout(ws, 16, 50, None) == 1      # no header
+    assert lib.dsa_check_wait_timeout(ws, 256, 0, None) == 1
+    assert lib.dsa_check_wait_timeout(ws, 256, 10001, None) == 1
+    assert lib.dsa_check_wait_timeout(ctypes.c_void_p((1 << 20) + 16), 256, 50, None) == 4
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "dsa.h"
+int main(void) {
+  dsa_config_t c = {16384, 4, 512, 0, 32, 128, 64, 512, 512, 256, 0.0f, 2ull << 30};
+  size_t bytes = 0;
+  dsa_step_tensors_t t = {0};
+  if (dsa_abi_version() != DSA_ABI_VERSION) return 2;
+  if (dsa_workspace_size(&c, DSA_WS_STEP, &bytes) != DSA_OK || bytes == 0) return 3;
+  if (dsa_step(&c, &t, NULL, 0, NULL) != DSA_ERR_INVALID_ARG) return 4;
+  printf("%zu %s\n", bytes, dsa_status_string(DSA_ERR_SCRATCH_CAP));
+  return 0;
+}
+"""
+
+
+def test_header_is_c_and_a_c_program_links(lib, tmp_path):
+    """include/dsa.h compiles as C99 with warnings as errors, and a C
+    program linked against the library calls it (no GPU needed)."""
+    import subprocess
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    libdir = os.path.dirname(dsa.library_path())
+    subprocess.run(["gcc", "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic",
+                    "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe),
+                    "-L", libdir, "-ldsa_gb300", "-Wl,-rpath," + libdir], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout
+    size, name = out.split()
+    assert int(size) == dsa.workspace_size(_cfg(), dsa.WS_STEP)
+    assert name == "DSA_ERR_SCRATCH_CAP"

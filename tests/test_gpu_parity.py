@@ -603,3 +603,18 @@ def test_step_host_equals_device_step(S, n_chunks, gated, kv, backward):
         _close_bf16(host["dk"], ref["dk"].cpu())
         if not kv:
             _close_bf16(host["dv"], ref["dv"].cpu())
+
+
+def test_bounded_wait_times_out_and_the_context_survives():
+    """A wait that nothing satisfies ends after its limit with
+    DSA_ERR_DEVICE_TIMEOUT in the status word; the next calls run normally."""
+    wl = synth.scaled(synth.WORKLOADS["tiny_fwd_s1k"], 512)
+    cfg = _cfg(wl)
+    ws = dsa.workspace(cfg, dsa.WS_STATUS, DEV)
+    dsa.check_wait_timeout(ws, 50)
+    assert dsa.get_device_status(ws) == 6          # DSA_ERR_DEVICE_TIMEOUT
+    assert dsa.get_device_status(ws) == 0          # read and cleared
+    _, k_idx, _ = synth.indexer_inputs(wl, 1, "cpu")
+    got = dsa.pool_keys(cfg, k_idx.to(DEV))
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(bits(got), oracle.pool(bits(k_idx)))
