@@ -300,6 +300,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
     }
     auto row_key = [&](int64_t i) { return order_key(__ldg(row + i)); };
     bool ok = true;
+    int cb0, cb1;  // this warp's candidates: sm.ckey / sm.cidx [cb0, cb1)
     if (n <= kCand) {
       // ---- the whole row is the candidate set: warp w takes a stretch of
       // at most kSub keys
@@ -310,7 +311,8 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
         my_key[i - b0] = row_key(i);
         my_idx[i - b0] = (int32_t)i;
       }
-      if (lane == 0) sm.cnt[warp] = (uint32_t)(b1 - b0);
+      cb0 = warp * kSub;
+      cb1 = cb0 + (int)(b1 - b0);
     } else {
       // ---- the cut: the lower edge of the first-digit bin that holds the
       // rank-th largest of kSamples evenly spaced keys, rank chosen so that
@@ -336,7 +338,9 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
           rank, sm, &T0, &ties0, 1);
       // ---- one sweep: warp w appends the keys >= T0 of its stretch (whole
       // 512-key blocks, four float4 loads in flight per lane) to its own
-      // sub-buffer, in order
+      // sub-buffer, in order.  A stretch with more than kSub of them (a band
+      // of high scores in one place) is swept again once every warp's count
+      // is known, straight into its exact place in the flat array.
       constexpr int kU = 4;
       const bool vec = ((reinterpret_cast<uintptr_t>(row) & 15u) == 0);
       const int64_t nblk = (n + 128 * kU - 1) / (128 * kU);
@@ -361,11 +365,16 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
         }
       };
       const uint32_t lt = (1u << lane) - 1u;
+      // round 0 writes the first kSub passing keys of the stretch to the
+      // warp's sub-buffer; round 1 (only after a spill) all of them to their
+      // exact place in the flat array
+      uint32_t dbase = (uint32_t)(warp * kSub), cap = kSub;
+#pragma unroll 1
+      for (int round = 0; round < 2; ++round) {
       uint32_t c = 0u;
-      float4 cur[kU], nxt[kU];
-      if (b0 < b1) load_block(b0, cur);
       for (int64_t i0 = b0; i0 < b1; i0 += 128 * kU) {
-        if (i0 + 128 * kU < b1) load_block(i0 + 128 * kU, nxt);  // in flight meanwhile
+        float4 cur[kU];
+        load_block(i0, cur);
 #pragma unroll
         for (int u = 0; u < kU; ++u) {
           const int64_t i = i0 + 128 * u + 4 * lane;
@@ -384,41 +393,53 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             if (pp4[e]) {
-              if (pos < (uint32_t)kSub) {
-                my_key[pos] = kk4[e];
-                my_idx[pos] = (int32_t)(i + e);
+              if (pos < cap) {
+                sm.ckey[dbase + pos] = kk4[e];
+                sm.cidx[dbase + pos] = (int32_t)(i + e);
               }
               ++pos;
             }
           }
           c += __popc(q0) + __popc(q1) + __popc(q2) + __popc(q3);
         }
-#pragma unroll
-        for (int u = 0; u < kU; ++u) cur[u] = nxt[u];
       }
+      if (round == 1) break;  // (c and the layout were set by round 0)
       if (lane == 0) sm.cnt[warp] = c;
       __syncthreads();
-      uint32_t total = 0u;
+      uint32_t total = 0u, before = 0u;
+      bool spill = false;
       for (int w = 0; w < kTopkWarps; ++w) {
+        before += w < warp ? sm.cnt[w] : 0u;
         total += sm.cnt[w];
-        ok = ok && sm.cnt[w] <= (uint32_t)kSub;
+        spill = spill || sm.cnt[w] > (uint32_t)kSub;
       }
-      ok = ok && total >= (uint32_t)K_p;  // else the cut was too high
+      // too few keys pass (the cut was too high) or too many: the full row
+      ok = total >= (uint32_t)K_p && total <= (uint32_t)kCand;
+      if (ok && spill) {  // (CTA-uniform)
+        dbase = before;
+        cap = c;
+        cb0 = (int)before;
+        cb1 = (int)(before + c);
+      } else {
+        cb0 = warp * kSub;
+        cb1 = cb0 + (int)c;
+        break;
+      }
+      }
     }
     __syncthreads();
     // (positions are < K_p by construction; the guards keep a row that
     // changed under the kernel from writing into its neighbour)
     uint32_t T, ties;
-    if (ok) {
-      const int mine = (int)sm.cnt[warp];  // each warp visits its own sub-buffer
+    if (ok) {  // each warp takes its own candidates, which follow the previous warp's
       radix_kth(
           [&](auto f) {
-            for (int j = lane; j < mine; j += 32) f(my_key[j]);
+            for (int j = cb0 + lane; j < cb1; j += 32) f(sm.ckey[j]);
           },
           (uint32_t)K_p, sm, &T, &ties);
-      ordered_take([&](int64_t j) { return my_key[j]; }, 0, sm.cnt[warp], T, ties, sm,
+      ordered_take([&](int64_t j) { return sm.ckey[j]; }, cb0, cb1, T, ties, sm,
                    [&](uint32_t pos, int64_t j) {
-                     if (pos < (uint32_t)K_p) o[pos] = my_idx[j];
+                     if (pos < (uint32_t)K_p) o[pos] = sm.cidx[j];
                    });
     } else {
       radix_kth(

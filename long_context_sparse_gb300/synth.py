@@ -20,6 +20,8 @@ from __future__ import annotations
 import dataclasses
 import math
 
+import numpy as np
+
 import torch
 
 
@@ -98,6 +100,42 @@ def indexer_inputs(wl: Workload, seed: int, device="cpu"):
     w = torch.softmax(torch.randn((wl.S, wl.H_I), generator=g, device=device),
                       dim=-1).contiguous()
     return q_idx, k_idx, w
+
+
+def indexer_row_inputs(wl: Workload, seed: int, n_rows: int, device="cpu"):
+    """Indexer inputs for a block of n_rows queries only (long sequences):
+    q_idx [n_rows,H_I,D_I] bf16, k_idx [S,D_I] bf16 (every key), w [n_rows,H_I]
+    fp32, with the distributions of indexer_inputs."""
+    g = _gen(seed + 7, device)
+    std = 1.0 / math.sqrt(wl.D_I)
+    k_idx = _normal_bf16((wl.S, wl.D_I), std, g, device)
+    q_idx = _normal_bf16((n_rows, wl.H_I, wl.D_I), std, g, device)
+    w = torch.softmax(torch.randn((n_rows, wl.H_I), generator=g, device=device),
+                      dim=-1).contiguous()
+    return q_idx, k_idx, w
+
+
+def vertical_slash_columns(wl: Workload, seed: int, n_cols: int = 16) -> np.ndarray:
+    """The seeded global pool columns of the vertical-slash score skew."""
+    rng = np.random.default_rng(seed + 31337)
+    return np.sort(rng.choice(max(1, wl.P), size=min(n_cols, wl.P), replace=False))
+
+
+def vertical_slash_bias(scores, rows, bias: float, cols, band: int = 256):
+    """Add `bias` in place to the skewed entries of score rows (numpy or
+    torch, row i <-> query rows[i]): the local band of the `band` most recent
+    complete pools, p in [n_full(t) - band, n_full(t)), and the global
+    columns `cols` with p < n_full(t) (each entry once).  This shapes the
+    synthetic scores of the 1M-token stress configuration after the
+    vertical-slash pattern; it is input shaping, not part of the method."""
+    for i, t in enumerate(rows):
+        nf = (int(t) + 1) // 4
+        lo = max(0, nf - band)
+        scores[i, lo:nf] += bias
+        c = [int(x) for x in cols if int(x) < lo]
+        if c:
+            scores[i, c] += bias
+    return scores
 
 
 def gate_inputs(wl: Workload, seed: int, device="cpu"):

@@ -618,3 +618,59 @@ def test_bounded_wait_times_out_and_the_context_survives():
     got = dsa.pool_keys(cfg, k_idx.to(DEV))
     torch.cuda.synchronize()
     np.testing.assert_array_equal(bits(got), oracle.pool(bits(k_idx)))
+
+
+def test_topk_on_vertical_slash_rows_at_1m_tokens():
+    """The 1M-token stress configuration: indexer scores of 262k-pool rows
+    skewed toward a vertical-slash pattern (+3 sigma on the 256 most recent
+    pools and on 16 seeded global columns, sigma the spread of the unbiased
+    scores on sampled rows, measured by the oracle), then top-k.  The band
+    crowds one warp's stretch of the row, so the kernel's second,
+    exact-placement sweep runs.  Checked bit-exactly against the oracle's
+    top-k of the same biased fp32 scores, and against the oracle's own fp64
+    scores with the same bias within the tie band."""
+    wl = synth.WORKLOADS["stress_fwd_s1m"]
+    cfg = _cfg(wl)
+    S, P, n_rows = wl.S, wl.P, 48
+    blocks = [S - n_rows, S // 2]
+    q_rows, k_idx, w_rows = synth.indexer_row_inputs(wl, 29, n_rows * len(blocks), "cpu")
+    kpool_h = oracle.pool(bits(k_idx))
+    # the spread of the unbiased scores, from the oracle on sampled rows
+    probe = np.array([blocks[0] + 5, blocks[0] + n_rows - 1, blocks[1] + 3], np.int64)
+    probe_i = np.array([5, n_rows - 1, n_rows + 3], np.int64)
+    sc_probe = oracle.index_scores(bits(q_rows)[probe_i], kpool_h,
+                                   w_rows.numpy()[probe_i], probe, S)
+    sigma = float(np.std(sc_probe[np.isfinite(sc_probe)]))
+    bias = float(np.float32(3.0 * sigma))
+    cols = synth.vertical_slash_columns(wl, 29)
+    q_full = torch.zeros((S, wl.H_I, wl.D_I), dtype=torch.bfloat16, device=DEV)
+    w_full = torch.zeros((S, wl.H_I), dtype=torch.float32, device=DEV)
+    kp = dsa.pool_keys(cfg, k_idx.to(DEV))
+    ws = dsa.workspace(cfg, dsa.WS_STATUS, DEV)
+    ld = (P + 127) // 128 * 128
+    for b, t0 in enumerate(blocks):
+        rows = np.arange(t0, t0 + n_rows, dtype=np.int64)
+        q_full[t0:t0 + n_rows] = q_rows[b * n_rows:(b + 1) * n_rows].to(DEV)
+        w_full[t0:t0 + n_rows] = w_rows[b * n_rows:(b + 1) * n_rows].to(DEV)
+        sc = dsa.index_scores(cfg, q_full, kp, w_full, t0, n_rows, ld=ld, ws=ws)
+        synth.vertical_slash_bias(sc, rows, bias, cols)
+        got = dsa.topk_from_scores(cfg, sc, t0, ws=ws)
+        _status_ok(ws)
+        # bit-exact on the shared (GPU-computed, biased) fp32 scores
+        ref_shared = oracle.topk(sc.cpu().numpy(), rows, wl.K_p)
+        np.testing.assert_array_equal(got.cpu().numpy(), ref_shared)
+        # against the oracle's fp64 scores with the same bias, on sampled rows
+        pick = np.array([0, n_rows // 2, n_rows - 1], np.int64)
+        sel = b * n_rows + pick
+        sc64 = oracle.index_scores(bits(q_rows)[sel], kpool_h, w_rows.numpy()[sel],
+                                   rows[pick], S)
+        synth.vertical_slash_bias(sc64, rows[pick], bias, cols)
+        ref = oracle.topk(sc64, rows[pick], wl.K_p)
+        eq, ex = check_index_rows(got.cpu().numpy()[pick], ref, sc64, rows[pick], wl.K_p)
+        assert eq + ex == pick.size
+        # the skew took effect: about half the +3 sigma band is selected (an
+        # unbiased band of 256 pools would hold about 0.5 of 512 out of 262k)
+        band_hits = (got.cpu().numpy()[pick] >= (rows[pick, None] + 1) // 4 - 256).sum(1)
+        assert band_hits.min() >= 16 and band_hits.mean() >= 48, band_hits
+        q_full[t0:t0 + n_rows] = 0
+        w_full[t0:t0 + n_rows] = 0
