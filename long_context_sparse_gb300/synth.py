@@ -102,6 +102,18 @@ def indexer_inputs(wl: Workload, seed: int, device="cpu"):
     return q_idx, k_idx, w
 
 
+def normal_bf16_blocks(shape, std: float, seed: int, device,
+                       block_rows: int) -> torch.Tensor:
+    """bf16 N(0,1)*std of `shape`, drawn block_rows leading rows at a time
+    from one seeded generator (no fp32 temporary of the whole tensor)."""
+    g = _gen(seed, device)
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    for r0 in range(0, shape[0], block_rows):
+        r1 = min(shape[0], r0 + block_rows)
+        out[r0:r1] = _normal_bf16((r1 - r0,) + tuple(shape[1:]), std, g, device)
+    return out
+
+
 def indexer_row_inputs(wl: Workload, seed: int, n_rows: int, device="cpu"):
     """Indexer inputs for a block of n_rows queries only (long sequences):
     q_idx [n_rows,H_I,D_I] bf16, k_idx [S,D_I] bf16 (every key), w [n_rows,H_I]

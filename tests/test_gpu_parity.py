@@ -674,3 +674,46 @@ def test_topk_on_vertical_slash_rows_at_1m_tokens():
         assert band_hits.min() >= 16 and band_hits.mean() >= 48, band_hits
         q_full[t0:t0 + n_rows] = 0
         w_full[t0:t0 + n_rows] = 0
+
+
+def test_forward_at_1m_tokens_sampled_rows():
+    """The 1M-token forward configuration end to end on the GPU: chunked
+    indexer + top-k under the 2 GiB scratch cap (256 MiB chunks of 262k-pool
+    rows), then the sparse attention forward; sampled late and middle rows
+    checked against the oracle (selection within the tie band, O and LSE
+    within the attention tolerance on the GPU's selection)."""
+    wl = synth.WORKLOADS["stress_fwd_s1m"]
+    cfg = _cfg(wl)
+    S = wl.S
+    torch.cuda.empty_cache()
+    try:
+        q_idx = synth.normal_bf16_blocks((S, wl.H_I, wl.D_I), 1 / math.sqrt(wl.D_I), 61,
+                                         DEV, 65536)
+        k_idx = synth.normal_bf16_blocks((S, wl.D_I), 1 / math.sqrt(wl.D_I), 62, DEV, S)
+        w = torch.softmax(torch.randn((S, wl.H_I), generator=synth._gen(63, DEV),
+                                      device=DEV), dim=-1).contiguous()
+        idx = dsa.index_scores_topk(cfg, q_idx, k_idx, w)
+        q = synth.normal_bf16_blocks((S, wl.H, wl.d_qk), 1 / math.sqrt(wl.d_qk), 64, DEV,
+                                     8192)
+        k = synth.normal_bf16_blocks((S, wl.d_qk), 1 / math.sqrt(wl.d_qk), 65, DEV, S)
+        v = synth.normal_bf16_blocks((S, wl.d_v), 1 / math.sqrt(wl.d_v), 66, DEV, S)
+        wsf = dsa.workspace(cfg, dsa.WS_FWD, DEV)
+        o, lse = dsa.sparse_attn_fwd(cfg, q, k, v, idx, ws=wsf)
+        _status_ok(wsf)
+        rows = np.array([S // 2 + 7, S - 257, S - 1], np.int64)
+        rt = torch.from_numpy(rows).to(DEV)
+        idx_h = idx.cpu().numpy()
+        kp = oracle.pool(bits(k_idx))
+        sc = oracle.index_scores(bits(q_idx[rt]), kp, w[rt].cpu().numpy(), rows, S)
+        ref = oracle.topk(sc, rows, wl.K_p)
+        eq, ex = check_index_rows(idx_h[rows], ref, sc, rows, wl.K_p)
+        assert eq + ex == rows.size
+        ro, rl = oracle.attn_fwd(bits(q[rt]), bits(k), bits(v), idx_h, wl.K_p, wl.n_loc,
+                                 cfg.scale, rows)
+        om, _ = oracle.attn_fwd(bits(q[rt]), bits(k), abs_bits(bits(v)), idx_h, wl.K_p,
+                                wl.n_loc, cfg.scale, rows)
+        assert_close(f64(o[rt]), ro, "o", mag=om)
+        assert_close(f64(lse[rt]), rl, "lse")
+    finally:
+        q_idx = k_idx = w = idx = q = k = v = o = lse = None
+        torch.cuda.empty_cache()
