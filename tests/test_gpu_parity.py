@@ -717,3 +717,73 @@ def test_forward_at_1m_tokens_sampled_rows():
     finally:
         q_idx = k_idx = w = idx = q = k = v = o = lse = None
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name,n_index_rows,n_attn_rows", [
+    ("glm_chunked_s128k", 4096, 16),   # the bench configuration, full size
+    ("padded2051_s64k", 1024, 16),     # 2,051 keys, 16 heads, full size
+])
+def test_full_size_configuration_sampled_rows(name, n_index_rows, n_attn_rows):
+    """A configuration at its full sequence length, in the launch
+    configuration the bench times (chunked indexer + top-k, forward,
+    backward): the selection of n_index_rows sampled queries (seeded rows
+    plus the edge rows) against the unchunked fp64 oracle within the tie
+    band, and O, LSE, dq, dK, dV of sampled rows against the oracle."""
+    import concurrent.futures
+    import os
+    wl = synth.WORKLOADS[name]
+    cfg = _cfg(wl)
+    S = wl.S
+    torch.cuda.empty_cache()
+    try:
+        q_idx = synth.normal_bf16_blocks((S, wl.H_I, wl.D_I), 1 / math.sqrt(wl.D_I), 71,
+                                         DEV, 16384)
+        k_idx = synth.normal_bf16_blocks((S, wl.D_I), 1 / math.sqrt(wl.D_I), 72, DEV, S)
+        w = torch.softmax(torch.randn((S, wl.H_I), generator=synth._gen(73, DEV),
+                                      device=DEV), dim=-1).contiguous()
+        q = synth.normal_bf16_blocks((S, wl.H, wl.d_qk), 1 / math.sqrt(wl.d_qk), 74, DEV,
+                                     8192)
+        k = synth.normal_bf16_blocks((S, wl.d_qk), 1 / math.sqrt(wl.d_qk), 75, DEV, S)
+        v = synth.normal_bf16_blocks((S, wl.d_v), 1 / math.sqrt(wl.d_v), 76, DEV, S)
+        dO = synth.normal_bf16_blocks((S, wl.H, wl.d_v), 1.0, 77, DEV, 8192)
+        wsi = dsa.workspace(cfg, dsa.WS_INDEX, DEV)
+        idx = dsa.index_scores_topk(cfg, q_idx, k_idx, w, ws=wsi)
+        o, lse = dsa.sparse_attn_fwd(cfg, q, k, v, idx)
+        _status_ok(wsi)
+        # ---- the selection, sampled rows, oracle calls spread over the cores
+        rows = synth.sample_rows(wl, n_index_rows, 9).numpy()
+        rt = torch.from_numpy(rows).to(DEV)
+        q_rows, w_rows = bits(q_idx[rt]), w[rt].cpu().numpy()
+        kp = oracle.pool(bits(k_idx))
+        got = idx[rt].cpu().numpy()
+        parts = np.array_split(np.arange(rows.size), max(1, min(32, os.cpu_count() or 1)))
+
+        def check(part):
+            sc = oracle.index_scores(q_rows[part], kp, w_rows[part], rows[part], S)
+            ref = oracle.topk(sc, rows[part], wl.K_p)
+            return check_index_rows(got[part], ref, sc, rows[part], wl.K_p)
+        with concurrent.futures.ThreadPoolExecutor(len(parts)) as ex:
+            res = list(ex.map(check, parts))
+        eq = sum(r[0] for r in res)
+        exempt = sum(r[1] for r in res)
+        assert eq + exempt == rows.size and eq >= 0.9 * rows.size
+        # ---- attention on sampled rows (the GPU selection on both sides)
+        arows = synth.sample_rows(wl, n_attn_rows, 10).numpy()
+        at = torch.from_numpy(arows).to(DEV)
+        idx_h = idx.cpu().numpy()
+        ro, rl = oracle.attn_fwd(bits(q[at]), bits(k), bits(v), idx_h, wl.K_p, wl.n_loc,
+                                 cfg.scale, arows)
+        om, _ = oracle.attn_fwd(bits(q[at]), bits(k), abs_bits(bits(v)), idx_h, wl.K_p,
+                                wl.n_loc, cfg.scale, arows)
+        assert_close(f64(o[at]), ro, "o", mag=om)
+        assert_close(f64(lse[at]), rl, "lse")
+        dq, _, _ = dsa.sparse_attn_bwd(cfg, q, k, v, o, lse, dO, idx)
+        rdq, _, _ = oracle.attn_bwd(bits(q[at]), bits(k), bits(v), bits(dO[at]), idx_h,
+                                    wl.K_p, wl.n_loc, cfg.scale, arows,
+                                    np.zeros(1, np.int64))
+        assert_close(f64(dq[at]), rdq, "dq")
+        dq = None
+        _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, arows[-6:])
+    finally:
+        q_idx = k_idx = w = q = k = v = dO = idx = o = lse = None
+        torch.cuda.empty_cache()
