@@ -411,7 +411,7 @@ def _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, rows):
 
 @pytest.mark.parametrize("name,S", [("glm_s16k", 16384),
                                     ("padded2051_s64k", 16500),
-                                    # large enough for the lock-step scatter
+                                    # several waves of queries per CTA
                                     ("glm_s16k", 32768)])
 def test_attn_large_sampled_rows(name, S):
     wl, q, k, v, dO, idx = _attn_case(name, S, 33)
