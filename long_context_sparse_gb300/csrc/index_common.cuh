@@ -1,9 +1,26 @@
 // index_common.cuh -- helpers shared by the indexer and the top-k kernels.
 #pragma once
 
+#include <atomic>
+
 #include "dsa_common.cuh"
 
 namespace dsa {
+
+// Raise a kernel's dynamic shared-memory limit on the current device once:
+// `done` holds one bit per device, set after the call succeeded, so threads
+// and devices may interleave freely (a repeated call is harmless).
+template <class Kernel>
+inline cudaError_t set_smem_once(Kernel kernel, int bytes, std::atomic<uint64_t>& done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_release);
+  return e;
+}
 
 // Order-preserving image of an fp32 score: larger float -> larger key.
 // -0.0 is first made +0.0 so the two compare equal (lower index wins).

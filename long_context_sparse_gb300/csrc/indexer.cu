@@ -273,16 +273,9 @@ cudaError_t launch_indexer_t(const LaunchCtx& c, const CUtensorMap& q_map,
   const int n_ptiles = (int)((p_lim + kBM - 1) / kBM);
   const int64_t n_items = n_ntiles * n_ptiles;
   if (n_items == 0) return cudaSuccess;
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(indexer_kernel<HI, DI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)C::kSmem);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = set_smem_once(indexer_kernel<HI, DI>, (int)C::kSmem, smem_set);
+  if (e != cudaSuccess) return e;
   int64_t grid = n_items < c.num_sms ? n_items : c.num_sms;
   indexer_kernel<HI, DI><<<(unsigned)grid, kThreads, C::kSmem, c.stream>>>(
       q_map, k_map, w, t0, q0, rows, p_lim, scores, ld, n_ptiles, n_items, c.status,

@@ -437,16 +437,9 @@ cudaError_t launch_t(const LaunchCtx& c, const CUtensorMap& q_map, const CUtenso
   constexpr int QT = kBN / HI;
   const int64_t n_ntiles = (t_end - t_begin + QT - 1) / QT;
   if (n_ntiles == 0) return cudaSuccess;
-  static int attr_dev = -1;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (attr_dev != dev) {
-    cudaError_t e = cudaFuncSetAttribute(indexer_topk_kernel<HI, DI>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_dev = dev;
-  }
+  static std::atomic<uint64_t> smem_set{0};
+  cudaError_t e = set_smem_once(indexer_topk_kernel<HI, DI>, (int)smem, smem_set);
+  if (e != cudaSuccess) return e;
   const int64_t grid = n_ntiles < c.num_sms ? n_ntiles : c.num_sms;
   indexer_topk_kernel<HI, DI><<<(unsigned)grid, kThreads, smem, c.stream>>>(
       q_map, k_map, w, t_begin, t_end, K_p, out, n_ntiles, c.status, c.timeout_ns);
