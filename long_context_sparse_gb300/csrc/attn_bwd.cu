@@ -83,14 +83,6 @@ cudaError_t launch_attn_bwd_zero(const LaunchCtx& c, const AttnShape& s, float* 
   return cudaGetLastError();
 }
 
-cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
-                                const __nv_bfloat16* o, const __nv_bfloat16* dO,
-                                float* delta, float* dk_acc, float* dv_acc) {
-  cudaError_t e = launch_attn_bwd_delta(c, s, o, dO, delta);
-  if (e != cudaSuccess) return e;
-  return launch_attn_bwd_zero(c, s, dk_acc, dv_acc);
-}
-
 cudaError_t launch_f32_to_bf16(const LaunchCtx& c, const float* a, __nv_bfloat16* out,
                                int64_t n) {
   const int64_t n4 = n / 4;

@@ -69,8 +69,10 @@ struct AttnShape {
 // head block, rounded up to 16, 32 or 64.
 int attn_tc_heads(int H);
 
-// a5 + a6: sparse attention forward (tcgen05).  q_map: q viewed as
-// [S*H, D] bf16, box {64, attn_tc_heads(H)}, 128-byte swizzle.
+// a5 + a6: sparse attention forward (tcgen05) for queries s.t_lo ..
+// s.t_hi - 1.  q_map: the call's q rows viewed as [(t_hi - t_lo)*H, D]
+// bf16, box {64, attn_tc_heads(H)}, 128-byte swizzle; idx, o, lse hold the
+// call's rows too.
 cudaError_t launch_attn_fwd_tc(const LaunchCtx& c, const AttnShape& s,
                                const CUtensorMap& q_map, const __nv_bfloat16* k,
                                const __nv_bfloat16* v, const int32_t* idx,
@@ -86,15 +88,10 @@ cudaError_t launch_attn_bwd_delta(const LaunchCtx& c, const AttnShape& s,
 cudaError_t launch_attn_bwd_zero(const LaunchCtx& c, const AttnShape& s, float* dk_acc,
                                  float* dv_acc);
 
-// a7: delta = rowsum(dO * O); zero the fp32 dK/dV accumulators (dv_acc may
-// be nullptr: one dKV accumulator).
-cudaError_t launch_attn_bwd_pre(const LaunchCtx& c, const AttnShape& s,
-                                const __nv_bfloat16* o,
-                                const __nv_bfloat16* dO, float* delta,
-                                float* dk_acc, float* dv_acc);
-
-// a8: sparse attention backward on tcgen05 (dQ direct, dK/dV fp32 scatter).
-// q_map / g_map: q and dO viewed as [S*H, D] bf16, box {64, 64}.
+// a8: sparse attention backward on tcgen05 (dQ direct, dK/dV fp32 scatter)
+// for queries s.t_lo .. s.t_hi - 1.  q_map / g_map: the call's q and dO
+// rows viewed as [(t_hi - t_lo)*H, D] bf16, box {64, 64}; lse, delta, idx
+// and dq hold the call's rows; dk_acc / dv_acc span every key.
 // dv_acc == nullptr: K and V are one tensor; dk_acc receives dK + dV.
 cudaError_t launch_attn_bwd_tc(const LaunchCtx& c, const AttnShape& s,
                                const CUtensorMap& q_map, const CUtensorMap& g_map,
