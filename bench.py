@@ -83,7 +83,7 @@ def work_model(wl, kv=False):
     }
 
 
-def launches_per_step(wl, streaming=False):
+def launches_per_step(wl, streaming=False, kv=False):
     """Kernel launches of one step, mirroring the library's host loop."""
     C = min(wl.chunk_q, wl.S)
     n = 1 if wl.S >= 4 else 0                   # pool
@@ -95,8 +95,8 @@ def launches_per_step(wl, streaming=False):
             n += 1                              # indexer chunk
         n += 1                                  # top-k chunk
     n += 1                                      # attention forward
-    if wl.backward:
-        n += 6                                  # delta, 2 zero, main, 2 finalize
+    if wl.backward:                             # delta, zero, main, finalize
+        n += 4 if kv else 6                     # (one accumulator when K = V)
     return n
 
 
@@ -649,7 +649,7 @@ def main():
             "roofline": roof,
             "clocks": clk.summary(),
             "gpu_launches": launches_per_step(
-                wl, args.select == "streaming") * args.steps,
+                wl, args.select == "streaming", kv) * args.steps,
             "e2e": e2e}
 
     if not args.no_cpu:
