@@ -365,12 +365,12 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
         }
       };
       const uint32_t lt = (1u << lane) - 1u;
-      // round 0 writes the first kSub passing keys of the stretch to the
-      // warp's sub-buffer; round 1 (only after a spill) all of them to their
+      // sweep 0 writes the first kSub passing keys of the stretch to the
+      // warp's sub-buffer; sweep 1 (only after a spill) all of them to their
       // exact place in the flat array
       uint32_t dbase = (uint32_t)(warp * kSub), cap = kSub;
 #pragma unroll 1
-      for (int round = 0; round < 2; ++round) {
+      for (int sweep = 0; sweep < 2; ++sweep) {
       uint32_t c = 0u;
       for (int64_t i0 = b0; i0 < b1; i0 += 128 * kU) {
         float4 cur[kU];
@@ -403,7 +403,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
           c += __popc(q0) + __popc(q1) + __popc(q2) + __popc(q3);
         }
       }
-      if (round == 1) break;  // (c and the layout were set by round 0)
+      if (sweep == 1) break;  // (c and the layout were set by sweep 0)
       if (lane == 0) sm.cnt[warp] = c;
       __syncthreads();
       uint32_t total = 0u, before = 0u;
