@@ -321,7 +321,10 @@ DSA_API dsa_status_t dsa_step(const dsa_config_t* cfg, const dsa_step_tensors_t*
  * last copy back, so synchronising `stream` makes every host output
  * valid.  Results equal dsa_step's, up to the order of dK/dV's fp32
  * additions.  The three streams must be distinct.  CUDA events are created
- * and released inside the call; no memory is allocated.  ws: DSA_WS_STEP. */
+ * and released inside the call; no memory is allocated.  Argument errors
+ * return before anything is queued; after DSA_ERR_CUDA part of the step may
+ * already be queued on the three streams: synchronise them before reusing
+ * any buffer.  ws: DSA_WS_STEP. */
 DSA_API dsa_status_t dsa_step_host(const dsa_config_t* cfg,
                            const dsa_step_tensors_t* host,
                            const dsa_step_tensors_t* dev, int32_t n_chunks, void* ws,
