@@ -167,6 +167,40 @@ def attention_inputs(wl: Workload, seed: int, device="cpu"):
     return q, k, v, dO
 
 
+# Input scales of the attention parity cases.  "pages": the workloads' own
+# N(0,1)/sqrt(dim), under which O, dQ and dK are far below one (a check with
+# an absolute bound cannot tell them from zero).  "unit": q, k, v, dO ~ N(0,1)
+# per element, so the logits have unit spread after the 1/sqrt(d) scale and
+# O, dQ, dK, dV are of order one.  "peaked": as "unit" with q eight times
+# larger, so each softmax row is dominated by a few keys and later key tiles
+# often raise the running maximum far above the first tile's.
+ATTN_INPUT_SCALES = ("pages", "unit", "peaked")
+_Q_GAIN = {"unit": 1.0, "peaked": 8.0}
+
+
+def attention_inputs_scaled(wl: Workload, seed: int, scale: str = "pages",
+                            device="cpu"):
+    """attention_inputs at one of ATTN_INPUT_SCALES (same shapes, dtypes)."""
+    if scale == "pages":
+        return attention_inputs(wl, seed, device)
+    gain = _Q_GAIN[scale]
+    g = _gen(seed + 6007, device)
+    q = _normal_bf16((wl.S, wl.H, wl.d_qk), gain, g, device)
+    k = _normal_bf16((wl.S, wl.d_qk), 1.0, g, device)
+    v = _normal_bf16((wl.S, wl.d_v), 1.0, g, device)
+    dO = _normal_bf16((wl.S, wl.H, wl.d_v), 1.0, g, device)
+    return q, k, v, dO
+
+
+def attention_std(wl: Workload, scale: str = "pages"):
+    """Standard deviations (q, k, v, dO) of attention_inputs_scaled, for
+    drawing the same distributions in row blocks on the device."""
+    if scale == "pages":
+        return (1.0 / math.sqrt(wl.d_qk), 1.0 / math.sqrt(wl.d_qk),
+                1.0 / math.sqrt(wl.d_v), 1.0)
+    return (_Q_GAIN[scale], 1.0, 1.0, 1.0)
+
+
 def random_selection(wl: Workload, seed: int, device="cpu",
                      rows_per_draw: int = 1024) -> torch.Tensor:
     """A valid pool selection [S, K_p] int32 drawn uniformly at random:

@@ -26,3 +26,19 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With DSA_PARITY_REPORT=<file>, write every output comparison of the
+    run (test, tensor, max error, max |oracle|, their ratio) as JSON lines:
+    the measured normalised errors of the parity checks."""
+    path = os.environ.get("DSA_PARITY_REPORT")
+    if not path:
+        return
+    import json
+    from tests.helpers import PARITY_LOG
+    with open(path, "w") as f:
+        for test, name, err, top in PARITY_LOG:
+            f.write(json.dumps({"test": test, "tensor": name, "max_err": err,
+                                "max_ref": top,
+                                "ratio": err / top if top else None}) + "\n")

@@ -9,7 +9,8 @@ import torch
 import long_context_sparse_gb300 as dsa
 import oracle
 from long_context_sparse_gb300 import synth
-from tests.helpers import abs_bits, assert_close, bits, check_index_rows, f64
+from tests.helpers import (abs_bits, assert_close, bits, check_index_rows, f64,
+                           oracle_attn_bwd, oracle_attn_fwd, tol)
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -282,37 +283,51 @@ def test_index_topk_full_budget_selects_every_pool():
 # ------------------------------------------------------------ attention
 
 
-def _attn_case(name, S, seed, **over):
+def _attn_case(name, S, seed, scale="pages", **over):
     wl = synth.scaled(synth.WORKLOADS[name], S, **over)
-    q, k, v, dO = synth.attention_inputs(wl, seed, "cpu")
+    q, k, v, dO = synth.attention_inputs_scaled(wl, seed, scale, "cpu")
     idx = synth.random_selection(wl, seed, "cpu")
     return wl, q, k, v, dO, idx
 
 
-@pytest.mark.parametrize("name,S,over", [
-    ("tiny_fwd_s1k", 1024, {}),
-    ("tiny_fwd_s1k", 77, dict(K_p=5, n_loc=3)),
-    ("glm_s16k", 3000, {}),
-    ("glm_s16k", 300, dict(H=80)),          # two head blocks
-    ("padded2051_s64k", 2300, {}),          # 16 heads, 2051 keys
-    ("glm_s16k", 13, dict(n_loc=3)),        # tiny, empty rows
+# Input scales (synth.ATTN_INPUT_SCALES): "pages" is the workloads' own; at
+# "unit" and "peaked" O, dQ, dK and dV are of order one, so every check below
+# fails for a kernel that leaves one of them at zero, gets its sign or scale
+# wrong, or drops a term (delta, the online-softmax rescale of later tiles).
+@pytest.mark.parametrize("name,S,over,scale", [
+    ("tiny_fwd_s1k", 1024, {}, "pages"),
+    ("tiny_fwd_s1k", 1024, {}, "peaked"),
+    ("tiny_fwd_s1k", 77, dict(K_p=5, n_loc=3), "pages"),
+    ("tiny_fwd_s1k", 77, dict(K_p=5, n_loc=3), "unit"),
+    ("glm_s16k", 3000, {}, "pages"),
+    ("glm_s16k", 3000, {}, "peaked"),       # 16 key tiles, sampled rows
+    ("glm_s16k", 640, {}, "unit"),          # 64 heads, d = 512, every row
+    ("glm_s16k", 640, {}, "peaked"),
+    ("glm_s16k", 300, dict(H=80), "pages"),  # two head blocks
+    ("glm_s16k", 300, dict(H=80), "unit"),
+    ("padded2051_s64k", 2300, {}, "pages"),  # 16 heads, 2051 keys
+    ("padded2051_s64k", 2300, {}, "unit"),
+    ("padded2051_s64k", 520, {}, "peaked"),
+    ("glm_s16k", 13, dict(n_loc=3), "pages"),  # tiny, empty rows
+    ("glm_s16k", 13, dict(n_loc=3), "unit"),
 ])
-def test_attn_fwd_bwd_match_oracle(name, S, over):
-    wl, q, k, v, dO, idx = _attn_case(name, S, 21, **over)
+def test_attn_fwd_bwd_match_oracle(name, S, over, scale):
+    wl, q, k, v, dO, idx = _attn_case(name, S, 21, scale, **over)
     cfg = _cfg(wl)
     qd, kd, vd, dOd, idd = (x.to(DEV) for x in (q, k, v, dO, idx))
     wsf = dsa.workspace(cfg, dsa.WS_FWD, DEV)
     o, lse = dsa.sparse_attn_fwd(cfg, qd, kd, vd, idd, ws=wsf)
     _status_ok(wsf)
     rows = np.arange(S) if S <= 700 else synth.sample_rows(wl, 48, 3).numpy()
-    ro, rl = oracle.attn_fwd(bits(q)[rows], bits(k), bits(v), idx.numpy(),
-                             wl.K_p, wl.n_loc, cfg.scale, rows)
+    qb, kb, vb, dOb, idx_h = bits(q), bits(k), bits(v), bits(dO), idx.numpy()
+    ro, rl = oracle_attn_fwd(qb[rows], kb, vb, idx_h, wl.K_p, wl.n_loc, cfg.scale,
+                             rows)
     go, gl = f64(o)[rows], f64(lse)[rows]
     fin = np.isfinite(rl)
     assert (go[~fin.any(1)] == 0).all()        # empty key set: O = 0
-    om, _ = oracle.attn_fwd(bits(q)[rows], bits(k), abs_bits(bits(v)),
-                            idx.numpy(), wl.K_p, wl.n_loc, cfg.scale, rows)
-    assert_close(go, ro, "o", mag=om)          # om = sum_j P_j |v_j|
+    om, _ = oracle_attn_fwd(qb[rows], kb, abs_bits(vb), idx_h, wl.K_p, wl.n_loc,
+                            cfg.scale, rows)
+    assert_close(go, ro, "o", mag=om, **tol(scale))   # om = sum_j P_j |v_j|
     assert_close(gl, rl, "lse")                # -inf rows must match exactly
     if not wl.backward and S > 200:
         return
@@ -320,32 +335,43 @@ def test_attn_fwd_bwd_match_oracle(name, S, over):
     dq, dk, dv = dsa.sparse_attn_bwd(cfg, qd, kd, vd, o, lse, dOd, idd, ws=wsb)
     _status_ok(wsb)
     if S <= 700:
-        rdq, rdk, rdv = oracle.attn_bwd(bits(q), bits(k), bits(v), bits(dO),
-                                        idx.numpy(), wl.K_p, wl.n_loc,
-                                        cfg.scale)
+        allr = np.arange(S)
+        rdq, rdk, rdv = oracle_attn_bwd(qb, kb, vb, dOb, idx_h, wl.K_p, wl.n_loc,
+                                        cfg.scale, allr)
         # sum P |dO| bounds the bf16-operand error of dV = P^T dO
-        _, _, mdv = oracle.attn_bwd(bits(q), bits(k), bits(v),
-                                    abs_bits(bits(dO)), idx.numpy(), wl.K_p,
-                                    wl.n_loc, cfg.scale)
-        assert_close(f64(dq), rdq, "dq")
-        assert_close(f64(dk), rdk, "dk")
-        assert_close(f64(dv), rdv, "dv", mag=mdv)
+        _, _, mdv = oracle_attn_bwd(qb, kb, vb, abs_bits(dOb), idx_h, wl.K_p,
+                                    wl.n_loc, cfg.scale, allr)
+        assert_close(f64(dq), rdq, "dq", **tol(scale))
+        assert_close(f64(dk), rdk, "dk", **tol(scale))
+        assert_close(f64(dv), rdv, "dv", mag=mdv, **tol(scale))
     else:
-        rdq, _, _ = oracle.attn_bwd(bits(q)[rows], bits(k), bits(v),
-                                    bits(dO)[rows], idx.numpy(), wl.K_p,
-                                    wl.n_loc, cfg.scale, rows)
-        assert_close(f64(dq)[rows], rdq, "dq")
+        rdq, _, _ = oracle_attn_bwd(qb[rows], kb, vb, dOb[rows], idx_h, wl.K_p,
+                                    wl.n_loc, cfg.scale, rows, np.zeros(1, np.int64))
+        assert_close(f64(dq)[rows], rdq, "dq", **tol(scale))
 
 
-@pytest.mark.parametrize("name,S,over", [
-    ("glm_s16k", 640, {}),                  # 64 heads, d = 512
-    ("padded2051_s64k", 520, {}),           # 16 heads, 2051 keys
-    ("tiny_fwd_s1k", 300, dict(K_p=16)),    # 8 heads, d = 128
-    ("glm_s16k", 4096, {}),                 # sampled rows
+def _check_dk_half(dkv, rdk, rdv, mdv, name, scale):
+    """K = V: dkv = dK + dV.  Where dV dominates, a wrong or missing dK half
+    hides inside dkv's tolerance; compare dkv - dV_oracle with dK_oracle on
+    its own scale.  The bf16 rounding of dkv (2^-9 |dK + dV|) is the floor of
+    this comparison, so it is made only at the unit and peaked input scales,
+    where |dK| is of the order of |dV|."""
+    assert_close(dkv - rdv, rdk, name, mag=np.abs(rdk) + np.abs(mdv), **tol(scale))
+
+
+@pytest.mark.parametrize("name,S,over,scale", [
+    ("glm_s16k", 640, {}, "pages"),                 # 64 heads, d = 512
+    ("glm_s16k", 640, {}, "unit"),
+    ("padded2051_s64k", 520, {}, "pages"),          # 16 heads, 2051 keys
+    ("padded2051_s64k", 520, {}, "peaked"),
+    ("tiny_fwd_s1k", 300, dict(K_p=16), "pages"),   # 8 heads, d = 128
+    ("tiny_fwd_s1k", 300, dict(K_p=16), "unit"),
+    ("glm_s16k", 4096, {}, "pages"),                # sampled rows
+    ("glm_s16k", 4096, {}, "unit"),
 ])
-def test_attn_kv_aliased_matches_oracle(name, S, over):
+def test_attn_kv_aliased_matches_oracle(name, S, over, scale):
     """K = V = one tensor: forward as with v = k, backward dkv = dK + dV."""
-    wl, q, k, _, dO, idx = _attn_case(name, S, 23, **over)
+    wl, q, k, _, dO, idx = _attn_case(name, S, 23, scale, **over)
     cfg = _cfg(wl)
     qd, kd, dOd, idd = (x.to(DEV) for x in (q, k, dO, idx))
     wsf = dsa.workspace(cfg, dsa.WS_FWD, DEV)
@@ -354,15 +380,20 @@ def test_attn_kv_aliased_matches_oracle(name, S, over):
     o2, lse2 = dsa.sparse_attn_fwd(cfg, qd, kd, kd, idd)
     assert torch.equal(o, o2) and torch.equal(lse, lse2)
     wsb = dsa.workspace(cfg, dsa.WS_BWD, DEV)
+    qb, kb, dOb, idx_h = bits(q), bits(k), bits(dO), idx.numpy()
     if S <= 700:
         dq, dkv = dsa.sparse_attn_bwd_kv(cfg, qd, kd, o, lse, dOd, idd, ws=wsb)
         _status_ok(wsb)
-        rdq, rdk, rdv = oracle.attn_bwd(bits(q), bits(k), bits(k), bits(dO),
-                                        idx.numpy(), wl.K_p, wl.n_loc, cfg.scale)
-        _, _, mdv = oracle.attn_bwd(bits(q), bits(k), bits(k), abs_bits(bits(dO)),
-                                    idx.numpy(), wl.K_p, wl.n_loc, cfg.scale)
-        assert_close(f64(dq), rdq, "dq")
-        assert_close(f64(dkv), rdk + rdv, "dkv", mag=np.abs(rdk) + np.abs(mdv))
+        allr = np.arange(S)
+        rdq, rdk, rdv = oracle_attn_bwd(qb, kb, kb, dOb, idx_h, wl.K_p, wl.n_loc,
+                                        cfg.scale, allr)
+        _, _, mdv = oracle_attn_bwd(qb, kb, kb, abs_bits(dOb), idx_h, wl.K_p,
+                                    wl.n_loc, cfg.scale, allr)
+        assert_close(f64(dq), rdq, "dq", **tol(scale))
+        assert_close(f64(dkv), rdk + rdv, "dkv", mag=np.abs(rdk) + np.abs(mdv),
+                     **tol(scale))
+        if scale != "pages":
+            _check_dk_half(f64(dkv), rdk, rdv, mdv, "dkv - dV", scale)
         return
     rows = synth.sample_rows(wl, 24, 5).numpy()
     rt = torch.from_numpy(rows).to(DEV)
@@ -370,21 +401,25 @@ def test_attn_kv_aliased_matches_oracle(name, S, over):
     dOz[rt] = dOd[rt]
     dq, dkv = dsa.sparse_attn_bwd_kv(cfg, qd, kd, o, lse, dOz, idd, ws=wsb)
     _status_ok(wsb)
-    idx_h = idx.numpy()
     keys = np.array(sorted({int(s_) for t in rows for s_ in
                             oracle.key_set(int(t), wl.K_p, wl.n_loc, idx_h[t])}),
                     np.int64)
-    rdq, rdk, rdv = oracle.attn_bwd(bits(q)[rows], bits(k), bits(k), bits(dO)[rows],
-                                    idx_h, wl.K_p, wl.n_loc, cfg.scale, rows, keys)
-    assert_close(f64(dq[rt]), rdq, "dq")
+    rdq, rdk, rdv = oracle_attn_bwd(qb[rows], kb, kb, dOb[rows], idx_h, wl.K_p,
+                                    wl.n_loc, cfg.scale, rows, keys)
+    assert_close(f64(dq[rt]), rdq, "dq", **tol(scale))
     kt = torch.from_numpy(keys).to(DEV)
-    assert_close(f64(dkv[kt]), rdk + rdv, "dkv")
+    _, _, mdv = oracle_attn_bwd(qb[rows], kb, kb, abs_bits(dOb[rows]), idx_h, wl.K_p,
+                                wl.n_loc, cfg.scale, rows, keys)
+    assert_close(f64(dkv[kt]), rdk + rdv, "dkv", mag=np.abs(rdk) + np.abs(mdv),
+                 **tol(scale))
+    if scale != "pages":
+        _check_dk_half(f64(dkv[kt]), rdk, rdv, mdv, "dkv - dV", scale)
     untouched = torch.ones(wl.S, dtype=torch.bool, device=DEV)
     untouched[kt] = False
     assert not dkv[untouched].any()
 
 
-def _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, rows):
+def _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, rows, scale="pages"):
     """dK/dV are not row-local: rerun the GPU backward with dO zeroed outside
     the sampled rows and compare with the oracle's contributions of those
     rows only, on every token they touch."""
@@ -399,31 +434,39 @@ def _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, rows):
     rdq, rdk, rdv = oracle.attn_bwd(bits(q[rt]), bits(k), bits(v),
                                     bits(dO[rt]), idx_h, wl.K_p, wl.n_loc,
                                     cfg.scale, rows, keys)
-    assert_close(f64(dq[rt]), rdq, "dq")
+    _, _, mdv = oracle.attn_bwd(bits(q[rt]), bits(k), bits(v),
+                                abs_bits(bits(dO[rt])), idx_h, wl.K_p, wl.n_loc,
+                                cfg.scale, rows, keys)
+    assert_close(f64(dq[rt]), rdq, "dq", **tol(scale))
     kt = torch.from_numpy(keys).to(dO.device)
-    assert_close(f64(dk[kt]), rdk, "dk")
-    assert_close(f64(dv[kt]), rdv, "dv")
+    assert_close(f64(dk[kt]), rdk, "dk", **tol(scale))
+    assert_close(f64(dv[kt]), rdv, "dv", mag=mdv, **tol(scale))
     # tokens nobody in `rows` attends get exactly zero
     untouched = torch.ones(wl.S, dtype=torch.bool, device=dO.device)
     untouched[kt] = False
     assert not dk[untouched].any() and not dv[untouched].any()
 
 
-@pytest.mark.parametrize("name,S", [("glm_s16k", 16384),
-                                    ("padded2051_s64k", 16500),
-                                    # several waves of queries per CTA
-                                    ("glm_s16k", 32768)])
-def test_attn_large_sampled_rows(name, S):
-    wl, q, k, v, dO, idx = _attn_case(name, S, 33)
+@pytest.mark.parametrize("name,S,scale", [
+    ("glm_s16k", 16384, "pages"),
+    ("glm_s16k", 16384, "unit"),
+    ("padded2051_s64k", 16500, "pages"),
+    ("padded2051_s64k", 16500, "peaked"),
+    ("glm_s16k", 32768, "pages"),             # several waves of queries per CTA
+])
+def test_attn_large_sampled_rows(name, S, scale):
+    wl, q, k, v, dO, idx = _attn_case(name, S, 33, scale)
     cfg = _cfg(wl)
     qd, kd, vd, dOd, idd = (x.to(DEV) for x in (q, k, v, dO, idx))
     o, lse = dsa.sparse_attn_fwd(cfg, qd, kd, vd, idd)
     rows = synth.sample_rows(wl, 12, 5).numpy()
     ro, rl = oracle.attn_fwd(bits(q)[rows], bits(k), bits(v), idx.numpy(),
                              wl.K_p, wl.n_loc, cfg.scale, rows)
-    assert_close(f64(o)[rows], ro, "o")
+    om, _ = oracle.attn_fwd(bits(q)[rows], bits(k), abs_bits(bits(v)), idx.numpy(),
+                            wl.K_p, wl.n_loc, cfg.scale, rows)
+    assert_close(f64(o)[rows], ro, "o", mag=om, **tol(scale))
     assert_close(f64(lse)[rows], rl, "lse")
-    _masked_dkdv_check(wl, cfg, qd, kd, vd, dOd, idd, o, lse, rows[-6:])
+    _masked_dkdv_check(wl, cfg, qd, kd, vd, dOd, idd, o, lse, rows[-6:], scale)
 
 
 def test_bad_index_is_latched_not_read():
@@ -784,6 +827,23 @@ def test_full_size_configuration_sampled_rows(name, n_index_rows, n_attn_rows):
         assert_close(f64(dq[at]), rdq, "dq")
         dq = None
         _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, arows[-6:])
+        # ---- the same selection with attention inputs of order one, where
+        # O, dq, dK and dV cannot pass as zeros
+        q = k = v = dO = o = lse = None
+        torch.cuda.empty_cache()
+        sq, sk, sv, sg = synth.attention_std(wl, "unit")
+        q = synth.normal_bf16_blocks((S, wl.H, wl.d_qk), sq, 84, DEV, 8192)
+        k = synth.normal_bf16_blocks((S, wl.d_qk), sk, 85, DEV, S)
+        v = synth.normal_bf16_blocks((S, wl.d_v), sv, 86, DEV, S)
+        dO = synth.normal_bf16_blocks((S, wl.H, wl.d_v), sg, 87, DEV, 8192)
+        o, lse = dsa.sparse_attn_fwd(cfg, q, k, v, idx)
+        ro, rl = oracle.attn_fwd(bits(q[at]), bits(k), bits(v), idx_h, wl.K_p, wl.n_loc,
+                                 cfg.scale, arows)
+        om, _ = oracle.attn_fwd(bits(q[at]), bits(k), abs_bits(bits(v)), idx_h, wl.K_p,
+                                wl.n_loc, cfg.scale, arows)
+        assert_close(f64(o[at]), ro, "o (unit inputs)", mag=om, **tol("unit"))
+        assert_close(f64(lse[at]), rl, "lse (unit inputs)")
+        _masked_dkdv_check(wl, cfg, q, k, v, dO, idx, o, lse, arows[-6:], "unit")
     finally:
         q_idx = k_idx = w = q = k = v = dO = idx = o = lse = None
         torch.cuda.empty_cache()
