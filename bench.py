@@ -261,11 +261,10 @@ def run_oracle_sample(wl, data, seconds: float, cores: int):
 
 
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch of
-# each attention kernel at full size, from a single-pass ncu capture of
-# `bench.py --steps 1 --warmup 1 --no-e2e --no-cpu` on glm_chunked_s128k
-# (summary in profiles/attn_tc_s131072_dram.md).  An entry holds only while
-# the kernel's sources hash to the value the capture was taken with; after
-# any change the traffic is reported as null until it is captured again.
+# each attention kernel at full size, from an ncu capture of the bench
+# command on glm_chunked_s128k.  An entry holds only while the kernel's
+# sources hash to the value the capture was taken with; after any change the
+# traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
     "attn_bwd_tc": {"workload": "glm_chunked_s128k", "S": 131072,
                     "bytes": 342.33e9 + 228.21e9,
@@ -405,6 +404,39 @@ class Step:
                                                    self.ws_b)]
 
 
+def index_only(args, wl, dev, seed, base_cfg, rank, dist_on):
+    """Time dsa_index_scores_topk alone (pool + chunked indexer + top-k):
+    inputs of the indexer only, so the whole sequence's selection fits in a
+    small device footprint (about 1.4 GB at S = 131072)."""
+    cfg = dsa.config_for(wl)
+    q_idx, k_idx, w = synth.indexer_inputs(wl, seed, dev)
+    idx = torch.empty((wl.S, wl.K_p), dtype=torch.int32, device=dev)
+    ws = dsa.workspace(cfg, dsa.WS_INDEX, dev)
+    for _ in range(args.warmup):
+        dsa.index_scores_topk(cfg, q_idx, k_idx, w, out=idx, ws=ws)
+    torch.cuda.synchronize()
+    barrier(dist_on)
+    e0, e1 = (torch.cuda.Event(enable_timing=True) for _ in range(2))
+    e0.record()
+    for _ in range(args.steps):
+        dsa.index_scores_topk(cfg, q_idx, k_idx, w, out=idx, ws=ws)
+    e1.record()
+    torch.cuda.synchronize()
+    if dsa.get_device_status(ws):
+        raise SystemExit("device status after the indexer calls")
+    ms = e0.elapsed_time(e1) / args.steps
+    wm = work_model(wl)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "dsa_index_scores_topk ms per call", "value": ms, "unit": "ms",
+            "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
+            "config": dict(base_cfg, passes="index"),
+            "indexer_tflops_whole_call": wm["indexer_flops"] / (ms / 1e3) / 1e12,
+            "peak_allocated_bytes": torch.cuda.max_memory_allocated(dev)}), flush=True)
+    if dist_on:
+        torch.distributed.destroy_process_group()
+
+
 def barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
@@ -432,6 +464,10 @@ def main():
                          "into the indexer")
     ap.add_argument("--kv", default="separate", choices=["separate", "aliased"],
                     help="K and V as two tensors (default) or one (K = V)")
+    ap.add_argument("--passes", default="step", choices=["step", "index"],
+                    help="the whole step (default), or only the chunked indexer "
+                         "+ top-k (a small device footprint for counter captures; "
+                         "prints its own line, not the step metric)")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -457,7 +493,7 @@ def main():
             return
         if args.warmup < 0 or args.steps < 1:
             raise SystemExit("bad steps")
-        cores = max(1, min(16, os.cpu_count() or 1))
+        cores = max(1, os.cpu_count() or 1)
         data = reference_rows_data(wl, 20262, gated=args.pool == "gated", kv=kv)
         per_step = max(2.0, 120.0 / max(1, args.steps + args.warmup))
         vals = []
@@ -489,6 +525,8 @@ def main():
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     seed = 20262 + rank
+    if args.passes == "index":
+        return index_only(args, wl, dev, seed, base_cfg, rank, dist_on)
     inputs = make_inputs(wl, seed, dev, gated=args.pool == "gated")
     step = Step(wl, dev, inputs, kv=kv, streaming=args.select == "streaming")
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
@@ -512,6 +550,7 @@ def main():
         torch.cuda.synchronize()
     barrier(dist_on)
     ms = start.elapsed_time(stop) / args.steps
+    peak_alloc = torch.cuda.max_memory_allocated(dev)
     if any(step.status()):
         raise SystemExit(f"device status after timed steps: {step.status()}")
     t_idx = statistics.mean(e[0].elapsed_time(e[1]) for e in evs)
@@ -538,7 +577,7 @@ def main():
         d2h = sum(t.numel() * t.element_size() for t in host_out)
         e_start = torch.cuda.Event(enable_timing=True)
         e_stop = torch.cuda.Event(enable_timing=True)
-        n_e2e = max(1, min(args.steps, 3))
+        n_e2e = max(10, args.steps)
         # dsa_step_host: query ranges whose copies overlap the kernels (the
         # fused streaming selection has no host-step form: serial copies)
         pipelined = args.select == "chunked"
@@ -638,7 +677,34 @@ def main():
     if wl.backward:
         aux["bwd_gather_gbs"] = wm["bwd_gather_bytes"] / (t_bwd / 1e3) / 1e9
         aux["bwd_tflops"] = wm["bwd_flops"] / (t_bwd / 1e3) / 1e12
+    # the forward against the ceilings it actually faces: its flops at the
+    # sustained tensor peak, and the DRAM bytes it moves (most gathered rows
+    # hit L2, so the gathered bytes at HBM speed are not a ceiling)
+    fwd_flops_ms = wm["fwd_flops"] / (pk["bf16_tflops_sustained"] * 1e12) * 1e3
+    fwd_dram = measured_traffic("attn_fwd_tc", wl, variant)
+    fwd_dram_ms = None if fwd_dram is None else fwd_dram / (pk["hbm_gbs"] * 1e9) * 1e3
+    fwd_bound = max(fwd_flops_ms, fwd_dram_ms or 0.0)
+    aux["fwd_roofline"] = {
+        "flops_at_sustained_peak_ms": fwd_flops_ms,
+        "dram_bytes_at_hbm_ms": fwd_dram_ms,
+        "bound_ms": fwd_bound, "measured_ms": t_fwd, "frac": fwd_bound / t_fwd,
+        "note": "max(flops / sustained bf16 peak, measured DRAM bytes / HBM "
+                "peak); the DRAM term is null when no capture matches the "
+                "kernel's sources"}
 
+    mem = {"workspace_bytes": {
+               "index": dsa.workspace_size(step.cfg, dsa.WS_STREAM if
+                                           args.select == "streaming" else dsa.WS_INDEX),
+               "fwd": dsa.workspace_size(step.cfg, dsa.WS_FWD),
+               "bwd": dsa.workspace_size(step.cfg, dsa.WS_BWD) if wl.backward else 0},
+           "score_chunk_bytes": (0 if args.select == "streaming" else
+                                 min(wl.chunk_q, wl.S) * ((wl.P + 127) // 128 * 128) * 4),
+           "unchunked_scores_bytes": wl.S * wl.P * 4,
+           "peak_allocated_bytes": peak_alloc,
+           "note": "peak_allocated_bytes: torch.cuda.max_memory_allocated over "
+                   "the device-resident steps (inputs, outputs, workspaces); "
+                   "unchunked_scores_bytes: one fp32 score per (query, pool), "
+                   "what scoring every query at once would hold"}
     line = {"metric": METRIC, "value": value, "unit": "tokens/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": ms_max, "higher_is_better": True,
@@ -647,13 +713,14 @@ def main():
             "parallelism": f"replicas{world}",
             "breakdown_ms": parts, "rates": aux,
             "roofline": roof,
+            "memory": mem,
             "clocks": clk.summary(),
             "gpu_launches": launches_per_step(
                 wl, args.select == "streaming", kv) * args.steps,
             "e2e": e2e}
 
     if not args.no_cpu:
-        cores = max(1, min(16, os.cpu_count() or 1))
+        cores = max(1, os.cpu_count() or 1)
         v, rows, used, wall = run_oracle_sample(
             wl, oracle_rows_data(wl, inputs, kv=kv), args.cpu_seconds, cores)
         line["cpu_baseline"] = {

@@ -343,9 +343,10 @@ DSA_API dsa_status_t dsa_step_host(const dsa_config_t* cfg,
  * and caches it; make that first call before any stream capture.  Every
  * call shares the array: calls whose work overlaps on the GPU race, so
  * serialise them (one stream, or events).  The status-word header is
- * cleared at the start of each call; device-side errors latched there are
- * not reported by this entry point.  Results equal dsa_index_scores_topk's.
- * No device memory is allocated by the call. */
+ * cleared at the start of each call; device-side errors that a call's
+ * kernels latch there are read with dsa_static_device_status.  Results
+ * equal dsa_index_scores_topk's.  No device memory is allocated by the
+ * call.  A device ordinal of 64 or more returns DSA_ERR_UNSUPPORTED_SHAPE. */
 #define DSA_STATIC_SCRATCH_BYTES (32u << 20)
 DSA_API dsa_status_t dsa_index_scores_topk_static(const dsa_config_t* cfg,
                                                   const void* q_idx,
@@ -353,6 +354,12 @@ DSA_API dsa_status_t dsa_index_scores_topk_static(const dsa_config_t* cfg,
                                                   const float* w,
                                                   int32_t* topk_idx,
                                                   void* stream);
+
+/* dsa_get_device_status for the array of dsa_index_scores_topk_static on
+ * the current device: synchronise `stream` (the stream of the static calls),
+ * read the status word that their kernels latch into *device_status
+ * (DSA_OK if nothing was latched) and clear it.  Allocates nothing. */
+DSA_API dsa_status_t dsa_static_device_status(void* stream, uint32_t* device_status);
 
 /* Synchronise `stream`, read the workspace status word into *device_status
  * (a dsa_status_t value, DSA_OK if nothing was latched) and clear it. */

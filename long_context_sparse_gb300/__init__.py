@@ -24,7 +24,7 @@ from .synth import Workload
 __all__ = [
     "Config", "DsaError", "config_for", "workspace_size", "workspace",
     "pool_keys", "index_scores", "topk_from_scores", "index_scores_topk",
-    "index_scores_topk_static",
+    "index_scores_topk_static", "static_device_status",
     "sparse_attn_fwd", "sparse_attn_bwd", "get_device_status",
     "status_string", "library_path", "WS_INDEX", "WS_FWD", "WS_BWD",
     "WS_STATUS",
@@ -54,7 +54,7 @@ EXPORTS = [
     "dsa_pool_keys_gated", "dsa_sparse_attn_fwd_kv", "dsa_sparse_attn_bwd_kv",
     "dsa_index_topk_streaming", "dsa_sparse_attn_fwd_range",
     "dsa_sparse_attn_bwd_range", "dsa_accum_to_bf16", "dsa_step",
-    "dsa_step_host", "dsa_check_wait_timeout",
+    "dsa_step_host", "dsa_check_wait_timeout", "dsa_static_device_status",
 ]
 
 
@@ -152,6 +152,7 @@ def _load():
                                     P],
             "dsa_get_device_status": [P, P, ctypes.POINTER(ctypes.c_uint32)],
             "dsa_index_scores_topk_static": [CP, P, P, P, P, P],
+            "dsa_static_device_status": [P, ctypes.POINTER(ctypes.c_uint32)],
             "dsa_index_scores_topk_range": [CP, P, P, P, P, I64, I64, P, P, SZ, P],
             "dsa_pool_keys_gated": [CP, P, P, P, P],
             "dsa_sparse_attn_fwd_kv": [CP, P, P, P, P, P, P, SZ, P],
@@ -685,6 +686,17 @@ def check_wait_timeout(ws: torch.Tensor, timeout_ms: int = 50) -> None:
     _check(_load().dsa_check_wait_timeout(_ptr(ws), ws.numel(), int(timeout_ms),
                                           _stream(ws.device)),
            "dsa_check_wait_timeout")
+
+
+def static_device_status(device=None) -> int:
+    """Synchronise the current stream of `device`, read and clear the status
+    word that index_scores_topk_static's kernels latch."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None \
+        else torch.device(device)
+    v = ctypes.c_uint32(0)
+    _check(_load().dsa_static_device_status(_stream(dev), ctypes.byref(v)),
+           "dsa_static_device_status")
+    return v.value
 
 
 def get_device_status(ws: torch.Tensor) -> int:

@@ -10,11 +10,33 @@
 
 #include <mutex>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "dsa_common.cuh"
 #include "dsa_internal.h"
 
 namespace dsa {
 namespace {
+
+// NVTX range over the launches of one host step (a profiler shows it on the
+// CPU timeline; without a tool attached it costs a call through a null hook).
+// `value` (e.g. a chunk's first query) is attached as the range's payload.
+class NvtxRange {
+ public:
+  NvtxRange(const char* name, int64_t value) {
+    nvtxEventAttributes_t a = {};
+    a.version = NVTX_VERSION;
+    a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+    a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+    a.message.ascii = name;
+    a.payloadType = NVTX_PAYLOAD_TYPE_INT64;
+    a.payload.llValue = value;
+    nvtxRangePushEx(&a);
+  }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 constexpr size_t kHeader = 256;        // status word + padding
 constexpr int64_t kPoolTile = 128;     // score row pitch granularity
@@ -396,6 +418,7 @@ dsa_status_t index_rows(const LaunchCtx& ctx, const dsa_config_t* cfg, const voi
       return st;
   }
   for (int64_t t0 = t_begin; t0 < t_end; t0 += C) {
+    const NvtxRange range("dsa.index_chunk", t0);
     const int64_t rows = (t_end - t0) < C ? (t_end - t0) : C;
     const int64_t p_lim = n_full(t0 + rows - 1);
     if (p_lim > cfg->topk_pools) {  // some row has more pools than K_p: score
@@ -511,6 +534,7 @@ dsa_status_t fwd_rows(const LaunchCtx& ctx, const AttnShape& s, const void* q,
                       float* lse) {
   const int64_t n = s.t_hi - s.t_lo;
   if (n == 0) return DSA_OK;
+  const NvtxRange range("dsa.attn_fwd", s.t_lo);
   CUtensorMap qm;
   dsa_status_t st = encode_2d(&qm, q, (uint64_t)(n * s.H), (uint64_t)s.D,
                               (uint32_t)attn_tc_heads(s.H));
@@ -531,6 +555,7 @@ dsa_status_t bwd_rows(const LaunchCtx& ctx, const AttnShape& s, const void* q,
                       float* dk_acc, float* dv_acc) {
   const int64_t n = s.t_hi - s.t_lo;
   if (n == 0) return DSA_OK;
+  const NvtxRange range("dsa.attn_bwd", s.t_lo);
   cudaError_t e = launch_attn_bwd_delta(ctx, s, static_cast<const __nv_bfloat16*>(o),
                                         static_cast<const __nv_bfloat16*>(dO), delta);
   if (e != cudaSuccess) return cuda_status(e);

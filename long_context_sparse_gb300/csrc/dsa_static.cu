@@ -13,8 +13,9 @@
 // is looked up once per device with cudaGetSymbolAddress (with that device
 // current) and cached.  All calls share the one array and it keeps the last
 // call's contents; the status-word header is cleared on the stream at the
-// start of every call.  Calls whose work overlaps on the GPU race on the
-// array.
+// start of every call, and dsa_static_device_status reads (and clears) what
+// a call's kernels latched there.  Calls whose work overlaps on the GPU race
+// on the array.
 #include <mutex>
 
 #include "dsa_common.cuh"
@@ -29,6 +30,34 @@ static __device__ __align__(256) uint8_t g_static_scratch[DSA_STATIC_SCRATCH_BYT
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
 
+// The array's device address on the current device, looked up once per
+// device (with that device current) and cached.
+dsa_status_t static_scratch_address(void** out) {
+  int dev = 0;
+  const cudaError_t ge = cudaGetDevice(&dev);
+  if (ge != cudaSuccess) {
+    dsa::set_error_detail("cudaGetDevice: %s", cudaGetErrorName(ge));
+    return DSA_ERR_CUDA;
+  }
+  if (dev < 0 || dev >= kMaxDevices) {
+    dsa::set_error_detail("device ordinal %d: the static scratch serves ordinals below %d",
+                          dev, kMaxDevices);
+    return DSA_ERR_UNSUPPORTED_SHAPE;
+  }
+  std::lock_guard<std::mutex> lk(g_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || !p) {
+      dsa::set_error_detail("cudaGetSymbolAddress: %s", cudaGetErrorName(e));
+      return DSA_ERR_CUDA;
+    }
+    g_scratch_addr[dev] = p;
+  }
+  *out = g_scratch_addr[dev];
+  return DSA_OK;
+}
+
 }  // namespace
 
 extern "C" DSA_API dsa_status_t dsa_index_scores_topk_static(
@@ -39,25 +68,19 @@ extern "C" DSA_API dsa_status_t dsa_index_scores_topk_static(
   if (st != DSA_OK) return st;
   if (need > DSA_STATIC_SCRATCH_BYTES) return DSA_ERR_WORKSPACE_TOO_SMALL;
   if (!q_idx || !k_idx || !w || !topk_idx) return DSA_ERR_INVALID_ARG;
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
-    return DSA_ERR_CUDA;
   void* scratch = nullptr;
-  {
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_addr[dev]) {
-      void* p = nullptr;
-      const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
-      if (e != cudaSuccess || !p) {
-        dsa::set_error_detail("cudaGetSymbolAddress: %s", cudaGetErrorName(e));
-        return DSA_ERR_CUDA;
-      }
-      g_scratch_addr[dev] = p;
-    }
-    scratch = g_scratch_addr[dev];
-  }
+  if ((st = static_scratch_address(&scratch)) != DSA_OK) return st;
   st = dsa_workspace_init(scratch, DSA_STATIC_SCRATCH_BYTES, stream);
   if (st != DSA_OK) return st;
   return dsa_index_scores_topk(cfg, q_idx, k_idx, w, topk_idx, scratch,
                                DSA_STATIC_SCRATCH_BYTES, stream);
+}
+
+extern "C" DSA_API dsa_status_t dsa_static_device_status(void* stream,
+                                                         uint32_t* device_status) {
+  if (!device_status) return DSA_ERR_INVALID_ARG;
+  void* scratch = nullptr;
+  const dsa_status_t st = static_scratch_address(&scratch);
+  if (st != DSA_OK) return st;
+  return dsa_get_device_status(scratch, stream, device_status);
 }

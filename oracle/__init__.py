@@ -63,8 +63,6 @@ def _load():
             lib.oracle_pool.argtypes = [_i64, _i32, _p, _p]
             lib.oracle_pool_gated.restype = None
             lib.oracle_pool_gated.argtypes = [_i64, _i32, _p, _p, _p]
-            lib.oracle_pool_f64.restype = None
-            lib.oracle_pool_f64.argtypes = [_i64, _i32, _p, _p]
             lib.oracle_index_scores.restype = None
             lib.oracle_index_scores.argtypes = [_i64, _i32, _i32, _p, _p, _p,
                                                 _i64, _p, _p]
@@ -145,14 +143,6 @@ def pool_gated(k_idx: np.ndarray, gate: np.ndarray) -> np.ndarray:
     assert g.shape == (S,)
     out = np.empty((S // 4, D), np.uint16)
     _load().oracle_pool_gated(S, D, _ptr(k), _ptr(g), _ptr(out))
-    return out
-
-
-def pool_f64(k_idx: np.ndarray) -> np.ndarray:
-    k = _c(k_idx, np.uint16)
-    S, D = k.shape
-    out = np.empty((S // 4, D), np.float64)
-    _load().oracle_pool_f64(S, D, _ptr(k), _ptr(out))
     return out
 
 

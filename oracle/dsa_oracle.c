@@ -121,18 +121,6 @@ void oracle_pool_gated(int64_t S, int32_t D_I, const uint16_t* k_idx,
   }
 }
 
-/* fp64 pooling, for information (not bit-matched by anything). */
-void oracle_pool_f64(int64_t S, int32_t D_I, const uint16_t* k_idx,
-                     double* k_pool) {
-  int64_t P = S / 4;
-  for (int64_t p = 0; p < P; ++p)
-    for (int32_t d = 0; d < D_I; ++d) {
-      double s = 0.0;
-      for (int j = 0; j < 4; ++j) s += bf(k_idx[(4 * p + j) * D_I + d]);
-      k_pool[p * D_I + d] = s / 4.0;
-    }
-}
-
 /* ------------------------------------------------------- indexer (a2,a3) */
 
 /* Scores of the listed query rows against every pool, fp64.

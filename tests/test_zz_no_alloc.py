@@ -41,6 +41,11 @@ def test_static_scratch_matches_workspace_entry_point_twice():
             assert _call(lib, cfg, q_idx, k_idx, w, out) == 0
             torch.cuda.synchronize()
             assert torch.equal(out, ref)    # indices: bit-exact
+            st = ctypes.c_uint32(99)        # nothing latched by the kernels
+            assert lib.dsa_static_device_status(
+                ctypes.c_void_p(torch.cuda.current_stream(DEV).cuda_stream),
+                ctypes.byref(st)) == 0
+            assert st.value == 0
 
 
 def test_static_scratch_rejects_problems_beyond_its_size():
