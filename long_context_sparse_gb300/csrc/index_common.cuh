@@ -43,4 +43,55 @@ __device__ __forceinline__ void fma2(float& a0, float& a1, float w0, float w1,
       : "f"(w0), "f"(w1), "f"(x0), "f"(x1));
 }
 
+// The indexer's epilogue for one pool (this thread's TMEM lane) over one
+// half of an N tile: 128 fp32 accumulator columns = 128 / HI queries x HI
+// heads, starting at TMEM address `taddr`.  For each query it forms
+//   I = sum_h w_h * max(0, x_h)
+// in fp32: head pair j of a query (columns 2j, 2j+1) is added with one
+// packed FMA into accumulator pair j % NA (NA = min(4, HI / 2) independent
+// chains), and the 2 NA partial sums are combined as a balanced tree;
+// emit(qi, I) receives query qi of the half (a compile-time constant after
+// unrolling).  wr holds the half's 128 weights.  The TMEM load of the next
+// 16 columns is issued before the current 16 are used.  Every kernel that
+// scores pools calls this, so their scores agree bit for bit.
+template <int HI, class Emit>
+__device__ __forceinline__ void relu_weighted_sums(uint32_t taddr, const float (&wr)[128],
+                                                   Emit emit) {
+  static_assert(HI >= 2 && HI <= 128 && (HI & (HI - 1)) == 0, "heads per query");
+  constexpr int NPQ = HI / 2;              // head pairs per query
+  constexpr int NA = NPQ < 4 ? NPQ : 4;    // accumulator pairs
+  float acc[2 * NA];
+  uint32_t buf[2][16];
+  tmem_ld16(taddr, buf[0]);
+  tmem_wait_ld_dep(buf[0]);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {            // 16-column groups
+    if (g + 1 < 8) tmem_ld16(taddr + (uint32_t)((g + 1) * 16), buf[(g + 1) & 1]);
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+      const int col = g * 16 + j;          // column within the half
+      const int pq = (col % HI) / 2;       // head pair within the query
+      const int ai = pq % NA;
+      const float x0 = fmaxf(__uint_as_float(buf[g & 1][j]), 0.f);
+      const float x1 = fmaxf(__uint_as_float(buf[g & 1][j + 1]), 0.f);
+      if (pq < NA) {                       // first pair of this chain
+        acc[2 * ai] = 0.f;
+        acc[2 * ai + 1] = 0.f;
+      }
+      fma2(acc[2 * ai], acc[2 * ai + 1], wr[col], wr[col + 1], x0, x1);
+      if (pq == NPQ - 1) {                 // last pair of the query
+        float s[2 * NA];
+#pragma unroll
+        for (int e = 0; e < 2 * NA; ++e) s[e] = acc[e];
+#pragma unroll
+        for (int w = 1; w < 2 * NA; w *= 2)
+#pragma unroll
+          for (int e = 0; e < 2 * NA; e += 2 * w) s[e] = s[e] + s[e + w];
+        emit(col / HI, s[0]);
+      }
+    }
+    if (g + 1 < 8) tmem_wait_ld_dep(buf[(g + 1) & 1]);
+  }
+}
+
 }  // namespace dsa

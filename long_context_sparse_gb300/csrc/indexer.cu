@@ -14,8 +14,9 @@
 //                         B = q_idx rows [256 x D_I], K-major
 //   K = D_I            -> D_I/16 tcgen05.mma (kind::f16, bf16 -> fp32)
 // Each epilogue thread owns one pool (one TMEM lane) and half of the tile's
-// columns: ReLU, times w[t,h], summed over heads in fp32 (four independent
-// partial sums, packed fp32x2 FMAs), then one coalesced store per query.
+// columns: ReLU, times w[t,h], summed over heads in fp32 (up to four
+// independent chains of packed fp32x2 FMAs, the TMEM load of the next 16
+// columns in flight), then one coalesced store per query.
 // No cross-lane traffic; the 128 weights of a thread's columns stay in
 // registers for all tiles of an N tile (read from shared memory per tile
 // they took as much shared-memory bandwidth as the MMA operands).
@@ -220,34 +221,27 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool p_ok = p < p_lim;
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) +
                              (uint32_t)(a * kBN + half * (kBN / 2));
-      // four partial sums (two packed pairs) per query
-      float acc[4] = {0.f, 0.f, 0.f, 0.f};
+      // the half's queries: rows q_half + 0 .. 128/HI - 1 of the chunk
+      const int64_t q_half = nt * QT + (int64_t)half * (kBN / 2 / HI);
+      float* const sp = scores + q_half * ld + p;
+      if constexpr (HI == 1) {  // one column per query
 #pragma unroll
-      for (int c = 0; c < kBN / 64; ++c) {
-        uint32_t r0[16], r1[16];
-        tmem_ld16(taddr + c * 32, r0);
-        tmem_ld16(taddr + c * 32 + 16, r1);
-        tmem_wait_ld();
+        for (int c = 0; c < kBN / 64; ++c) {
+          uint32_t r0[16], r1[16];
+          tmem_ld16(taddr + c * 32, r0);
+          tmem_ld16(taddr + c * 32 + 16, r1);
+          tmem_wait_ld();
 #pragma unroll
-        for (int j = 0; j < 32; j += 2) {
-          const int col = half * (kBN / 2) + c * 32 + j;
-          const float x0 = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
-          const float x1 = __uint_as_float(j < 16 ? r0[j + 1] : r1[j - 15]);
-          const int pr = (j >> 1) & 1;
-          fma2(acc[2 * pr], acc[2 * pr + 1], wr[c * 32 + j], wr[c * 32 + j + 1],
-               fmaxf(x0, 0.f), fmaxf(x1, 0.f));
-          if (HI == 1) {  // two queries in the pair
-            const int64_t q0 = nt * QT + col;
-            if (p_ok && q0 < rows) scores[q0 * ld + p] = acc[2 * pr];
-            if (p_ok && q0 + 1 < rows) scores[(q0 + 1) * ld + p] = acc[2 * pr + 1];
-            acc[2 * pr] = acc[2 * pr + 1] = 0.f;
-          } else if ((col + 1) % HI == HI - 1) {
-            const int64_t qrow = nt * QT + col / HI;
-            if (p_ok && qrow < rows)
-              scores[qrow * ld + p] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-            acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
+          for (int j = 0; j < 32; ++j) {
+            const int qi = c * 32 + j;
+            const float x = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
+            if (p_ok && q_half + qi < rows) sp[qi * ld] = wr[qi] * fmaxf(x, 0.f);
           }
         }
+      } else {
+        relu_weighted_sums<HI>(taddr, wr, [&](int qi, float score) {
+          if (p_ok && q_half + qi < rows) sp[qi * ld] = score;
+        });
       }
       tc_fence_before();
       __syncwarp();

@@ -330,27 +330,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (uint32_t)(a * kBN + half * (kBN / 2));
         // scores of this half's queries, computed exactly as indexer.cu does
         float sc[QH];
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int c = 0; c < kBN / 64; ++c) {
-          uint32_t r0[16], r1[16];
-          tmem_ld16(taddr + c * 32, r0);
-          tmem_ld16(taddr + c * 32 + 16, r1);
-          tmem_wait_ld();
-#pragma unroll
-          for (int j = 0; j < 32; j += 2) {
-            const int colh = c * 32 + j;  // column within the half
-            const float x0 = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
-            const float x1 = __uint_as_float(j < 16 ? r0[j + 1] : r1[j - 15]);
-            const int pr = (j >> 1) & 1;
-            fma2(acc[2 * pr], acc[2 * pr + 1], wr[colh], wr[colh + 1], fmaxf(x0, 0.f),
-                 fmaxf(x1, 0.f));
-            if ((colh + 1) % HI == HI - 1) {
-              sc[colh / HI] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
-              acc[0] = acc[1] = acc[2] = acc[3] = 0.f;
-            }
-          }
-        }
+        relu_weighted_sums<HI>(taddr, wr, [&](int qi, float score) { sc[qi] = score; });
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_empty(a));
