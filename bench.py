@@ -222,7 +222,7 @@ def oracle_rows_data(wl, inputs, n_rows=256, seed=99, kv=False):
         out["k_gate"] = _np(inputs["k_gate"])
     if kv:
         out["v"] = out["k"]
-    for k in ("q_idx", "w", "q", "dO"):
+    for k in ("q_idx", "w", "q") + (("dO",) if wl.backward else ()):
         out[k] = _np(inputs[k][rt])
     return out
 
@@ -285,12 +285,17 @@ def measured_traffic(kernel, wl, variant=""):
     e = MEASURED_TRAFFIC.get(kernel)
     if e is None or variant or e["workload"] != wl.name or e["S"] != wl.S:
         return None
+    return e["bytes"] if sources_hash(e["sources"]) == e["sha256_16"] else None
+
+
+def sources_hash(sources):
+    """First 16 hex digits of the sha256 of the kernel sources, in order."""
     h = hashlib.sha256()
-    for f in e["sources"]:
+    for f in sources:
         with open(os.path.join(ROOT, "long_context_sparse_gb300", "csrc", f),
                   "rb") as fh:
             h.update(fh.read())
-    return e["bytes"] if h.hexdigest()[:16] == e["sha256_16"] else None
+    return h.hexdigest()[:16]
 
 
 def peaks():
@@ -301,10 +306,33 @@ def peaks():
     return FALLBACK_PEAKS, "fallback"
 
 
-def make_inputs(wl, seed, device, gated=False):
-    q_idx, k_idx, w = synth.indexer_inputs(wl, seed, device)
-    q, k, v, dO = synth.attention_inputs(wl, seed, device)
-    x = {"q_idx": q_idx, "k_idx": k_idx, "w": w, "q": q, "k": k, "v": v, "dO": dO}
+def make_inputs(wl, seed, device, gated=False, attention=True):
+    """The workload's inputs on `device`.  Up to S = 131072 they come from
+    synth.indexer_inputs / attention_inputs; beyond, the same distributions
+    are drawn in row blocks (no fp32 temporary of a whole tensor)."""
+    if wl.S <= 131072:
+        q_idx, k_idx, w = synth.indexer_inputs(wl, seed, device)
+        x = {"q_idx": q_idx, "k_idx": k_idx, "w": w}
+        if attention:
+            q, k, v, dO = synth.attention_inputs(wl, seed, device)
+            x.update(q=q, k=k, v=v, dO=dO)
+    else:
+        S, blk = wl.S, 8192
+        x = {"q_idx": synth.normal_bf16_blocks((S, wl.H_I, wl.D_I), 1 / math.sqrt(wl.D_I),
+                                               seed, device, 65536),
+             "k_idx": synth.normal_bf16_blocks((S, wl.D_I), 1 / math.sqrt(wl.D_I),
+                                               seed + 1, device, S),
+             "w": torch.softmax(torch.randn((S, wl.H_I), generator=synth._gen(seed + 2, device),
+                                            device=device), dim=-1).contiguous()}
+        if attention:
+            sq, sk, sv, sg = synth.attention_std(wl)
+            x["q"] = synth.normal_bf16_blocks((S, wl.H, wl.d_qk), sq, seed + 3, device, blk)
+            x["k"] = synth.normal_bf16_blocks((S, wl.d_qk), sk, seed + 4, device, S)
+            x["v"] = synth.normal_bf16_blocks((S, wl.d_v), sv, seed + 5, device, S)
+            if wl.backward:
+                x["dO"] = synth.normal_bf16_blocks((S, wl.H, wl.d_v), sg, seed + 6, device, blk)
+    if attention and not wl.backward:
+        x.pop("dO", None)
     if gated:
         x["k_gate"] = synth.gate_inputs(wl, seed, device)
     return x
@@ -349,12 +377,13 @@ class Step:
         self.idx = torch.empty((S, wl.K_p), dtype=torch.int32, device=dev)
         self.o = torch.empty((S, H, wl.d_v), dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty((S, H), dtype=torch.float32, device=dev)
-        self.dq = torch.empty((S, H, wl.d_qk), dtype=torch.bfloat16, device=dev)
-        self.dk = torch.empty((S, wl.d_qk), dtype=torch.bfloat16, device=dev)
-        self.dv = torch.empty((S, wl.d_v), dtype=torch.bfloat16, device=dev)
         self.ws_i = dsa.workspace(self.cfg, dsa.WS_INDEX, dev)
         self.ws_f = dsa.workspace(self.cfg, dsa.WS_FWD, dev)
-        self.ws_b = dsa.workspace(self.cfg, dsa.WS_BWD, dev)
+        if wl.backward:
+            self.dq = torch.empty((S, H, wl.d_qk), dtype=torch.bfloat16, device=dev)
+            self.dk = torch.empty((S, wl.d_qk), dtype=torch.bfloat16, device=dev)
+            self.dv = torch.empty((S, wl.d_v), dtype=torch.bfloat16, device=dev)
+            self.ws_b = dsa.workspace(self.cfg, dsa.WS_BWD, dev)
         if streaming:
             self.ws_i = dsa.workspace(self.cfg, dsa.WS_STREAM, dev)
 
@@ -400,8 +429,8 @@ class Step:
         return out
 
     def status(self):
-        return [dsa.get_device_status(w) for w in (self.ws_i, self.ws_f,
-                                                   self.ws_b)]
+        ws = (self.ws_i, self.ws_f) + ((self.ws_b,) if self.wl.backward else ())
+        return [dsa.get_device_status(w) for w in ws]
 
 
 def index_only(args, wl, dev, seed, base_cfg, rank, dist_on):
@@ -409,7 +438,8 @@ def index_only(args, wl, dev, seed, base_cfg, rank, dist_on):
     inputs of the indexer only, so the whole sequence's selection fits in a
     small device footprint (about 1.4 GB at S = 131072)."""
     cfg = dsa.config_for(wl)
-    q_idx, k_idx, w = synth.indexer_inputs(wl, seed, dev)
+    x = make_inputs(wl, seed, dev, attention=False)
+    q_idx, k_idx, w = x["q_idx"], x["k_idx"], x["w"]
     idx = torch.empty((wl.S, wl.K_p), dtype=torch.int32, device=dev)
     ws = dsa.workspace(cfg, dsa.WS_INDEX, dev)
     for _ in range(args.warmup):
@@ -432,7 +462,17 @@ def index_only(args, wl, dev, seed, base_cfg, rank, dist_on):
             "higher_is_better": False, "steps": args.steps, "warmup": args.warmup,
             "config": dict(base_cfg, passes="index"),
             "indexer_tflops_whole_call": wm["indexer_flops"] / (ms / 1e3) / 1e12,
-            "peak_allocated_bytes": torch.cuda.max_memory_allocated(dev)}), flush=True)
+            "memory": {
+                "workspace_bytes": dsa.workspace_size(cfg, dsa.WS_INDEX),
+                "score_chunk_bytes": min(wl.chunk_q, wl.S) * ((wl.P + 127) // 128 * 128) * 4,
+                "unchunked_scores_bytes": wl.S * wl.P * 4,
+                "unchunked_per_head_scores_bytes": wl.S * wl.P * wl.H_I * 4,
+                "peak_allocated_bytes": torch.cuda.max_memory_allocated(dev),
+                "note": "peak_allocated_bytes: torch.cuda.max_memory_allocated over "
+                        "the calls (indexer inputs, selection, workspace); the "
+                        "unchunked figures are what scoring every query at once "
+                        "would hold (one fp32 per (query, pool), and per head)"}}),
+            flush=True)
     if dist_on:
         torch.distributed.destroy_process_group()
 
@@ -564,9 +604,17 @@ def main():
         ms_max = float(tt.item())
     value = world * wl.S / (ms_max / 1000.0)
 
-    # ---- e2e through the public API with pinned host buffers
+    # ---- e2e through the public API with pinned host buffers (up to
+    # S = 131072: beyond, the pinned copies of q and o alone would take a
+    # large part of the host's memory)
     e2e = None
-    if not args.no_e2e:
+    if wl.S > 131072 and not args.no_e2e:
+        e2e = {"value": None, "unit": "tokens/s", "h2d_bytes_per_step": None,
+               "d2h_bytes_per_step": None,
+               "skipped": "host-buffer step not run above S = 131072 (q and o "
+                          "alone would pin %.0f GB of host memory)"
+                          % (2 * wl.S * wl.H * wl.d_qk * 2 / 1e9)}
+    if not args.no_e2e and e2e is None:
         host_in = {k: torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
                    for k, t in inputs.items()}
         for k in host_in:

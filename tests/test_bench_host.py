@@ -51,19 +51,24 @@ def test_launch_count_mirrors_the_chunk_loop():
 
 
 def test_traffic_guard_drops_stale_figures(tmp_path, monkeypatch):
+    """A stored DRAM-traffic figure is reported only for the workload, the
+    default variant and the kernel sources it was captured with."""
     wl = synth.WORKLOADS["glm_chunked_s128k"]
-    for kernel, e in bench.MEASURED_TRAFFIC.items():
-        assert bench.measured_traffic(kernel, wl) == e["bytes"]    # sources as captured
-        assert bench.measured_traffic(kernel, wl, "kv") is None    # another variant
-        assert bench.measured_traffic(kernel, synth.WORKLOADS["glm_s16k"]) is None
-    # a changed kernel source invalidates the figure
     csrc = os.path.join(bench.ROOT, "long_context_sparse_gb300", "csrc")
     fake = tmp_path / "long_context_sparse_gb300" / "csrc"
     fake.mkdir(parents=True)
     for f in ("attn_bwd_tc.cu", "attn_fwd_tc.cu", "attn_common.cuh", "dsa_common.cuh"):
         shutil.copy(os.path.join(csrc, f), fake / f)
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
-    assert bench.measured_traffic("attn_bwd_tc", wl) is not None
+    # the table as if captured on these sources
+    table = {k: dict(e, sha256_16=bench.sources_hash(e["sources"]))
+             for k, e in bench.MEASURED_TRAFFIC.items()}
+    monkeypatch.setattr(bench, "MEASURED_TRAFFIC", table)
+    for kernel, e in table.items():
+        assert bench.measured_traffic(kernel, wl) == e["bytes"]    # sources as captured
+        assert bench.measured_traffic(kernel, wl, "kv") is None    # another variant
+        assert bench.measured_traffic(kernel, synth.WORKLOADS["glm_s16k"]) is None
+    # a changed kernel source invalidates the figure
     with open(fake / "attn_bwd_tc.cu", "a") as fh:
         fh.write("\n// changed\n")
     assert bench.measured_traffic("attn_bwd_tc", wl) is None
