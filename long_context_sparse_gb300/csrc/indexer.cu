@@ -13,19 +13,20 @@
 //   N = 256 columns    -> (query, head) pairs, 256/H_I queries x H_I heads;
 //                         B = q_idx rows [256 x D_I], K-major
 //   K = D_I            -> D_I/16 tcgen05.mma (kind::f16, bf16 -> fp32)
-// Each epilogue thread owns one pool (one TMEM lane) and half of the tile's
-// columns: ReLU, times w[t,h], summed over heads in fp32 (up to four
+// Each epilogue thread owns one pool (one TMEM lane) and a quarter of the
+// tile's columns: ReLU, times w[t,h], summed over heads in fp32 (up to four
 // independent chains of packed fp32x2 FMAs, the TMEM load of the next 16
 // columns in flight), then one coalesced store per query.
-// No cross-lane traffic; the 128 weights of a thread's columns stay in
-// registers for all tiles of an N tile (read from shared memory per tile
-// they took as much shared-memory bandwidth as the MMA operands).
+// No cross-lane traffic.
 //
-// Warp roles (320 threads): warp 0 TMA producer, warp 1 TMEM allocator and
-// MMA issuer, warps 2-9 epilogue (two per TMEM lane quadrant, one per
-// column half).  The epilogue's ALU work per tile is about half the MMA
-// time only when two warps per SM sub-partition hide each other's
-// latencies.  A tiles stream through a 4-stage TMA ring;
+// Warp roles (608 threads): warp 0 TMA producer, warps 1-2 MMA issuers
+// (alternate tiles; warp 1 also allocates TMEM), warps 3-18 epilogue (four
+// per TMEM lane quadrant, one per quarter of the columns).  The epilogue's ALU work per tile fits under the
+// MMA time only when four warps per SM sub-partition hide each other's
+// latencies (with two, the tile took 1.8x its MMA time); the head weights
+// of the N tile sit in shared memory and are read as broadcast 16-byte
+// loads, which leaves the warps' registers for the accumulator values.  A
+// tiles stream through a 4-stage TMA ring;
 // the B tile stays resident while consecutive tiles share it; accumulators
 // are double-buffered in TMEM (2 x 256 columns) so the epilogue of one tile
 // overlaps the MMAs of the next.
@@ -37,8 +38,13 @@ namespace {
 
 constexpr int kBM = 128;  // pools per tile
 constexpr int kBN = 256;  // (query, head) columns per tile
-constexpr int kThreads = 320;
-constexpr int kEpiWarps = 8;
+constexpr int kEpiWarps = 16;            // four per SM sub-partition
+constexpr int kEpiWarp0 = 3;             // warps 0 TMA, 1-2 MMA issuers
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
+constexpr int kEpiCols = kBN / (kEpiWarps / 4);  // columns per epilogue warp
+// registers: the fullest SM sub-partition holds ceil(19 / 4) = 5 warps
+constexpr int kMaxReg = (16384 / (((kThreads / 32) + 3) / 4 * 32)) & ~7;
+static_assert(kMaxReg == 96, "register budget");
 
 template <int DI>
 struct IdxCfg {
@@ -46,7 +52,8 @@ struct IdxCfg {
   static constexpr int kStages = DI == 64 ? 8 : 4;
   static constexpr uint32_t kABytes = kBM * DI * 2;  // one pool tile
   static constexpr uint32_t kBBytes = kBN * DI * 2;  // one query tile
-  static constexpr uint32_t kSmem = kBBytes + kStages * kABytes + 256 + 1024;
+  // + barriers (256) + weights of two N tiles (2 x kBN floats) + alignment
+  static constexpr uint32_t kSmem = kBBytes + kStages * kABytes + 256 + 8 * kBN + 1024;
 };
 
 __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
@@ -59,7 +66,7 @@ __device__ __forceinline__ bool drain_wait(uint32_t bar, uint32_t parity,
 }
 
 template <int HI, int DI>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __maxnreg__(kMaxReg)
     indexer_kernel(const __grid_constant__ CUtensorMap q_map,
                    const __grid_constant__ CUtensorMap k_map,
                    const float* __restrict__ w, int64_t t0, int64_t q0,
@@ -77,6 +84,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t sB = base;
   const uint32_t sA = base + C::kBBytes;
   uint64_t* bars = reinterpret_cast<uint64_t*>(gbase + C::kBBytes + C::kStages * C::kABytes);
+  // head weights of the current and the previous N tile: [2][kBN]
+  float* wsm = reinterpret_cast<float*>(gbase + C::kBBytes + C::kStages * C::kABytes + 256);
   // barrier slots
   const uint32_t bar0 = smem_u32(bars);
   auto a_full = [&](int s) { return bar0 + 8u * s; };
@@ -85,7 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t b_empty = b_full + 8u;
   auto acc_full = [&](int a) { return b_full + 16u + 8u * a; };
   auto acc_empty = [&](int a) { return b_full + 32u + 8u * a; };
-  const uint32_t done_bar = b_full + 48u;
+  const uint32_t done_bar = b_full + 48u;      // [2], one per MMA issuer: slots +48, +72
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(bars + 2 * C::kStages + 7);
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * C::kStages + 8);
 
@@ -94,6 +103,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int64_t beg = (int64_t)blockIdx.x * n_items / gridDim.x;
   const int64_t end = (int64_t)(blockIdx.x + 1) * n_items / gridDim.x;
+  // item = nt * n_ptiles + pt (N tile, pool tile); every role steps the
+  // pair instead of dividing a 64-bit item number per tile (an emulated
+  // division costs several hundred cycles on the epilogue's critical path)
+  const int64_t nt_beg = beg / n_ptiles;
+  const int pt_beg = (int)(beg - nt_beg * n_ptiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::kStages; ++s) {
@@ -101,12 +115,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(a_empty(s), 1);
     }
     mbar_init(b_full, 1);
-    mbar_init(b_empty, 1);
+    mbar_init(b_empty, 2);  // both MMA issuers release each B tile
     for (int a = 0; a < 2; ++a) {
       mbar_init(acc_full(a), 1);
       mbar_init(acc_empty(a), kEpiWarps);
     }
     mbar_init(done_bar, 1);
+    mbar_init(done_bar + 24u, 1);
     *abort_flag = 0u;
     fence_mbar_init();
     prefetch_tensormap(&q_map);
@@ -124,8 +139,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int64_t it = 0;
       int bcount = 0;
       int64_t cur_nt = -1;
-      for (int64_t item = beg; item < end; ++item) {
-        const int64_t nt = item / n_ptiles, pt = item - nt * n_ptiles;
+      int64_t nt = nt_beg;
+      int pt = pt_beg;
+      for (int64_t item = beg; item < end; ++item, pt = pt + 1 == n_ptiles ? 0 : pt + 1,
+                   nt += pt == 0 ? 1 : 0) {
         if (nt != cur_nt) {
           if (!W.wait(b_empty, (bcount & 1) ^ 1)) break;
           mbar_expect_tx(b_full, C::kBBytes);
@@ -153,80 +170,108 @@ __global__ void __launch_bounds__(kThreads, 1)
                    timeout_ns);
       if (bcount > 0) drain_wait(b_full, (uint32_t)(bcount - 1) & 1u, timeout_ns);
     }
-  } else if (warp == 1) {
-    // ------------------------------------------------------- MMA issuer
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------ MMA issuers
+    // Issuer me takes the CTA's tiles k with k % 2 == me into accumulator
+    // me: while one waits on its barriers and commits, the other's MMAs
+    // keep the tensor core busy (one issuer left it idle half the time,
+    // since an MMA issue blocks until the tensor core's short queue takes
+    // it).  Stages and tiles keep their order; only the issuing thread
+    // alternates.
+    const int me = warp - 1;
     if (lane == 0) {
       int64_t it = 0, local = 0;
       int bcount = 0;
       int64_t cur_nt = -1;
-      bool issued = false;
-      for (int64_t item = beg; item < end; ++item) {
-        const int64_t nt = item / n_ptiles;
+      bool issued = false, issued_nt = false;
+      int64_t nt = nt_beg;
+      int pt = pt_beg;
+      bool ok = true;
+      for (int64_t item = beg; item < end; ++item, ++it, pt = pt + 1 == n_ptiles ? 0 : pt + 1,
+                   nt += pt == 0 ? 1 : 0) {
         if (nt != cur_nt) {
-          if (!W.wait(b_full, bcount & 1)) break;
+          if (!(ok = W.wait(b_full, bcount & 1))) break;
           ++bcount;
           cur_nt = nt;
+          issued_nt = false;
         }
-        const int a = (int)(local & 1);
-        const uint32_t v = (uint32_t)(local >> 1);
-        if (!W.wait(acc_empty(a), (v & 1u) ^ 1u)) break;
-        const int s = (int)(it % C::kStages);
-        const uint32_t u = (uint32_t)(it / C::kStages);
-        if (!W.wait(a_full(s), u & 1u)) break;
-        tc_fence_after();
-        const uint32_t d = tmem + (uint32_t)(a * kBN);
-        const uint32_t a_tile = sA + s * C::kABytes;
+        if (((item - beg) & 1) == me) {
+          const uint32_t v = (uint32_t)local;
+          if (!(ok = W.wait(acc_empty(me), (v & 1u) ^ 1u))) break;
+          const int s = (int)(it % C::kStages);
+          const uint32_t u = (uint32_t)(it / C::kStages);
+          if (!(ok = W.wait(a_full(s), u & 1u))) break;
+          tc_fence_after();
+          const uint32_t d = tmem + (uint32_t)(me * kBN);
+          const uint32_t a_tile = sA + s * C::kABytes;
 #pragma unroll
-        for (int ks = 0; ks < DI / 16; ++ks) {
-          const int kb = ks >> 2, kin = ks & 3;
-          const uint64_t ad = sdesc_sw128(a_tile + kb * (kBM * 128) + kin * 32, 16, 1024);
-          const uint64_t bd = sdesc_sw128(sB + kb * (kBN * 128) + kin * 32, 16, 1024);
-          tc_mma(d, ad, bd, IDESC, ks > 0 ? 1u : 0u);
+          for (int ks = 0; ks < DI / 16; ++ks) {
+            const int kb = ks >> 2, kin = ks & 3;
+            const uint64_t ad = sdesc_sw128(a_tile + kb * (kBM * 128) + kin * 32, 16, 1024);
+            const uint64_t bd = sdesc_sw128(sB + kb * (kBN * 128) + kin * 32, 16, 1024);
+            tc_mma(d, ad, bd, IDESC, ks > 0 ? 1u : 0u);
+          }
+          issued = issued_nt = true;
+          tc_commit(a_empty(s));
+          tc_commit(acc_full(me));
+          ++local;
         }
-        issued = true;
-        tc_commit(a_empty(s));
-        tc_commit(acc_full(a));
-        const int64_t next_nt = (item + 1 < end) ? (item + 1) / n_ptiles : -1;
-        if (next_nt != nt) tc_commit(b_empty);
-        ++it;
-        ++local;
+        // last pool tile of this N tile in the CTA's range: this issuer is
+        // done with the B tile (after its MMAs complete, if it issued any)
+        if (pt + 1 == n_ptiles || item + 1 == end) {
+          if (issued_nt) tc_commit(b_empty);
+          else mbar_arrive(b_empty);
+        }
       }
+      (void)ok;
       if (issued) {
-        tc_commit(done_bar);
-        drain_wait(done_bar, 0, timeout_ns);
+        tc_commit(done_bar + 24u * me);
+        drain_wait(done_bar + 24u * me, 0, timeout_ns);
       }
     }
   } else {
     // --------------------------------------------------------- epilogue
+    const int ew = warp - kEpiWarp0;          // epilogue warp 0..15
     const int quad = warp & 3;                // TMEM lane quadrant
-    const int half = (warp - 2) >> 2;         // columns half*128 .. +127
+    const int part = ew >> 2;                 // columns part*kEpiCols .. +kEpiCols-1
     int64_t cur_nt = -1, local = 0;
-    float wr[kBN / 2];  // weights of this half's columns (all lanes alike)
-    for (int64_t item = beg; item < end; ++item) {
-      const int64_t nt = item / n_ptiles, pt = item - nt * n_ptiles;
+    int wbuf = 1;
+    int64_t nt = nt_beg;
+    int pt = pt_beg;
+    for (int64_t item = beg; item < end; ++item, pt = pt + 1 == n_ptiles ? 0 : pt + 1,
+                 nt += pt == 0 ? 1 : 0) {
       if (nt != cur_nt) {
-#pragma unroll
-        for (int j = 0; j < kBN / 2; ++j) {
-          const int col = half * (kBN / 2) + j;
+        // the N tile's weights into the other buffer: every epilogue warp
+        // has finished the tiles of two N tiles ago (previous barrier), so
+        // nobody still reads it
+        wbuf ^= 1;
+        for (int col = ew * 32 + lane; col < kBN; col += 32 * kEpiWarps) {
           const int64_t qrow = nt * QT + col / HI;
-          wr[j] = qrow < rows ? __ldg(w + (t0 - q0 + qrow) * HI + (col % HI)) : 0.f;
+          wsm[wbuf * kBN + col] =
+              qrow < rows ? __ldg(w + (t0 - q0 + qrow) * HI + (col % HI)) : 0.f;
         }
+        named_bar(1, 32 * kEpiWarps);
         cur_nt = nt;
       }
+      const float* wv = wsm + wbuf * kBN + part * kEpiCols;
       const int a = (int)(local & 1);
       const uint32_t v = (uint32_t)(local >> 1);
-      if (!W.wait(acc_full(a), v & 1u)) break;
+      ++local;
+      // after a failed wait (the CTA is aborting, every later wait returns
+      // at once) the warp skips the tile but keeps iterating, so that all
+      // epilogue warps reach the same weight barriers
+      if (!W.wait(acc_full(a), v & 1u)) continue;
       tc_fence_after();
       const int64_t p = pt * kBM + quad * 32 + lane;
       const bool p_ok = p < p_lim;
       const uint32_t taddr = tmem + ((uint32_t)(quad * 32) << 16) +
-                             (uint32_t)(a * kBN + half * (kBN / 2));
-      // the half's queries: rows q_half + 0 .. 128/HI - 1 of the chunk
-      const int64_t q_half = nt * QT + (int64_t)half * (kBN / 2 / HI);
-      float* const sp = scores + q_half * ld + p;
+                             (uint32_t)(a * kBN + part * kEpiCols);
+      // this part's queries: rows q_part + 0 .. kEpiCols/HI - 1 of the chunk
+      const int64_t q_part = nt * QT + (int64_t)part * (kEpiCols / HI);
+      float* const sp = scores + q_part * ld + p;
       if constexpr (HI == 1) {  // one column per query
 #pragma unroll
-        for (int c = 0; c < kBN / 64; ++c) {
+        for (int c = 0; c < kEpiCols / 32; ++c) {
           uint32_t r0[16], r1[16];
           tmem_ld16(taddr + c * 32, r0);
           tmem_ld16(taddr + c * 32 + 16, r1);
@@ -235,18 +280,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 32; ++j) {
             const int qi = c * 32 + j;
             const float x = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
-            if (p_ok && q_half + qi < rows) sp[qi * ld] = wr[qi] * fmaxf(x, 0.f);
+            if (p_ok && q_part + qi < rows) sp[qi * ld] = wv[qi] * fmaxf(x, 0.f);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acc_empty(a));
       } else {
-        relu_weighted_sums<HI>(taddr, wr, [&](int qi, float score) {
-          if (p_ok && q_half + qi < rows) sp[qi * ld] = score;
-        });
+        // the warp's 64 columns come into registers first and the
+        // accumulator is released before the arithmetic, so the next
+        // tile's MMAs into it need not wait for the epilogue
+        relu_weighted_sums<HI, kEpiCols, true>(
+            taddr, [&](int i) { return reinterpret_cast<const float4*>(wv)[i]; },
+            [&](int qi, float score) {
+              if (p_ok && q_part + qi < rows) sp[qi * ld] = score;
+            },
+            [&] {
+              tc_fence_before();
+              __syncwarp();
+              if (lane == 0) mbar_arrive(acc_empty(a));
+            });
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty(a));
-      ++local;
     }
   }
 

@@ -59,9 +59,6 @@ constexpr uint32_t fused_smem() {
 // They cost a few cycles where an mbarrier round trip costs far more, and
 // they are safe here: the only wait before them that can give up is the
 // accumulator wait, whose outcome the warps first agree on with bar_and.
-__device__ __forceinline__ void named_bar(uint32_t id, uint32_t n) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
-}
 // Barrier that also ANDs one flag over all participating threads.
 __device__ __forceinline__ bool bar_and(uint32_t id, uint32_t n, bool v) {
   uint32_t r;
@@ -301,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int half = ew >> 2;               // columns half*128 .. +127
     const uint32_t lt = (1u << lane) - 1u;
     uint64_t local = 0;
-    float wr[kBN / 2];  // weights of this half's columns (all lanes alike)
+    float2 wr[kBN / 4];  // weights of this half's columns, in pairs (all lanes alike)
     int64_t nt, tq0;
     int n_pt;
     bool ok = true;
@@ -311,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int j = 0; j < kBN / 2; ++j) {
         const int col = half * (kBN / 2) + j;
         const int64_t qr = nt * QT + col / HI;  // row of w
-        wr[j] = col / HI < nq ? __ldg(w + qr * HI + (col % HI)) : 0.f;
+        const float wj = col / HI < nq ? __ldg(w + qr * HI + (col % HI)) : 0.f;
+        if (j & 1) wr[j >> 1].y = wj; else wr[j >> 1].x = wj;
       }
       if (ew < QT && lane == 0) {
         cnt[ew] = 0u;
@@ -330,7 +328,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                (uint32_t)(a * kBN + half * (kBN / 2));
         // scores of this half's queries, computed exactly as indexer.cu does
         float sc[QH];
-        relu_weighted_sums<HI>(taddr, wr, [&](int qi, float score) { sc[qi] = score; });
+        relu_weighted_sums<HI, kBN / 2, false>(
+            taddr,
+            [&](int i) {
+              return make_float4(wr[2 * i].x, wr[2 * i].y, wr[2 * i + 1].x, wr[2 * i + 1].y);
+            },
+            [&](int qi, float score) { sc[qi] = score; }, [] {});
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(acc_empty(a));
