@@ -24,7 +24,7 @@ from .synth import Workload
 __all__ = [
     "Config", "DsaError", "config_for", "workspace_size", "workspace",
     "pool_keys", "index_scores", "topk_from_scores", "index_scores_topk",
-    "index_scores_topk_static", "static_device_status",
+    "index_scores_topk_static", "static_device_status", "host_buffer",
     "sparse_attn_fwd", "sparse_attn_bwd", "get_device_status",
     "status_string", "library_path", "WS_INDEX", "WS_FWD", "WS_BWD",
     "WS_STATUS",
@@ -676,6 +676,55 @@ def step_host(cfg: Config, host: dict, dev: dict, n_chunks: int = 8, ws=None,
         _ptr(ws), ws.numel(), _stream(d), ctypes.c_void_p(hs.cuda_stream),
         ctypes.c_void_p(ds.cuda_stream)), "dsa_step_host")
     return host
+
+
+_HUGE = 2 << 20  # transparent huge page size requested for host buffers
+
+
+def host_buffer(shape, dtype) -> torch.Tensor:
+    """A page-locked host tensor for step_host's copies, backed by 2 MiB
+    transparent huge pages (anonymous mmap + madvise(MADV_HUGEPAGE), then
+    cudaHostRegister), unregistered and unmapped when the tensor is freed.
+
+    On a Grace host the GPU's copies translate every host page.  With the
+    default 64 KiB pages, host-to-device copies from cudaHostAlloc memory
+    were measured to fall from about 200 GB/s to 15-25 GB/s for as long as
+    the host was still releasing memory after another process had touched
+    and freed a large amount (e.g. a test run just before); buffers on huge
+    pages kept 120-130 GB/s under the same conditions, and the same 200 GB/s
+    otherwise."""
+    import weakref
+    numel = 1
+    for x in shape:
+        numel *= int(x)
+    nbytes = numel * torch.empty((), dtype=dtype).element_size()
+    if nbytes == 0:
+        return torch.empty(shape, dtype=dtype, pin_memory=True)
+    libc = ctypes.CDLL("libc.so.6", use_errno=True)
+    libc.mmap.restype = ctypes.c_void_p
+    libc.mmap.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.c_int,
+                          ctypes.c_int, ctypes.c_long]
+    libc.munmap.argtypes = [ctypes.c_void_p, ctypes.c_size_t]
+    libc.madvise.argtypes = [ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int]
+    span = (nbytes + _HUGE - 1) // _HUGE * _HUGE + _HUGE
+    raw = libc.mmap(None, span, 0x1 | 0x2, 0x02 | 0x20, -1, 0)  # RW, private anonymous
+    if raw in (None, ctypes.c_void_p(-1).value):
+        raise MemoryError(f"host_buffer: mmap of {span} bytes failed")
+    base = (raw + _HUGE - 1) // _HUGE * _HUGE
+    libc.madvise(ctypes.c_void_p(base), span - (base - raw), 14)  # MADV_HUGEPAGE (a hint)
+    cudart = torch.cuda.cudart()
+    rc = cudart.cudaHostRegister(base, nbytes, 0)
+    if int(rc) != 0:
+        libc.munmap(ctypes.c_void_p(raw), span)
+        raise DsaError(5, "host_buffer", f"cudaHostRegister returned {rc}")
+    arr = (ctypes.c_uint8 * nbytes).from_address(base)
+
+    def release(raw=raw, span=span, base=base, libc=libc, cudart=cudart):
+        cudart.cudaHostUnregister(base)
+        libc.munmap(ctypes.c_void_p(raw), span)
+    # the buffer object lives as long as any tensor on its memory
+    weakref.finalize(arr, release)
+    return torch.frombuffer(arr, dtype=torch.uint8).view(dtype).view(shape)
 
 
 def check_wait_timeout(ws: torch.Tensor, timeout_ms: int = 50) -> None:

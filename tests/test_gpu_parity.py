@@ -612,6 +612,40 @@ def test_step_equals_separate_calls(S, gated, kv, backward):
     assert torch.equal(dev["dq"], dq)
 
 
+def test_host_buffer_is_page_locked_and_serves_the_host_step():
+    """dsa.host_buffer: a registered (page-locked) host tensor of the asked
+    shape; the host step over such buffers equals the one over cudaHostAlloc
+    buffers."""
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], 2500)
+    cfg = _cfg(wl)
+    shapes = dsa.step_shapes(cfg, False, True, False)
+    inp = _step_tensors(wl, 47)
+    res = []
+    for alloc in ("pin", "huge"):
+        if alloc == "pin":
+            host = {n: t.pin_memory() for n, t in inp.items()}
+            host.update(_step_outputs(cfg, shapes, host, "cpu"))
+        else:
+            host = {}
+            for n, t in inp.items():
+                host[n] = dsa.host_buffer(t.shape, t.dtype)
+                host[n].copy_(t)
+            for n in ("topk_idx", "o", "lse", "dq", "dk", "dv"):
+                shape, dtype = shapes[n]
+                host[n] = dsa.host_buffer(shape, dtype)
+            assert host["q"].is_pinned() and host["dq"].is_pinned()
+            assert host["q"].shape == inp["q"].shape and host["w"].dtype == torch.float32
+        dev = {n: torch.empty(shape, dtype=dtype, device=DEV)
+               for n, (shape, dtype) in shapes.items()}
+        dsa.step_host(cfg, host, dev, 3)
+        torch.cuda.synchronize()
+        res.append({n: host[n].clone() for n in ("topk_idx", "o", "lse", "dq", "dk", "dv")})
+    for n in ("topk_idx", "o", "lse", "dq"):
+        assert torch.equal(res[0][n], res[1][n]), n
+    for n in ("dk", "dv"):      # fp32 additions in another order
+        _close_bf16(res[0][n], res[1][n])
+
+
 @pytest.mark.parametrize("S,n_chunks,gated,kv,backward", [
     (3000, 1, False, False, True),
     (3000, 3, False, False, True),
