@@ -776,8 +776,8 @@ def main():
         line["cpu_baseline"] = {
             "value": v, "unit": "tokens/s", "cores": used, "kind": "oracle",
             "sample": f"{rows} late query rows (last S/8) of the same workload, "
-                      "each through index+top-k+fwd+bwd in fp64, "
-                      f"{wall:.1f} s wall"}
+                      "each through index+top-k+fwd" + ("+bwd" if wl.backward else "") +
+                      f" in fp64, {wall:.1f} s wall"}
     print(json.dumps(line), flush=True)
     if dist_on:
         torch.distributed.destroy_process_group()

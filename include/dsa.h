@@ -64,7 +64,10 @@ typedef enum dsa_status {
   DSA_ERR_CUDA = 5,              /* a CUDA runtime/driver call failed */
   DSA_ERR_DEVICE_TIMEOUT = 6,    /* a kernel's bounded wait ran out */
   DSA_ERR_DEVICE_BAD_INDEX = 7,  /* a kernel read an out-of-range pool index */
-  DSA_ERR_SCRATCH_CAP = 8        /* one score chunk would exceed scratch_cap */
+  DSA_ERR_SCRATCH_CAP = 8,       /* one score chunk would exceed scratch_cap */
+  DSA_ERR_DEVICE_CHECK = 9       /* debug build (DSA_CHECKS) only: a kernel computed an
+                                    out-of-range shared-memory, TMEM or global offset; the
+                                    access was skipped */
 } dsa_status_t;
 
 /* Problem description (one sequence per call; batch = 1).

@@ -31,7 +31,12 @@ __all__ = [
 ]
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-_LIB_PATH = os.path.join(_HERE, "libdsa_gb300.so")
+# DSA_GB300_CHECKS=1 loads the debug build (built by build(checks=True)):
+# every kernel bounds-checks its shared-memory, TMEM and global offsets and
+# latches DSA_ERR_DEVICE_CHECK instead of making the access
+_LIB_PATH = os.path.join(
+    _HERE, "libdsa_gb300_checks.so" if os.environ.get("DSA_GB300_CHECKS") == "1"
+    else "libdsa_gb300.so")
 _lock = threading.Lock()
 _lib = None
 
@@ -41,7 +46,7 @@ STATUS_NAMES = {
     0: "DSA_OK", 1: "DSA_ERR_INVALID_ARG", 2: "DSA_ERR_UNSUPPORTED_SHAPE",
     3: "DSA_ERR_WORKSPACE_TOO_SMALL", 4: "DSA_ERR_MISALIGNED",
     5: "DSA_ERR_CUDA", 6: "DSA_ERR_DEVICE_TIMEOUT",
-    7: "DSA_ERR_DEVICE_BAD_INDEX", 8: "DSA_ERR_SCRATCH_CAP",
+    7: "DSA_ERR_DEVICE_BAD_INDEX", 8: "DSA_ERR_SCRATCH_CAP", 9: "DSA_ERR_DEVICE_CHECK",
 }
 
 # every symbol include/dsa.h declares
@@ -134,8 +139,8 @@ def _load():
         if not os.path.exists(_LIB_PATH):
             raise ImportError(
                 f"CUDA library {_LIB_PATH} is missing; build it with "
-                "`python -m long_context_sparse_gb300.build` (there is no "
-                "CPU fallback)")
+                "`python -m long_context_sparse_gb300.build` (add --checks "
+                "for the debug build; there is no CPU fallback)")
         lib = ctypes.CDLL(_LIB_PATH)
         P, I32, I64, SZ = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
                            ctypes.c_size_t)

@@ -17,6 +17,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa_gb300.so")
+LIB_CHECKS = os.path.join(PKG, "libdsa_gb300_checks.so")
 SOURCES = ["select.cu", "indexer.cu", "indexer_topk.cu", "attn_fwd_tc.cu", "attn_bwd.cu",
            "attn_bwd_tc.cu", "dsa_api.cu",
            "dsa_static.cu"]
@@ -43,8 +44,15 @@ def _stale(target: str, deps) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(force: bool = False, verbose: bool = False) -> str:
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, checks: bool = False) -> str:
+    """Compile the library.  checks=True builds the debug variant
+    (libdsa_gb300_checks.so, -DDSA_CHECKS): the kernels bounds-check their
+    shared-memory, TMEM and global offsets, latch DSA_ERR_DEVICE_CHECK and
+    skip the access."""
+    build_dir = BUILD + ("_checks" if checks else "")
+    lib = LIB_CHECKS if checks else LIB
+    flags = FLAGS + (["-DDSA_CHECKS"] if checks else [])
+    os.makedirs(build_dir, exist_ok=True)
     nvcc = _nvcc()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC)
                if f.endswith((".cuh", ".h"))]
@@ -53,10 +61,10 @@ def build(force: bool = False, verbose: bool = False) -> str:
     objs = []
     for src in SOURCES:
         s = os.path.join(CSRC, src)
-        o = os.path.join(BUILD, src.replace(".cu", ".o"))
+        o = os.path.join(build_dir, src.replace(".cu", ".o"))
         objs.append(o)
         if force or _stale(o, [s] + headers):
-            jobs.append([nvcc] + FLAGS + ["-c", s, "-o", o])
+            jobs.append([nvcc] + flags + ["-c", s, "-o", o])
 
     def run(cmd):
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -69,12 +77,12 @@ def build(force: bool = False, verbose: bool = False) -> str:
         for out in ex.map(run, jobs):
             if verbose and out.strip():
                 print(out)
-    if force or _stale(LIB, objs):
-        tmp = LIB + f".tmp{os.getpid()}"
+    if force or _stale(lib, objs):
+        tmp = lib + f".tmp{os.getpid()}"
         run([nvcc] + ARCH + ["-shared", "-o", tmp] + objs)
-        os.replace(tmp, LIB)
-    return LIB
+        os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose=True))
+    print(build(force="--force" in sys.argv, verbose=True, checks="--checks" in sys.argv))

@@ -366,8 +366,10 @@ __global__ void __maxnreg__(kMaxReg)
                 const int32_t tok = tt[r];
                 const __nv_bfloat16* sp =
                     src + (int64_t)(tok >= 0 ? tok : 0) * D + a * 64 + ch8 * 8;
-                cp_async16(st + r * 128 + ((ch8 ^ (r & 7)) << 4), sp,
-                           tok >= 0 ? 16u : 0u);
+                const uint32_t dst = st + r * 128 + ((ch8 ^ (r & 7)) << 4);
+                if (DSA_IN_BOUNDS(dst - sStage < (uint32_t)(kStages * kStageBytes) && tok <= t,
+                                  status))
+                  cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
               }
             } else {
               // stage a = (dc, kh): keys kh*64 .. +63, dims dc*128 .. +127
@@ -378,8 +380,10 @@ __global__ void __maxnreg__(kMaxReg)
                 const int32_t tok = tt[kh * 64 + r];
                 const __nv_bfloat16* sp = src + (int64_t)(tok >= 0 ? tok : 0) * D +
                                           dc * 128 + blk * 64 + ch8 * 8;
-                cp_async16(st + blk * 8192 + r * 128 + ((ch8 ^ (r & 7)) << 4), sp,
-                           tok >= 0 ? 16u : 0u);
+                const uint32_t dst = st + blk * 8192 + r * 128 + ((ch8 ^ (r & 7)) << 4);
+                if (DSA_IN_BOUNDS(dst - sStage < (uint32_t)(kStages * kStageBytes) && tok <= t,
+                                  status))
+                  cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
               }
             }
             cp_async_mbar_arrive(full(s));
@@ -659,6 +663,9 @@ __global__ void __maxnreg__(kMaxReg)
       const int32_t* pl = pools + buf * (K_p + 8);
       const int32_t* lc = pl + K_p;
       const int ntiles = (n + kTileK - 1) / kTileK;
+#ifdef DSA_CHECKS
+      const int64_t tq = t_hi - 1 - (int64_t)item_s[buf] / n_hblk;  // the query
+#endif
       for (int j = 0; j < ntiles && ok; ++j) {
         const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
         for (int which = 0; which < (KV ? 1 : 2) && ok; ++which) {
@@ -681,13 +688,15 @@ __global__ void __maxnreg__(kMaxReg)
               const int s4 = slot0 + 4 * e4;  // 4 keys of one pool (or locals)
               if (s4 < npool) {
                 const int32_t p = pl[s4 >> 2];
-                if (p >= 0)
+                // the pool's four keys come at or before the query
+                if (p >= 0 && DSA_IN_BOUNDS((int64_t)4 * p + 3 <= tq, status))
                   red_add_pool<D>(dst + (int64_t)(4 * p) * D, cv[4 * e4], cv[4 * e4 + 1],
                                   cv[4 * e4 + 2], cv[4 * e4 + 3]);
               } else {
 #pragma unroll
                 for (int e = 0; e < 4; ++e)
-                  if (s4 + e < n)
+                  if (s4 + e < n &&
+                      DSA_IN_BOUNDS(lc[s4 + e - npool] >= 0 && lc[s4 + e - npool] <= tq, status))
                     red_add_f32(dst + (int64_t)lc[s4 + e - npool] * D, cv[4 * e4 + e]);
               }
             }

@@ -337,7 +337,11 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
               const int32_t tok = tt[r];
               const __nv_bfloat16* sp =
                   src + (int64_t)(tok >= 0 ? tok : 0) * D + c * 128 + c16 * 8;
-              cp_async16(st + r * 128 + ((ch8 ^ (r & 7)) << 4), sp, tok >= 0 ? 16u : 0u);
+              const uint32_t dst = st + r * 128 + ((ch8 ^ (r & 7)) << 4);
+              // inside the ring, and no key after the query
+              if (DSA_IN_BOUNDS(dst - sStage < (uint32_t)(kStages * kStageBytes) && tok <= t,
+                                status))
+                cp_async16(dst, sp, tok >= 0 ? 16u : 0u);
             }
             cp_async_mbar_arrive(full(s));
           }

@@ -290,6 +290,7 @@ const char* dsa_status_string(dsa_status_t s) {
     case DSA_ERR_DEVICE_TIMEOUT: return "DSA_ERR_DEVICE_TIMEOUT";
     case DSA_ERR_DEVICE_BAD_INDEX: return "DSA_ERR_DEVICE_BAD_INDEX";
     case DSA_ERR_SCRATCH_CAP: return "DSA_ERR_SCRATCH_CAP";
+    case DSA_ERR_DEVICE_CHECK: return "DSA_ERR_DEVICE_CHECK";
   }
   return "DSA_ERR_UNKNOWN";
 }

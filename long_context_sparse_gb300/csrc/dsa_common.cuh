@@ -18,6 +18,17 @@ __device__ __forceinline__ void latch_error(uint32_t* status, uint32_t code) {
   if (status) atomicCAS(status, 0u, code);
 }
 
+// Debug builds (-DDSA_CHECKS): DSA_IN_BOUNDS(cond, status) latches
+// DSA_ERR_DEVICE_CHECK and yields false when cond fails, so the caller
+// skips the access (nothing traps); in a normal build it is `true` and the
+// check compiles away.
+#ifdef DSA_CHECKS
+#define DSA_IN_BOUNDS(cond, status) \
+  ((cond) ? true : (::dsa::latch_error((status), DSA_ERR_DEVICE_CHECK), false))
+#else
+#define DSA_IN_BOUNDS(cond, status) true
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

@@ -280,7 +280,8 @@ __global__ void __maxnreg__(kMaxReg)
           for (int j = 0; j < 32; ++j) {
             const int qi = c * 32 + j;
             const float x = __uint_as_float(j < 16 ? r0[j] : r1[j - 16]);
-            if (p_ok && q_part + qi < rows) sp[qi * ld] = wv[qi] * fmaxf(x, 0.f);
+            if (p_ok && q_part + qi < rows && DSA_IN_BOUNDS(p < ld, status))
+              sp[qi * ld] = wv[qi] * fmaxf(x, 0.f);
           }
         }
         tc_fence_before();
@@ -293,7 +294,8 @@ __global__ void __maxnreg__(kMaxReg)
         relu_weighted_sums<HI, kEpiCols, true>(
             taddr, [&](int i) { return reinterpret_cast<const float4*>(wv)[i]; },
             [&](int qi, float score) {
-              if (p_ok && q_part + qi < rows) sp[qi * ld] = score;
+              if (p_ok && q_part + qi < rows && DSA_IN_BOUNDS(p < ld, status))
+                sp[qi * ld] = score;
             },
             [&] {
               tc_fence_before();

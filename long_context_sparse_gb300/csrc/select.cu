@@ -282,7 +282,7 @@ __device__ void ordered_take(KeyAt key_at, int64_t b0, int64_t b1, uint32_t T,
 // the row is selected directly from global memory.
 __global__ void __launch_bounds__(kTopkThreads, 2)
     topk_rows_kernel(const float* __restrict__ scores, int64_t ld, int64_t row0,
-                     int64_t rows, int K_p, int32_t* __restrict__ out) {
+                     int64_t rows, int K_p, int32_t* __restrict__ out, uint32_t* status) {
   __shared__ TopkShared sm;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   uint32_t* my_key = sm.ckey + warp * kSub;
@@ -393,7 +393,7 @@ __global__ void __launch_bounds__(kTopkThreads, 2)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             if (pp4[e]) {
-              if (pos < cap) {
+              if (pos < cap && DSA_IN_BOUNDS(dbase + pos < (uint32_t)kCand, status)) {
                 sm.ckey[dbase + pos] = kk4[e];
                 sm.cidx[dbase + pos] = (int32_t)(i + e);
               }
@@ -464,7 +464,7 @@ cudaError_t launch_topk(const LaunchCtx& c, const float* scores, int64_t ld,
   const int64_t cap = (int64_t)c.num_sms * 2;
   if (grid > cap) grid = cap;
   topk_rows_kernel<<<(unsigned)grid, kTopkThreads, 0, c.stream>>>(scores, ld, row0, rows,
-                                                                  K_p, out);
+                                                                  K_p, out, c.status);
   return cudaGetLastError();
 }
 
