@@ -343,8 +343,7 @@ DSA_API dsa_status_t dsa_step_host(const dsa_config_t* cfg,
  * exits; problems whose DSA_WS_INDEX workspace exceeds it return
  * DSA_ERR_WORKSPACE_TOO_SMALL before anything is launched.  The first call
  * on a device looks up the array's device address (cudaGetSymbolAddress)
- * and caches it; make that first call before any stream capture.  Every
- * call shares the array: calls whose work overlaps on the GPU race, so
+ * and caches it.  Every call shares the array: calls whose work overlaps on the GPU race, so
  * serialise them (one stream, or events).  The status-word header is
  * cleared at the start of each call; device-side errors that a call's
  * kernels latch there are read with dsa_static_device_status.  Results
