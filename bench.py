@@ -267,15 +267,15 @@ def run_oracle_sample(wl, data, seconds: float, cores: int):
 # traffic is reported as null until it is captured again.
 MEASURED_TRAFFIC = {
     "attn_bwd_tc": {"workload": "glm_chunked_s128k", "S": 131072,
-                    "bytes": 342.33e9 + 228.21e9,
+                    "bytes": 343.04e9 + 228.90e9,
                     "sources": ("attn_bwd_tc.cu", "attn_common.cuh",
                                 "dsa_common.cuh"),
-                    "sha256_16": "225888bd77b9bd62"},
+                    "sha256_16": "cd3300051e284773"},
     "attn_fwd_tc": {"workload": "glm_chunked_s128k", "S": 131072,
-                    "bytes": 117.32e9 + 9.59e9,
+                    "bytes": 116.62e9 + 9.59e9,
                     "sources": ("attn_fwd_tc.cu", "attn_common.cuh",
                                 "dsa_common.cuh"),
-                    "sha256_16": "a4431782b6f2b1e7"},
+                    "sha256_16": "34f2ff3ff44815f0"},
 }
 
 
@@ -477,6 +477,43 @@ def index_only(args, wl, dev, seed, base_cfg, rank, dist_on):
         torch.distributed.destroy_process_group()
 
 
+def settle_host_link(dev, limit_s=180.0, target_gbs=120.0):
+    """Host->device copy rate of a page-locked buffer, polled until two
+    polls in a row reach target_gbs or limit_s has passed.
+
+    On the GPU host, right after another process has released a large
+    amount of host memory (the GPU test suite does), host->device copies
+    run at 13-18 GB/s instead of ~210 for minutes; device->host copies are
+    unaffected.  The host step is timed once the link is back (or the limit
+    is reached), and the rates are reported with it.  Each poll copies 256
+    MiB four times back to back and keeps the last rate (the first copy
+    after an idle spell is slow on its own)."""
+    n = 256 << 20
+    hb = dsa.host_buffer((n,), torch.uint8)
+    hb.fill_(1)
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def poll():
+        for _ in range(4):
+            e0.record()
+            d.copy_(hb, non_blocking=True)
+            e1.record()
+            torch.cuda.synchronize()
+        return n / 1e9 / (e0.elapsed_time(e1) / 1e3)
+
+    t0 = time.time()
+    first = last = poll()
+    ok = 1 if last >= target_gbs else 0
+    while ok < 2 and time.time() - t0 < limit_s:
+        time.sleep(0.5)
+        last = poll()
+        ok = ok + 1 if last >= target_gbs else 0
+    del hb, d
+    return {"h2d_gbs_first_poll": round(first, 1), "h2d_gbs_before_timing": round(last, 1),
+            "settle_wait_s": round(time.time() - t0, 1), "target_gbs": target_gbs}
+
+
 def barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
@@ -660,6 +697,7 @@ def main():
         # the kernels run on a stream of their own, as in a training loop;
         # the events are recorded on it
         e2e_stream = torch.cuda.Stream(dev)
+        link = settle_host_link(dev)
         with torch.cuda.stream(e2e_stream):
             one()
             torch.cuda.synchronize()
@@ -669,6 +707,7 @@ def main():
                 one()
             e_stop.record(e2e_stream)
         torch.cuda.synchronize()
+        link["h2d_gbs_after_timing"] = settle_host_link(dev, limit_s=0.0)["h2d_gbs_first_poll"]
         e_ms = e_start.elapsed_time(e_stop) / n_e2e
         if dist_on:
             tt = torch.tensor([e_ms], device=dev)
@@ -676,7 +715,7 @@ def main():
             e_ms = float(tt.item())
         e2e = {"value": world * wl.S / (e_ms / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms,
+               "ms_per_step": e_ms, "host_link": link,
                "path": (f"dsa_step_host, {args.e2e_chunks} query ranges, "
                         "copies overlapped on two side streams, host buffers "
                         "page-locked on 2 MiB pages") if pipelined
