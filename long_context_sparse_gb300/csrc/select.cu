@@ -114,13 +114,14 @@ constexpr int kCand = kSub * kTopkWarps;  // candidate (key, pool) slots of a ro
 constexpr int kSamples = 1024;            // evenly spaced keys that place the cut
 
 // Digit d of the highest bins that holds the kk-th largest key; *above =
-// number of keys in higher bins.  Warp 0 only: lane l first sums the 64
-// bins kBins-64(l+1) .. kBins-64l-1 (lane 0: the top 64), starting at its
-// own offset l so that the 32 lanes read 32 different banks; a warp scan
-// finds the lane whose range holds the kk-th key, then the whole warp scans
-// that range two bins per lane, highest first.
+// number of keys in higher bins, *count = keys in bin d.  Warp 0 only: lane
+// l first sums the 64 bins kBins-64(l+1) .. kBins-64l-1 (lane 0: the top
+// 64), starting at its own offset l so that the 32 lanes read 32 different
+// banks; a warp scan finds the lane whose range holds the kk-th key, then
+// the whole warp scans that range two bins per lane, highest first.
 __device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t kk,
-                                           uint32_t* sel_digit, uint32_t* sel_above) {
+                                           uint32_t* sel_digit, uint32_t* sel_above,
+                                           uint32_t* sel_count) {
   const int lane = threadIdx.x & 31;
   const int base = kBins - 64 * (lane + 1);
   uint32_t s = 0u;
@@ -151,9 +152,11 @@ __device__ __forceinline__ void find_digit(const uint32_t* hist, uint32_t kk,
     if (before + c0 >= kk) {
       *sel_digit = (uint32_t)(top - 2 * lane);
       *sel_above = before;
+      *sel_count = c0;
     } else {
       *sel_digit = (uint32_t)(top - 2 * lane - 1);
       *sel_above = before + c0;
+      *sel_count = c1;
     }
   }
 }
@@ -170,7 +173,7 @@ struct TopkShared {
   uint32_t samp[kSamples];
   uint32_t cnt[kTopkWarps];  // entries of each sub-buffer
   uint32_t wcnt[2][kTopkWarps];
-  uint32_t sel_digit, sel_above;
+  uint32_t sel_digit, sel_above, sel_count;
 };
 
 // The kk-th largest of a set of keys by radix select.  visit(f) calls
@@ -181,6 +184,10 @@ struct TopkShared {
 // (a set of close keys would otherwise pile onto one) and a narrow set
 // takes fewer passes.  *T = that key, *ties = how many keys equal to T rank
 // among the kk largest (ties broken by position).
+//
+// When every key of the chosen bin ranks among the kk largest, no further
+// digit is needed: the kk largest are exactly the keys >= the bin's lower
+// edge, returned as *T = edge - 1 with *ties = 0.
 //
 // With max_passes = 1 the result is only a cut: *T is the lower edge of the
 // first digit's bin that holds the kk-th largest key (at least kk keys are
@@ -209,8 +216,9 @@ __device__ void radix_kth(Visit visit, uint32_t kk, TopkShared& sm, uint32_t* T,
   uint32_t pmask = L == 32 ? 0xffffffffu : ~(0xffffffffu >> L);
   uint32_t prefix = hi & pmask;
   int start = 32 - L;  // bits start-1 .. 0 are still open
+  bool whole_bin = false;
 #pragma unroll 1
-  for (int pass = 0; start > 0 && pass < max_passes; ++pass) {
+  for (int pass = 0; start > 0 && pass < max_passes && !whole_bin; ++pass) {
     const int shift = start > 11 ? start - 11 : 0;
     const uint32_t dmask = (1u << (start - shift)) - 1u;
     for (int i = tid; i < kBins; i += kTopkThreads) sm.hist[i] = 0u;
@@ -219,17 +227,20 @@ __device__ void radix_kth(Visit visit, uint32_t kk, TopkShared& sm, uint32_t* T,
       if ((key & pmask) == prefix) atomicAdd(&sm.hist[(key >> shift) & dmask], 1u);
     });
     __syncthreads();
-    if (warp == 0) find_digit(sm.hist, kk, &sm.sel_digit, &sm.sel_above);
+    if (warp == 0) find_digit(sm.hist, kk, &sm.sel_digit, &sm.sel_above, &sm.sel_count);
     __syncthreads();
     prefix |= sm.sel_digit << shift;
     pmask |= dmask << shift;
     kk -= sm.sel_above;
     start = shift;
+    // (sel_count is rewritten only by the next pass's find_digit, after two
+    // more barriers: every thread reads the same value here)
+    whole_bin = max_passes > 1 && start > 0 && kk == sm.sel_count && (prefix & pmask) != 0u;
   }
   __syncthreads();  // every thread has read the bounds and the digits
   prefix &= pmask;  // (a cut: the bits below the resolved digits are zero)
-  *T = prefix;
-  *ties = kk;
+  *T = whole_bin ? prefix - 1u : prefix;
+  *ties = whole_bin ? 0u : kk;
 }
 
 // Index-ordered selection: keys above T, then the first `ties` keys equal
