@@ -477,41 +477,44 @@ def index_only(args, wl, dev, seed, base_cfg, rank, dist_on):
         torch.distributed.destroy_process_group()
 
 
-def settle_host_link(dev, limit_s=180.0, target_gbs=120.0):
-    """Host->device copy rate of a page-locked buffer, polled until two
-    polls in a row reach target_gbs or limit_s has passed.
+def settle_host_link(h2d, d2h, limit_s=180.0, target_gbs=120.0):
+    """Copy rates of the host step's own largest buffers, polled until two
+    polls in a row reach target_gbs both ways or limit_s has passed.
 
     On the GPU host, right after another process has released a large
-    amount of host memory (the GPU test suite does), host->device copies
-    run at 13-18 GB/s instead of ~210 for minutes; device->host copies are
-    unaffected.  The host step is timed once the link is back (or the limit
-    is reached), and the rates are reported with it.  Each poll copies 256
-    MiB four times back to back and keeps the last rate (the first copy
-    after an idle spell is slow on its own)."""
-    n = 256 << 20
-    hb = dsa.host_buffer((n,), torch.uint8)
-    hb.fill_(1)
-    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    amount of host memory (the GPU test suite does), copies between the
+    device and page-locked host memory can run at 13-18 GB/s instead of
+    ~210 for minutes, for multi-GB buffers while a 256 MiB buffer still
+    copies at full speed.  So the probe copies the step's largest input
+    (h2d = (host, device)) and output (d2h = (device, host)) tensors, each
+    twice back to back, keeping the second rate (the first copy after an
+    idle spell is slow on its own).  The host step is timed once the link
+    is back (or the limit is reached); the rates are reported with it."""
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
 
-    def poll():
-        for _ in range(4):
+    def rate(src, dst):
+        for _ in range(2):
             e0.record()
-            d.copy_(hb, non_blocking=True)
+            dst.copy_(src, non_blocking=True)
             e1.record()
             torch.cuda.synchronize()
-        return n / 1e9 / (e0.elapsed_time(e1) / 1e3)
+        return src.numel() * src.element_size() / 1e9 / (e0.elapsed_time(e1) / 1e3)
+
+    def poll():
+        return rate(*h2d), rate(*d2h)
 
     t0 = time.time()
     first = last = poll()
-    ok = 1 if last >= target_gbs else 0
+    ok = 1 if min(last) >= target_gbs else 0
     while ok < 2 and time.time() - t0 < limit_s:
-        time.sleep(0.5)
         last = poll()
-        ok = ok + 1 if last >= target_gbs else 0
-    del hb, d
-    return {"h2d_gbs_first_poll": round(first, 1), "h2d_gbs_before_timing": round(last, 1),
-            "settle_wait_s": round(time.time() - t0, 1), "target_gbs": target_gbs}
+        ok = ok + 1 if min(last) >= target_gbs else 0
+    return {"h2d_gbs_first_poll": round(first[0], 1), "d2h_gbs_first_poll": round(first[1], 1),
+            "h2d_gbs_before_timing": round(last[0], 1),
+            "d2h_gbs_before_timing": round(last[1], 1),
+            "settle_wait_s": round(time.time() - t0, 1), "target_gbs": target_gbs,
+            "probe_bytes": [h2d[0].numel() * h2d[0].element_size(),
+                            d2h[0].numel() * d2h[0].element_size()]}
 
 
 def barrier(dist_on):
@@ -697,17 +700,28 @@ def main():
         # the kernels run on a stream of their own, as in a training loop;
         # the events are recorded on it
         e2e_stream = torch.cuda.Stream(dev)
-        link = settle_host_link(dev)
+        big_in = max(host_in, key=lambda k: host_in[k].numel() * host_in[k].element_size())
+        big_out = max(range(len(host_out)),
+                      key=lambda i: host_out[i].numel() * host_out[i].element_size())
+        probe = ((host_in[big_in], inputs[big_in]),
+                 (step.outputs()[big_out], host_out[big_out]))
+        link = settle_host_link(*probe)
         with torch.cuda.stream(e2e_stream):
             one()
             torch.cuda.synchronize()
             barrier(dist_on)
             e_start.record(e2e_stream)
+            marks = []
             for _ in range(n_e2e):
                 one()
+                marks.append(torch.cuda.Event(enable_timing=True))
+                marks[-1].record(e2e_stream)
             e_stop.record(e2e_stream)
         torch.cuda.synchronize()
-        link["h2d_gbs_after_timing"] = settle_host_link(dev, limit_s=0.0)["h2d_gbs_first_poll"]
+        step_ms = [round(a.elapsed_time(b), 1) for a, b in zip([e_start] + marks[:-1], marks)]
+        after = settle_host_link(*probe, limit_s=0.0)
+        link["h2d_gbs_after_timing"] = after["h2d_gbs_first_poll"]
+        link["d2h_gbs_after_timing"] = after["d2h_gbs_first_poll"]
         e_ms = e_start.elapsed_time(e_stop) / n_e2e
         if dist_on:
             tt = torch.tensor([e_ms], device=dev)
@@ -715,7 +729,7 @@ def main():
             e_ms = float(tt.item())
         e2e = {"value": world * wl.S / (e_ms / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "ms_per_step": e_ms, "host_link": link,
+               "ms_per_step": e_ms, "step_ms": step_ms, "host_link": link,
                "path": (f"dsa_step_host, {args.e2e_chunks} query ranges, "
                         "copies overlapped on two side streams, host buffers "
                         "page-locked on 2 MiB pages") if pipelined
