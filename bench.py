@@ -517,6 +517,44 @@ def settle_host_link(h2d, d2h, limit_s=180.0, target_gbs=120.0):
                             d2h[0].numel() * d2h[0].element_size()]}
 
 
+def host_link_probe(dev, seconds, rank):
+    """Host<->device copy rates over time, about one sample a second, for 2
+    GiB page-locked buffers of both kinds: cudaHostAlloc (torch's pinned
+    memory) and dsa.host_buffer (2 MiB pages, cudaHostRegister).  Each
+    sample times one copy each way per buffer, after a second of idle (so
+    each first copy also shows the idle effect).  Prints one JSON line."""
+    n = 2 << 30
+    d = torch.empty(n, dtype=torch.uint8, device=dev)
+    bufs = {"pinned": torch.empty(n, dtype=torch.uint8, pin_memory=True),
+            "host_buffer": dsa.host_buffer((n,), torch.uint8)}
+    for b in bufs.values():
+        b.fill_(1)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    samples = []
+    t0 = time.time()
+    while time.time() - t0 < seconds:
+        row = {"t_s": round(time.time() - t0, 1)}
+        for name, hb in bufs.items():
+            for direction in ("h2d", "d2h"):
+                e0.record()
+                if direction == "h2d":
+                    d.copy_(hb, non_blocking=True)
+                else:
+                    hb.copy_(d, non_blocking=True)
+                e1.record()
+                torch.cuda.synchronize()
+                row[f"{name}_{direction}_gbs"] = round(n / 1e9 / (e0.elapsed_time(e1) / 1e3), 1)
+        samples.append(row)
+        time.sleep(1.0)
+    if rank == 0:
+        keys = [k for k in samples[0] if k != "t_s"]
+        print(json.dumps({"metric": "host<->device copy GB/s over time, 2 GiB buffers",
+                          "unit": "GB/s", "buffer_bytes": n,
+                          "median": {k: statistics.median(r[k] for r in samples) for k in keys},
+                          "min": {k: min(r[k] for r in samples) for k in keys},
+                          "samples": samples}), flush=True)
+
+
 def barrier(dist_on):
     if dist_on:
         torch.distributed.barrier()
@@ -544,10 +582,13 @@ def main():
                          "into the indexer")
     ap.add_argument("--kv", default="separate", choices=["separate", "aliased"],
                     help="K and V as two tensors (default) or one (K = V)")
-    ap.add_argument("--passes", default="step", choices=["step", "index"],
+    ap.add_argument("--passes", default="step", choices=["step", "index", "host_link"],
                     help="the whole step (default), or only the chunked indexer "
                          "+ top-k (a small device footprint for counter captures; "
-                         "prints its own line, not the step metric)")
+                         "prints its own line, not the step metric), or the host "
+                         "link's copy rates over time (its own line)")
+    ap.add_argument("--probe-seconds", type=float, default=60.0,
+                    help="--passes host_link: how long to sample")
     args = ap.parse_args()
 
     rank = int(os.environ.get("RANK", "0"))
@@ -607,6 +648,8 @@ def main():
     seed = 20262 + rank
     if args.passes == "index":
         return index_only(args, wl, dev, seed, base_cfg, rank, dist_on)
+    if args.passes == "host_link":
+        return host_link_probe(dev, args.probe_seconds, rank)
     inputs = make_inputs(wl, seed, dev, gated=args.pool == "gated")
     step = Step(wl, dev, inputs, kv=kv, streaming=args.select == "streaming")
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)]
