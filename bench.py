@@ -517,6 +517,56 @@ def settle_host_link(h2d, d2h, limit_s=180.0, target_gbs=120.0):
                             d2h[0].numel() * d2h[0].element_size()]}
 
 
+def buffer_copy_gbs(hb, scratch):
+    """min(host->device, device->host) GB/s of a whole host buffer, copied
+    through a device scratch in scratch-sized pieces (one piece first as a
+    warm-up: the first copy after an idle spell is slow on its own)."""
+    flat = hb.view(-1).view(torch.uint8)
+    n, m = flat.numel(), scratch.numel()
+    scratch[:min(n, m)].copy_(flat[:min(n, m)], non_blocking=True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    rates = []
+    for direction in ("h2d", "d2h"):
+        e0.record()
+        for i in range(0, n, m):
+            j = min(n, i + m)
+            if direction == "h2d":
+                scratch[:j - i].copy_(flat[i:j], non_blocking=True)
+            else:
+                flat[i:j].copy_(scratch[:j - i], non_blocking=True)
+        e1.record()
+        torch.cuda.synchronize()
+        rates.append(n / 1e9 / (e0.elapsed_time(e1) / 1e3))
+    return min(rates)
+
+
+def checked_host_buffer(shape, dtype, scratch, log, min_gbs=150.0, tries=4):
+    """dsa.host_buffer whose copies run at full rate.  On the GPU host some
+    freshly allocated page-locked buffers copy at 15-50 GB/s instead of
+    ~200 GB/s, and stay that slow (measured with both cudaHostAlloc and 2
+    MiB-page buffers, most often right after another process released a
+    lot of memory; a buffer allocated next to a slow one is usually
+    fine).  A buffer of 256 MiB or more is timed both ways once; below
+    min_gbs it is replaced (the slow one is held until a good one is found,
+    so that the host does not hand the same pages back), at most tries - 1
+    times.  log gets (replacements, rate) per checked buffer."""
+    n = 1
+    for x in shape:
+        n *= int(x)
+    if n * torch.empty((), dtype=dtype).element_size() < (256 << 20):
+        log.append(None)
+        return dsa.host_buffer(shape, dtype)
+    held = []
+    for attempt in range(tries):
+        hb = dsa.host_buffer(shape, dtype)
+        r = buffer_copy_gbs(hb, scratch)
+        if r >= min_gbs or attempt == tries - 1:
+            log.append((attempt, round(r, 1)))
+            del held
+            return hb
+        held.append(hb)
+
+
 def host_link_probe(dev, seconds, rank):
     """Host<->device copy rates over time, about one sample a second, for 2
     GiB page-locked buffers of both kinds: cudaHostAlloc (torch's pinned
@@ -698,13 +748,18 @@ def main():
                           "alone would pin %.0f GB of host memory)"
                           % (2 * wl.S * wl.H * wl.d_qk * 2 / 1e9)}
     if not args.no_e2e and e2e is None:
-        # page-locked host buffers on 2 MiB pages (dsa.host_buffer): on this
-        # host, copies from 64 KiB-page pinned memory crawl while the host is
-        # still releasing memory that an earlier process freed
-        host_in = {k: dsa.host_buffer(t.shape, t.dtype) for k, t in inputs.items()}
+        # page-locked host buffers on 2 MiB pages (dsa.host_buffer), each
+        # checked for full-rate copies and replaced if the host gave it
+        # memory that copies crawl from (see checked_host_buffer)
+        scratch = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        checks = []
+        host_in = {k: checked_host_buffer(t.shape, t.dtype, scratch, checks)
+                   for k, t in inputs.items()}
         for k in host_in:
             host_in[k].copy_(inputs[k])
-        host_out = [dsa.host_buffer(t.shape, t.dtype) for t in step.outputs()]
+        host_out = [checked_host_buffer(t.shape, t.dtype, scratch, checks)
+                    for t in step.outputs()]
+        del scratch
         h2d = sum(t.numel() * t.element_size() for t in host_in.values())
         d2h = sum(t.numel() * t.element_size() for t in host_out)
         e_start = torch.cuda.Event(enable_timing=True)
@@ -773,6 +828,11 @@ def main():
         e2e = {"value": world * wl.S / (e_ms / 1000.0), "unit": "tokens/s",
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "ms_per_step": e_ms, "step_ms": step_ms, "host_link": link,
+               "host_buffers": {
+                   "checked": sum(1 for c in checks if c is not None),
+                   "replaced": sum(c[0] for c in checks if c is not None),
+                   "min_gbs_kept": min((c[1] for c in checks if c is not None),
+                                       default=None)},
                "path": (f"dsa_step_host, {args.e2e_chunks} query ranges, "
                         "copies overlapped on two side streams, host buffers "
                         "page-locked on 2 MiB pages") if pipelined

@@ -691,13 +691,13 @@ def host_buffer(shape, dtype) -> torch.Tensor:
     transparent huge pages (anonymous mmap + madvise(MADV_HUGEPAGE), then
     cudaHostRegister), unregistered and unmapped when the tensor is freed.
 
-    On a Grace host the GPU's copies translate every host page.  With the
-    default 64 KiB pages, host-to-device copies from cudaHostAlloc memory
-    were measured to fall from about 200 GB/s to 15-25 GB/s for as long as
-    the host was still releasing memory after another process had touched
-    and freed a large amount (e.g. a test run just before); buffers on huge
-    pages kept 120-130 GB/s under the same conditions, and the same 200 GB/s
-    otherwise."""
+    On a Grace host the GPU's copies translate every host page; huge pages
+    need 32 times fewer translations than the default 64 KiB pages.  After
+    another process had touched and freed a large amount of memory (e.g. a
+    test run just before), copies from some cudaHostAlloc buffers were
+    measured at 15-25 GB/s instead of about 200 GB/s while huge-page
+    buffers kept full rate; at other times a huge-page buffer was slow too.
+    A slow buffer stays slow: time it once and allocate another if needed."""
     import weakref
     numel = 1
     for x in shape:
