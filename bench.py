@@ -543,10 +543,11 @@ def buffer_copy_gbs(hb, scratch):
 def checked_host_buffer(shape, dtype, scratch, log, min_gbs=150.0, tries=4):
     """dsa.host_buffer whose copies run at full rate.  On the GPU host some
     freshly allocated page-locked buffers copy at 15-50 GB/s instead of
-    ~200 GB/s, and stay that slow (measured with both cudaHostAlloc and 2
-    MiB-page buffers, most often right after another process released a
-    lot of memory; a buffer allocated next to a slow one is usually
-    fine).  A buffer of 256 MiB or more is timed both ways once; below
+    ~200 GB/s, and stay that slow for minutes (measured with both
+    cudaHostAlloc and 2 MiB-page buffers, most often right after another
+    process released a lot of memory; a buffer allocated next to a slow
+    one is usually fine; the same host also slows every copy for seconds
+    at a time, which no choice of buffer avoids).  A buffer of 256 MiB or more is timed both ways once; below
     min_gbs it is replaced (the slow one is held until a good one is found,
     so that the host does not hand the same pages back), at most tries - 1
     times.  log gets (replacements, rate) per checked buffer."""
