@@ -94,6 +94,55 @@ def test_topk_bit_exact_on_shared_scores(row0, rows, ld, K):
     np.testing.assert_array_equal(got, ref)
 
 
+def _radix_edge_rows(ld, K, seed):
+    """Rows whose keys around rank K sit in radix bins of every occupancy:
+    keys spread over 40 octaves (mostly alone in their bin, so a bin is
+    taken whole after one or two digits), a cluster of distinct keys
+    2^-12 apart inside one first-digit bin (settled by a later digit), a
+    run of exact ties across rank K (no bin is taken whole: the ties rule),
+    and keys one ulp apart (resolved by the last digit)."""
+    g = np.random.default_rng(seed)
+    base = g.uniform(0.0, 1.0, ld).astype(np.float32)
+    rows = []
+    a = base.copy()
+    pos = g.choice(ld, K + 64, replace=False)
+    a[pos] = np.exp2(g.uniform(-20.0, 20.0, K + 64)).astype(np.float32) + np.float32(1.0)
+    rows.append(a)
+    b = base.copy()
+    pos = g.choice(ld, K + 64, replace=False)
+    b[pos] = np.float32(16.0) + np.arange(K + 64, dtype=np.float32) * np.float32(2.0 ** -12)
+    rows.append(b)
+    c = base.copy()
+    pos = g.choice(ld, K + 40, replace=False)
+    c[pos[:K - 20]] = np.float32(32.0) + g.uniform(0.0, 1.0, K - 20).astype(np.float32)
+    c[pos[K - 20:]] = np.float32(20.0)                 # 60 equal keys across rank K
+    rows.append(c)
+    d = base.copy()
+    pos = g.choice(ld, K + 16, replace=False)
+    ulp = np.float32(np.nextafter(np.float32(24.0), np.float32(25.0)) - np.float32(24.0))
+    d[pos] = np.float32(24.0) + np.arange(K + 16, dtype=np.float32) * ulp
+    rows.append(d)
+    return np.stack(rows).astype(np.float32)
+
+
+@pytest.mark.parametrize("ld,K", [(8192, 512), (4000, 64), (32768, 512), (3000, 2048)])
+def test_topk_bit_exact_where_the_radix_select_stops(ld, K):
+    """The exact selection stops when every key of the chosen bin ranks
+    among the K largest; rows built to stop after the first digit, after
+    the second, or never (ties, last-bit differences) must still give the
+    oracle's selection bit for bit, on the cut path (rows longer than the
+    candidate buffer) and on the whole-row path."""
+    row0 = 4 * ld + 100
+    wl = synth.scaled(synth.WORKLOADS["glm_s16k"], row0 + 8, K_p=K)
+    cfg = _cfg(wl)
+    s = _radix_edge_rows(ld, K, ld + K)
+    rows = np.arange(row0, row0 + s.shape[0])
+    ws = dsa.workspace(cfg, dsa.WS_STATUS, DEV)
+    got = dsa.topk_from_scores(cfg, torch.from_numpy(s).to(DEV), row0, ws=ws).cpu().numpy()
+    _status_ok(ws)
+    np.testing.assert_array_equal(got, oracle.topk(s, rows, K))
+
+
 # --------------------------------------------------------------- indexer
 
 
