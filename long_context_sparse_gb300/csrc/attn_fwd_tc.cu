@@ -74,7 +74,7 @@ struct TcFwdCfg {
   // dynamic shared memory: the selected pool ids (K_p) + 4 local tokens
   static uint32_t smem(int K_p) {
     return 1024 + kQBytes + kPBytes + kStages * kStageBytes + carved((K_p + 4) * 4) +
-           carved(3 * kTileK * 4) + carved(2 * kMaskWords * 4) + carved(4 * NH * 4) +
+           carved(2 * kMaskWords * 4) + carved(4 * NH * 4) +
            3 * carved(NH * 4) + carved(48) + carved(32 * 8);
   }
 };
@@ -130,7 +130,6 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
   uint8_t* tail = gb + C::kQBytes + C::kPBytes + kStages * kStageBytes;
   int32_t* pools = carve<int32_t>(tail, K_p + 4);
   int32_t* locs = pools + K_p;
-  int32_t* tile_tok = carve<int32_t>(tail, 3 * kTileK);       // [3][128]
   uint32_t* vmask = carve<uint32_t>(tail, 2 * kMaskWords);    // [2][words]
   float* red = carve<float>(tail, 4 * NH);                    // [4][NH]
   float* m_s = carve<float>(tail, NH);                        // [NH]
@@ -314,27 +313,40 @@ __global__ void __maxnreg__((TcFwdCfg<D, NH>::kMaxReg))
       const int a16 = c16 >> 3, ch8 = c16 & 7;    // 64-dim atom, 16B chunk
       const int rot = rot_s[buf];
       bool ok = true;
-      // order: K(0), then K(j), V(j-1) for j = 1 .. ntiles-1, then V(last);
-      // token tables rotate over three buffers (tile j is read at steps j
-      // and j+1 and rewritten at j+3, after two more group barriers)
+      // order: K(0), then K(j), V(j-1) for j = 1 .. ntiles-1, then V(last).
+      // Each lane keeps the tokens of its own rows (r = 2g + sub, g = pw +
+      // x * kProdWarps) in registers: those of tile j for K, and the
+      // previous tile's for V, so the producer warps share no table and
+      // need no barrier between tiles (they stay within the ring's reach of
+      // each other through the stage barriers)
+      constexpr int kRowsPerLane = (kTileK / 2 + kProdWarps - 1) / kProdWarps;
+      int32_t tokK[kRowsPerLane], tokV[kRowsPerLane];
+#pragma unroll
+      for (int x = 0; x < kRowsPerLane; ++x) tokK[x] = -1;
       for (int j = 0; j <= ntiles && ok; ++j) {
+#pragma unroll
+        for (int x = 0; x < kRowsPerLane; ++x) tokV[x] = tokK[x];
         if (j < ntiles) {
           const int jr = j + rot < ntiles ? j + rot : j + rot - ntiles;
-          int32_t* tt = tile_tok + (j % 3) * kTileK;
-          for (int r = ptid; r < kTileK; r += kProdThreads) tt[r] = tok_of(jr * kTileK + r);
+#pragma unroll
+          for (int x = 0; x < kRowsPerLane; ++x) {
+            const int g = pw + x * kProdWarps;
+            tokK[x] = g < kTileK / 2 ? tok_of(jr * kTileK + 2 * g + sub) : -1;
+          }
         }
-        if (!(ok = G.sync(W))) break;
         for (int kv = 0; kv < 2 && ok; ++kv) {
           if (kv == 0 ? j == ntiles : j == 0) continue;
           const __nv_bfloat16* src = kv == 0 ? k : v;
-          const int32_t* tt = tile_tok + ((kv == 0 ? j : j - 1) % 3) * kTileK;
           for (int c = 0; c < C::kChunks; ++c, ++u) {
             const int s = (int)(u % kStages);
             if (!(ok = W.wait(empty(s), ((u / kStages) & 1u) ^ 1u))) break;
             const uint32_t st = sStage + s * kStageBytes + a16 * 16384;
-            for (int g = pw; g < kTileK / 2; g += kProdWarps) {
+#pragma unroll
+            for (int x = 0; x < kRowsPerLane; ++x) {
+              const int g = pw + x * kProdWarps;
+              if (g >= kTileK / 2) continue;
               const int r = 2 * g + sub;
-              const int32_t tok = tt[r];
+              const int32_t tok = kv == 0 ? tokK[x] : tokV[x];
               const __nv_bfloat16* sp =
                   src + (int64_t)(tok >= 0 ? tok : 0) * D + c * 128 + c16 * 8;
               const uint32_t dst = st + r * 128 + ((ch8 ^ (r & 7)) << 4);
