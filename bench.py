@@ -570,14 +570,17 @@ def checked_host_buffer(shape, dtype, scratch, log, min_gbs=150.0, tries=4):
 
 def host_link_probe(dev, seconds, rank):
     """Host<->device copy rates over time, about one sample a second, for 2
-    GiB page-locked buffers of both kinds: cudaHostAlloc (torch's pinned
-    memory) and dsa.host_buffer (2 MiB pages, cudaHostRegister).  Each
-    sample times one copy each way per buffer, after a second of idle (so
-    each first copy also shows the idle effect).  Prints one JSON line."""
+    GiB page-locked buffers: cudaHostAlloc (torch's pinned memory),
+    dsa.host_buffer (2 MiB pages, cudaHostRegister), and a cudaHostAlloc
+    buffer that the CPU rewrites before each sample.  Each sample times one
+    copy each way per buffer (host to device first, so the first two
+    buffers are read after the previous sample's device-to-host copy wrote
+    them), after a second of idle.  Prints one JSON line."""
     n = 2 << 30
     d = torch.empty(n, dtype=torch.uint8, device=dev)
     bufs = {"pinned": torch.empty(n, dtype=torch.uint8, pin_memory=True),
-            "host_buffer": dsa.host_buffer((n,), torch.uint8)}
+            "host_buffer": dsa.host_buffer((n,), torch.uint8),
+            "pinned_cpu_written": torch.empty(n, dtype=torch.uint8, pin_memory=True)}
     for b in bufs.values():
         b.fill_(1)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -586,6 +589,8 @@ def host_link_probe(dev, seconds, rank):
     while time.time() - t0 < seconds:
         row = {"t_s": round(time.time() - t0, 1)}
         for name, hb in bufs.items():
+            if name == "pinned_cpu_written":
+                hb.fill_(len(samples) & 255)  # rewritten by the CPU before each sample
             for direction in ("h2d", "d2h"):
                 e0.record()
                 if direction == "h2d":
@@ -756,8 +761,13 @@ def main():
         checks = []
         host_in = {k: checked_host_buffer(t.shape, t.dtype, scratch, checks)
                    for k, t in inputs.items()}
+        # the inputs are written into the host buffers by the CPU, as a data
+        # loader would (on this host, cudaHostAlloc memory last written by a
+        # device-to-host copy was measured copying back to the device at
+        # 8-20 GB/s at times; rewritten by the CPU, at 96-170 GB/s in the
+        # same run)
         for k in host_in:
-            host_in[k].copy_(inputs[k])
+            host_in[k].copy_(inputs[k].cpu())
         host_out = [checked_host_buffer(t.shape, t.dtype, scratch, checks)
                     for t in step.outputs()]
         del scratch
