@@ -122,6 +122,8 @@ def test_bad_pointers_and_sizes_fail_before_launch(lib):
                                    ctypes.c_void_p(4096), ws_bytes, None)
     assert rc == 8
     assert lib.dsa_get_device_status(None, None, None) == 1
+    # the allocation-free entry's status accessor: no output pointer
+    assert lib.dsa_static_device_status(None, None) == 1
 
 
 def test_range_and_step_workspace_sizes(lib):
